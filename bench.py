@@ -1,0 +1,404 @@
+"""Benchmark of the Q4 MoE hot path on one GB300 (or N independent replicas).
+
+One step = one pass of the whole hot path over synthetic inputs resident in HBM:
+  * decode: 40 independently seeded MoE layers (hidden 2048, 256 experts, top-8 + shared,
+    intermediate 512), batch 1, one lily_q4_moe_decode call per layer, back to back;
+  * LM head: lily_q4_gemv_argmax over a 151,936 x 2048 Q4 head;
+  * prefill: one 2048-token chunk through one such layer with skewed router offsets
+    (lily_q4_moe_prefill).
+`value` is decode tokens/s per MoE layer (layers x tokens / decode time).  Weights of the
+40 layers (18.2 GB), the LM head (175 MB) and the prefill layer (455 MB) are each larger
+than L2 (129 MB), so every timed read comes from HBM without an explicit flush.
+
+`--impl reference` times the CPU oracle instead (the same metric on the same workload,
+a bounded sample per step).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "Q4 MoE decode tok/s per layer & HBM GB/s vs peak; prefill chunk TFLOP/s"
+UNIT = "tok/s per layer"
+EXPERT_BYTES = 1769472  # gate + up + down of one expert at H=2048, I=512 (codes + s + b)
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained", d["bf16_tflops"]),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "source": "fallback"}
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--layers", type=int, default=40)
+    ap.add_argument("--tokens", type=int, default=1)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile-small", action="store_true",
+                    help="few layers, no LM head/prefill repeats: for ncu launch lists")
+    return ap.parse_args()
+
+
+def max_over_ranks(values, device=None):
+    """Max of each timing over all ranks (a no-op without an initialised process group)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return [float(v) for v in values]
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t.tolist()]
+
+
+def replica_throughput(units_per_rank, seconds_max, world):
+    """Weak-scaling throughput: units all ranks processed / the slowest rank's time."""
+    return units_per_rank * world / seconds_max
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+class Clocks:
+    """nvidia-smi samples during the timed region."""
+
+    def __init__(self, dev_index: int):
+        self.dev = dev_index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_bench_{os.getpid()}.csv")
+
+    def start(self):
+        q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.dev), f"--query-gpu={q}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# ----------------------------------------------------------------------------- GB300 arm
+
+def run_gb300(args):
+    import torch
+    import torch.distributed as dist
+
+    ws_n, rank, local = dist_env()
+    if ws_n > 1:
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    from bit_affine_quantized_mlx_gb300 import build as q4build
+    q4build.build()
+    import bit_affine_quantized_mlx_gb300 as q4
+    from bit_affine_quantized_mlx_gb300 import synth
+
+    pk = peaks()
+    wl, lmw, pfw = synth.DECODE, synth.LMHEAD, synth.PREFILL
+    T = args.tokens
+    nl = args.layers
+
+    # ---- inputs, resident in HBM before timing
+    t0 = time.time()
+    layers = [q4.DeviceLayer.upload(wl.layer(l), dev) for l in range(nl)]
+    xs = [q4.to_device(synth.draw_tokens(wl.H, T, wl.tokens_key(l)), dev) for l in range(nl)]
+    ys = [torch.empty_like(x) for x in xs]
+    dws = q4.new_workspace(q4.lily_q4_moe_workspace_bytes(layers[0], T), dev)
+    idx_all = torch.empty((nl, T, wl.k), dtype=torch.int32, device=dev)
+    W = q4.DeviceQ4.upload(synth.draw_lm_head(lmw.V, lmw.H), dev)
+    xl = q4.to_device(synth.draw_lm_x(lmw.H), dev)
+    tok = torch.empty(1, dtype=torch.int32, device=dev)
+    lmws = q4.new_workspace(q4.lily_q4_gemv_argmax_workspace_bytes(lmw.V, lmw.H), dev)
+    pl = q4.DeviceLayer.upload(pfw.layer(0), dev)
+    Tp = pfw.tokens[0]
+    xp = q4.to_device(synth.draw_tokens(pfw.H, Tp, pfw.tokens_key(0)), dev)
+    yp = torch.empty_like(xp)
+    idxp = torch.empty((Tp, pfw.k), dtype=torch.int32, device=dev)
+    pws = q4.new_workspace(q4.lily_q4_moe_workspace_bytes(pl, Tp, prefill=True), dev)
+    torch.cuda.synchronize()
+    gen_s = time.time() - t0
+
+    # One CUDA graph per part of the step (captured after a warm-up call of each part, so
+    # one-time library set-up happens outside capture).  Replaying graphs keeps the host
+    # (ctypes per call) off the critical path, as a serving loop would.
+    stream = torch.cuda.Stream(device=dev)
+
+    def dec_part():
+        for l in range(nl):
+            q4.lily_q4_moe_decode(layers[l], xs[l], ys[l], topk_idx=idx_all[l], ws=dws,
+                                  stream=stream)
+
+    def lm_part():
+        q4.lily_q4_gemv_argmax(W, xl, tok, ws=lmws, stream=stream)
+
+    def pf_part():
+        q4.lily_q4_moe_prefill(pl, xp, yp, topk_idx=idxp, ws=pws, stream=stream)
+
+    parts = [dec_part, lm_part, pf_part]
+    with torch.cuda.stream(stream):
+        for f in parts:
+            f()
+    stream.synchronize()
+    graphs = []
+    for f in parts:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            f()
+        graphs.append(g)
+    stream.synchronize()
+
+    def step(ev=None):
+        with torch.cuda.stream(stream):
+            for i, g in enumerate(graphs):
+                if ev:
+                    ev[i].record(stream)
+                g.replay()
+            if ev:
+                ev[3].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if q4.lily_q4_workspace_status(pws, stream) != 0:
+        raise RuntimeError("prefill reported a device-side timeout during warm-up")
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    clocks = Clocks(local)
+    if ws_n > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    g0 = torch.cuda.Event(enable_timing=True)
+    g1 = torch.cuda.Event(enable_timing=True)
+    g0.record(stream)
+    for s_ in range(args.steps):
+        step(evs[s_])
+    g1.record(stream)
+    torch.cuda.synchronize()
+    if ws_n > 1:
+        dist.barrier()
+    clk = clocks.stop()
+    total_ms = g0.elapsed_time(g1)
+    dec_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    lm_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    pf_ms = [e[2].elapsed_time(e[3]) for e in evs]
+    total_ms, dec_mean, lm_mean, pf_mean = max_over_ranks(
+        [total_ms, statistics.mean(dec_ms), statistics.mean(lm_ms), statistics.mean(pf_ms)], dev)
+    if q4.lily_q4_workspace_status(pws, stream) != 0:
+        raise RuntimeError("prefill reported a device-side timeout")
+
+    # ---- algorithmic work
+    idx_h = idx_all.cpu().numpy()
+    uniq = [len(np.unique(idx_h[l])) for l in range(nl)]
+    layer_bytes = [(u + 1) * EXPERT_BYTES + wl.E * wl.H * 2 + wl.H * 2 + 2 * T * wl.H * 2
+                   for u in uniq]
+    bytes_per_layer = statistics.mean(layer_bytes)
+    t_layer_s = dec_mean / 1e3 / nl
+    dec_gbs = bytes_per_layer / t_layer_s / 1e9
+    tok_per_s_layer = replica_throughput(T, t_layer_s, ws_n)
+    lm_bytes = lmw.V * lmw.H // 2 + lmw.V * (lmw.H // 64) * 4 + lmw.H * 2 + 4
+    lm_gbs = lm_bytes / (lm_mean / 1e3) / 1e9
+    P = Tp * (pfw.k + 1)
+    pf_flops = 6.0 * P * pfw.H * pfw.I + 2.0 * Tp * pfw.H * pfw.E
+    pf_tflops = pf_flops / (pf_mean / 1e3) / 1e12
+    pf_bytes = 257 * EXPERT_BYTES + pfw.E * pfw.H * 2 + 2 * Tp * pfw.H * 2
+
+    # ---- end to end through the public API: host x in, host y out, every layer
+    x_host = [torch.empty((T, wl.H), dtype=torch.int16, pin_memory=True) for _ in range(nl)]
+    for l in range(nl):
+        x_host[l].copy_(xs[l].cpu())
+    y_host = [torch.empty((T, wl.H), dtype=torch.int16, pin_memory=True) for _ in range(nl)]
+    xdev = torch.empty((T, wl.H), dtype=torch.int16, device=dev)
+    ydev = torch.empty((T, wl.H), dtype=torch.int16, device=dev)
+
+    def e2e_step():
+        with torch.cuda.stream(stream):
+            for l in range(nl):
+                xdev.copy_(x_host[l], non_blocking=True)
+                q4.lily_q4_moe_decode(layers[l], xdev, ydev, ws=dws, stream=stream)
+                y_host[l].copy_(ydev, non_blocking=True)
+        stream.synchronize()
+
+    for _ in range(2):
+        e2e_step()
+    e0 = time.perf_counter()
+    for _ in range(args.steps):
+        e2e_step()
+    e2e_s = (time.perf_counter() - e0) / args.steps
+    e2e_val = nl * T / e2e_s * ws_n
+
+    launches_per_step = nl * 3 + 1 + 8
+    res = {
+        "metric": METRIC,
+        "value": round(tok_per_s_layer, 1),
+        "unit": UNIT,
+        "n_gpus": ws_n,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(total_ms / args.steps, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "q4 weights, bf16 activations, fp32 accumulation",
+        "data": "synthetic (seeded generator; value distributions of the workloads)",
+        "config": {
+            "workload": f"decode MoE H2048 E256 top-8 + shared I512, batch {T}, {nl} "
+                        "independently seeded layers; + LM head 151936x2048 argmax; + prefill "
+                        "chunk 2048 tokens through one skewed-router layer",
+            "layers": nl, "tokens": T, "parallelism": f"replicas x{ws_n}",
+            "l2": "no flush: every timed read set (18.2 GB layers, 175 MB head, 455 MB prefill "
+                  "layer) exceeds the 129 MB L2",
+        },
+        "decode": {"tok_s_per_layer": round(tok_per_s_layer, 1), "us_per_layer": round(t_layer_s * 1e6, 3),
+                   "bytes_per_layer": int(bytes_per_layer), "hbm_gbs": round(dec_gbs, 1),
+                   "frac_of_measured_hbm": round(dec_gbs / pk["hbm_gbs"], 4)},
+        "lm_head": {"us": round(lm_mean * 1e3, 2), "bytes": lm_bytes,
+                    "hbm_gbs": round(lm_gbs, 1), "frac_of_measured_hbm": round(lm_gbs / pk["hbm_gbs"], 4)},
+        "prefill": {"us": round(pf_mean * 1e3, 1), "gflop": round(pf_flops / 1e9, 2),
+                    "tflops": round(pf_tflops, 1),
+                    "frac_of_measured_bf16": round(pf_tflops / pk["bf16_tflops_sustained"], 4),
+                    "tok_s": round(Tp / (pf_mean / 1e3), 1),
+                    "hbm_gbs_min_bytes": round(pf_bytes / (pf_mean / 1e3) / 1e9, 1)},
+        "roofline": {"bound": "hbm", "kernel": "lily_q4_moe_decode (router+top-k, gate/up, down)",
+                     "achieved": round(dec_gbs, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
+                     "frac": round(dec_gbs / pk["hbm_gbs"], 4), "peak_source": pk["source"],
+                     "traffic": None},
+        "e2e": {"value": round(e2e_val, 1), "unit": UNIT,
+                "h2d_bytes_per_step": nl * T * wl.H * 2, "d2h_bytes_per_step": nl * T * wl.H * 2,
+                "scope": "decode layers through lily_q4_moe_decode with pinned host x/y copies"},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk,
+        "setup_s": round(gen_s, 1),
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        res["cpu_baseline"] = cpu_baseline(wl, budget_s=12.0)
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+    if ws_n > 1:
+        dist.destroy_process_group()
+
+
+# ----------------------------------------------------------------------------- oracle timing
+
+def _oracle_layer_time(wl, l, T):
+    from bit_affine_quantized_mlx_gb300 import synth
+    from oracle import oracle as orc
+    L = wl.layer(l)
+    x = synth.draw_tokens(wl.H, T, wl.tokens_key(l))
+    t0 = time.perf_counter()
+    orc.moe(L, x)
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(wl, budget_s=12.0, T=1):
+    """Oracle (as it stands) on this host's cores: decode layers at batch T until the budget."""
+    from oracle import oracle as orc
+    orc.build()
+    times, l = [], 0
+    t_start = time.perf_counter()
+    while time.perf_counter() - t_start < budget_s and l < wl.layers:
+        times.append(_oracle_layer_time(wl, l, T))
+        l += 1
+    per_layer = statistics.mean(times)
+    return {"value": round(T / per_layer, 3), "unit": UNIT, "cores": 1 if T == 1 else orc.threads(),
+            "kind": "oracle",
+            "sample": f"{len(times)} decode layers at batch {T} (of the {wl.layers}), oracle only, "
+                      "input generation excluded"}
+
+
+def run_reference(args):
+    ws_n, rank, _ = dist_env()
+    if rank != 0:
+        return
+    from bit_affine_quantized_mlx_gb300 import synth
+    from oracle import oracle as orc
+    orc.build()
+    wl = synth.DECODE
+    T = args.tokens
+    for s in range(args.warmup):
+        _oracle_layer_time(wl, s % wl.layers, T)
+    times = [_oracle_layer_time(wl, s % wl.layers, T) for s in range(args.steps)]
+    per_layer = statistics.mean(times)
+    val = T / per_layer
+    cores = 1 if T == 1 else orc.threads()
+    res = {
+        "impl": "reference", "metric": METRIC, "value": round(val, 3), "unit": UNIT,
+        "n_gpus": ws_n, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(per_layer * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "fp32 dequant, fp64 accumulation", "data": "synthetic",
+        "config": {"workload": f"decode MoE H2048 E256 top-8 + shared I512, batch {T}; one "
+                               "layer per step (the CPU oracle)", "tokens": T},
+        "cpu_baseline": {"value": round(val, 3), "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": f"one decode layer per step, {args.steps} steps"},
+        "e2e": {"value": round(val, 3), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(res), flush=True)
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gb300(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,75 @@
+// Internal declarations shared by the library's translation units (host side).
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "../../include/lily_q4.h"
+
+namespace lq4 {
+
+constexpr size_t kAlign = 256;
+inline size_t align_up(size_t v, size_t a = kAlign) { return (v + a - 1) / a * a; }
+
+// Every workspace starts with a 256-byte header of int32 words.
+enum HeaderWord : int {
+  kHdrError = 0,    // nonzero after a bounded device-side wait gave up
+  kHdrCounterA = 1, // last-block-done counters (self-resetting)
+  kHdrCounterB = 2,
+  kHdrCounterC = 3,
+  kHdrWords = 64,
+};
+
+// ---------------------------------------------------------------- LM head
+struct LmWsLayout {
+  size_t off_partial_v, off_partial_i, total;
+  int grid;
+};
+LmWsLayout lm_ws_layout(int N, int K);
+int launch_gemv_argmax(const lily_q4_mat &W, int N, int K, const uint16_t *x, int32_t *token,
+                       float *logits, void *ws, cudaStream_t st);
+
+// ---------------------------------------------------------------- decode MoE
+struct DecodeWsLayout {
+  int T, E, k, I, H, P, Umax;
+  size_t off_logits;    // f32 [T][E]
+  size_t off_idx;       // i32 [T][k]
+  size_t off_p;         // f32 [T][k]
+  size_t off_sigma;     // f32 [T]
+  size_t off_meta;      // i32: [0] = number of unique experts U, [1..Umax] expert ids, then ubase[Umax+1]
+  size_t off_pair_tok;  // i32 [P]: token of each (unique expert, token) pair
+  size_t off_pair_w;    // f32 [P]: its combine weight (p, or sigma for the shared expert)
+  size_t off_h;         // f32 [P][I]: SwiGLU activations of each pair
+  size_t total;
+};
+DecodeWsLayout decode_ws_layout(const lily_q4_moe_layer &L, int T);
+int launch_moe_decode(const lily_q4_moe_layer &L, const uint16_t *x, int T, uint16_t *y,
+                      int32_t *topk_idx, float *topk_w, void *ws, cudaStream_t st);
+
+// ---------------------------------------------------------------- prefill MoE
+struct PrefillWsLayout {
+  int T, E, k, I, H, P, Tpad;
+  size_t off_logits;    // f32 [T][E]
+  size_t off_idx;       // i32 [T][k]
+  size_t off_p;         // f32 [T][k]
+  size_t off_sigma;     // f32 [T]
+  size_t off_counts;    // i32 [E+1] tokens per expert (slot E = shared, = T)
+  size_t off_offsets;   // i32 [E+2] exclusive prefix of counts
+  size_t off_perm;      // i32 [P] token of each sorted pair
+  size_t off_pw;        // f32 [P] combine weight of each sorted pair
+  size_t off_inv;       // i32 [T][k+1] sorted position of (token, slot)
+  size_t off_items;     // int4 work lists of the grouped GEMMs
+  size_t off_xperm;     // bf16 [T][H] token rows in the permuted K order
+  size_t off_h;         // bf16 [P][I] SwiGLU activations, sorted by expert
+  size_t off_o;         // bf16 [P][H] weighted expert outputs, sorted by expert
+  size_t total;
+  int max_items;
+};
+PrefillWsLayout prefill_ws_layout(const lily_q4_moe_layer &L, int T);
+int launch_moe_prefill(const lily_q4_moe_layer &L, const uint16_t *x, int T, uint16_t *y,
+                       int32_t *topk_idx, float *topk_w, void *ws, cudaStream_t st);
+
+int sm_count();
+int check_launch();
+
+}  // namespace lq4

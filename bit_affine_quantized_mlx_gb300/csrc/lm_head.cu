@@ -1,0 +1,197 @@
+// Q4 LM-head GEMV fused with greedy argmax.
+//
+// Greedy token selection without logprobs, with the generated id kept on the
+// device (Lily README, first paragraph; Lily-vs-MLX report, "Measurement
+// contract").  One pass over the weights: each warp dequantises rows in
+// registers (lane = one 64-wide group of the row), reduces the row with
+// shuffles, keeps a running (max, argmax); blocks publish their best pair to
+// the workspace and the last block to finish reduces those pairs into the token.
+// The pass is bound by HBM bandwidth: 0.5625 bytes per weight.
+#include <cfloat>
+#include <climits>
+
+#include "internal.h"
+#include "q4_device.cuh"
+
+namespace lq4 {
+
+constexpr int kLmThreads = 256;
+constexpr int kLmWarps = kLmThreads / 32;
+constexpr int kLmBlocksPerSm = 2;
+
+LmWsLayout lm_ws_layout(int N, int K) {
+  (void)K;
+  LmWsLayout l{};
+  int sms = sm_count();
+  if (sms <= 0) sms = 152;
+  // at most one block per 32 rows, at most kLmBlocksPerSm per SM
+  int want = (N + 31) / 32;
+  l.grid = want < sms * kLmBlocksPerSm ? want : sms * kLmBlocksPerSm;
+  if (l.grid < 1) l.grid = 1;
+  size_t off = kHdrWords * sizeof(int32_t);
+  off = align_up(off);
+  l.off_partial_v = off;
+  off = align_up(off + sizeof(float) * (size_t)sms * kLmBlocksPerSm);
+  l.off_partial_i = off;
+  off = align_up(off + sizeof(int32_t) * (size_t)sms * kLmBlocksPerSm);
+  l.total = off;
+  return l;
+}
+
+// G = groups per row (K/64), U = row-steps issued together (bytes in flight).
+template <int G, int U>
+__global__ void __launch_bounds__(kLmThreads, kLmBlocksPerSm)
+    gemv_argmax_kernel(const uint32_t *__restrict__ w, const uint16_t *__restrict__ s,
+                       const uint16_t *__restrict__ b, int N, const uint16_t *__restrict__ x,
+                       float *__restrict__ logits, int32_t *__restrict__ token,
+                       int32_t *__restrict__ hdr, float *__restrict__ part_v,
+                       int32_t *__restrict__ part_i) {
+  constexpr int RPS = 32 / G;  // rows per warp-step
+  constexpr int K8 = G * 8;    // words per row
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int g = lane % G, rsub = lane / G;
+
+  XGroup xg;
+  {
+    uint4 c[8];
+    const uint4 *xp = reinterpret_cast<const uint4 *>(x + kGroup * g);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) c[i] = __ldg(xp + i);
+    xgroup_from_bf16(xg, c);
+  }
+
+  float best_v = -FLT_MAX;
+  int best_i = INT_MAX;
+  const int gwarp = blockIdx.x * kLmWarps + warp;
+  const int nwarps = gridDim.x * kLmWarps;
+  constexpr int RPI = RPS * U;  // rows per warp-iteration
+
+  for (int r0 = gwarp * RPI; r0 < N; r0 += nwarps * RPI) {
+    uint4 wa[U], wb[U];
+    float sv[U], bv[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int row = r0 + u * RPS + rsub;
+      if (row < N) {
+        const uint32_t *wr = w + (size_t)row * K8 + 8 * g;
+        wa[u] = ld_stream(wr);
+        wb[u] = ld_stream(wr + 4);
+        sv[u] = bf16f(ld_u16(s + (size_t)row * G + g));
+        bv[u] = bf16f(ld_u16(b + (size_t)row * G + g));
+      } else {
+        wa[u] = wb[u] = make_uint4(0, 0, 0, 0);
+        sv[u] = bv[u] = 0.f;
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      float d = seg_sum<G>(q4_group_dot(wa[u], wb[u], xg, sv[u], bv[u]));
+      const int row = r0 + u * RPS + rsub;
+      if (g == 0 && row < N) {
+        if (logits) logits[row] = d;
+        if (better(d, row, best_v, best_i)) {
+          best_v = d;
+          best_i = row;
+        }
+      }
+    }
+  }
+  // warp argmax
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    float ov = __shfl_xor_sync(0xffffffffu, best_v, o);
+    int oi = __shfl_xor_sync(0xffffffffu, best_i, o);
+    if (better(ov, oi, best_v, best_i)) {
+      best_v = ov;
+      best_i = oi;
+    }
+  }
+  __shared__ float sv_[kLmWarps];
+  __shared__ int si_[kLmWarps];
+  __shared__ int is_last;
+  if (lane == 0) {
+    sv_[warp] = best_v;
+    si_[warp] = best_i;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float bv_ = sv_[0];
+    int bi_ = si_[0];
+    for (int i = 1; i < kLmWarps; ++i)
+      if (better(sv_[i], si_[i], bv_, bi_)) {
+        bv_ = sv_[i];
+        bi_ = si_[i];
+      }
+    part_v[blockIdx.x] = bv_;
+    part_i[blockIdx.x] = bi_;
+    __threadfence();
+    const int ticket = atomicAdd(hdr + kHdrCounterA, 1);
+    is_last = (ticket == (int)gridDim.x - 1);
+  }
+  __syncthreads();
+  if (!is_last) return;
+  __threadfence();
+  // last block: reduce the per-block pairs
+  float v = -FLT_MAX;
+  int i = INT_MAX;
+  for (int j = threadIdx.x; j < (int)gridDim.x; j += kLmThreads) {
+    const float pv = __ldcg(part_v + j);
+    const int pi = __ldcg(part_i + j);
+    if (better(pv, pi, v, i)) {
+      v = pv;
+      i = pi;
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    float ov = __shfl_xor_sync(0xffffffffu, v, o);
+    int oi = __shfl_xor_sync(0xffffffffu, i, o);
+    if (better(ov, oi, v, i)) {
+      v = ov;
+      i = oi;
+    }
+  }
+  if (lane == 0) {
+    sv_[warp] = v;
+    si_[warp] = i;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float bv_ = sv_[0];
+    int bi_ = si_[0];
+    for (int j = 1; j < kLmWarps; ++j)
+      if (better(sv_[j], si_[j], bv_, bi_)) {
+        bv_ = sv_[j];
+        bi_ = si_[j];
+      }
+    *token = bi_;
+    hdr[kHdrCounterA] = 0;  // leave the counter ready for the next call
+  }
+}
+
+template <int G>
+static void launch_g(const lily_q4_mat &W, int N, const uint16_t *x, int32_t *token,
+                     float *logits, void *ws, const LmWsLayout &l, cudaStream_t st) {
+  char *base = static_cast<char *>(ws);
+  gemv_argmax_kernel<G, (G >= 16 ? 2 : 4)><<<l.grid, kLmThreads, 0, st>>>(
+      W.w, W.s, W.b, N, x, logits, token, reinterpret_cast<int32_t *>(base),
+      reinterpret_cast<float *>(base + l.off_partial_v),
+      reinterpret_cast<int32_t *>(base + l.off_partial_i));
+}
+
+int launch_gemv_argmax(const lily_q4_mat &W, int N, int K, const uint16_t *x, int32_t *token,
+                       float *logits, void *ws, cudaStream_t st) {
+  const LmWsLayout l = lm_ws_layout(N, K);
+  switch (K / kGroup) {
+    case 1: launch_g<1>(W, N, x, token, logits, ws, l, st); break;
+    case 2: launch_g<2>(W, N, x, token, logits, ws, l, st); break;
+    case 4: launch_g<4>(W, N, x, token, logits, ws, l, st); break;
+    case 8: launch_g<8>(W, N, x, token, logits, ws, l, st); break;
+    case 16: launch_g<16>(W, N, x, token, logits, ws, l, st); break;
+    case 32: launch_g<32>(W, N, x, token, logits, ws, l, st); break;
+    default: return LILY_Q4_ERR_UNSUPPORTED;
+  }
+  return check_launch();
+}
+
+}  // namespace lq4

@@ -1,0 +1,824 @@
+// Prefill-chunk MoE feed-forward on the tensor cores.
+//
+// Prefill is compute-bound and runs the expert GEMM on the matrix units ("Prefill on
+// the tensor ops ... better tiling for the expert GEMM", fork page, "How the speed was
+// achieved"; prompt chunks of 2,048 tokens, Lily-vs-MLX report, "Measurement
+// contract").  Launch sequence on the caller's stream:
+//
+//   x_perm      : token rows with K permuted inside every 8-element chunk to the order
+//                 the Q4 unpack produces (0,4,1,5,2,6,3,7), so dequantised weight words
+//                 are stored without a shuffle (a dot product is unchanged when both
+//                 operands are permuted alike)
+//   router GEMM : logits[T][E] = x Wr^T (+ offsets), bf16 x bf16 -> fp32 on tcgen05
+//   topk        : top-k per token, softmax over the k, shared gate sigmoid(x . g)
+//   scan        : per-expert offsets of the token-sorted pairs, GEMM work lists
+//   perm        : stable bucketing (token order inside an expert)
+//   gate/up GEMM: per (expert, 128 intermediate rows, <=128 tokens): dequantised Q4
+//                 gate and up tiles x gathered token rows, SwiGLU in the epilogue -> h (bf16)
+//   down GEMM   : per (expert, 128 output rows, <=128 tokens): Q4 down tile x h rows,
+//                 scaled by the pair's gate weight -> o (bf16)
+//   combine     : y[t] = sum over t's k slots (+ shared) of o, in slot order (deterministic)
+//
+// The GEMM kernel is persistent (one CTA per SM) and warp-specialised:
+//   warps 0-3  epilogue: tcgen05.ld of the fp32 accumulator (TMEM lanes 0..127)
+//   warp  4    TMEM allocation and the single-thread tcgen05.mma issue loop
+//   warps 5-7  token-row gather: cp.async into a 128-byte-swizzled K-major tile
+//   warps 8-15 weight producers: Q4 codes and scales cp.async'd into a 4-deep raw ring,
+//              dequantised in registers (bf16x2 FMA: s*q + b, one rounding) and stored
+//              as a 128-byte-swizzled K-major bf16 tile
+// Stages are handed over with mbarriers; accumulators are double-buffered in TMEM so the
+// epilogue of one tile overlaps the main loop of the next.  Every wait is bounded: on
+// time-out the kernel records an error word in the workspace, drains and returns.
+#include <cfloat>
+#include <climits>
+#include <cuda_bf16.h>
+
+#include "internal.h"
+#include "q4_device.cuh"
+#include "tc_sm100.cuh"
+
+namespace lq4 {
+
+constexpr int kBM = 128;  // weight rows per tile (MMA M)
+constexpr int kBN = 128;  // tokens per tile (MMA N, padded to a multiple of 16)
+constexpr int kGemmThreads = 512;
+constexpr int kMmaWarp = 4;
+constexpr int kBWarp0 = 5, kBThreads = 96;
+constexpr int kAWarp0 = 8, kAThreads = 256;
+constexpr int kRing = 4;       // raw-code ring depth (k-blocks)
+constexpr int kScSlots = 4;    // scale-block slots
+constexpr long long kWaitCycles = 4000000000LL;  // ~2 s at GB300 clocks
+constexpr int kHdrItemsGU = 8, kHdrItemsDN = 9;
+
+enum { kRouter = 0, kGateUp = 1, kDown = 2 };
+
+template <int MODE>
+struct Cfg {
+  static constexpr int NA = MODE == kGateUp ? 2 : 1;  // A tiles per stage
+  static constexpr int S = MODE == kGateUp ? 3 : 4;   // operand stages
+  static constexpr int A_BYTES = kBM * 128;
+  static constexpr int B_BYTES = kBN * 128;
+  static constexpr int STAGE = NA * A_BYTES + B_BYTES;
+  static constexpr int RAW_SLOT = NA * kBM * 32;
+  static constexpr int SC_SLOT = 2 * 2 * kBM * 16;  // [copy][s|b][row][8 groups]
+  static constexpr int ACC_COLS = NA * kBN;
+  static constexpr int TMEM_COLS = 2 * ACC_COLS;  // double buffer
+  static constexpr int OFF_RAW = S * STAGE;
+  static constexpr int OFF_SC = OFF_RAW + (MODE == kRouter ? 0 : kRing * RAW_SLOT);
+  static constexpr int OFF_BAR = OFF_SC + (MODE == kRouter ? 0 : kScSlots * SC_SLOT);
+  static constexpr int NBARS = 2 * S + 4 + 1;
+  static constexpr int BYTES = OFF_BAR + NBARS * 8 + 1024;
+};
+
+struct GemmArgs {
+  lily_q4_mat a0, a1, sh0, sh1;  // routed stacks and shared matrices (a1/sh1: up)
+  const uint16_t *a_bf16;        // router weights [E][H]
+  int a_rows;                    // rows of one expert matrix (or E for the router)
+  int K;                         // reduction length
+  int E;
+  const uint16_t *b_src;         // x_perm / h / x
+  const int32_t *perm;
+  const int4 *items;
+  const int32_t *n_items_ptr;
+  int n_items_static, mt_static, T;
+  uint16_t *h_out;
+  uint16_t *o_out;
+  int o_ld;                      // H
+  const float *pw;
+  float *logits;
+  const float *bias;
+  int32_t *hdr;
+};
+
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int *abort_flag,
+                                         int32_t *err) {
+  if (tc::mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (true) {
+    if (tc::mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (clock64() - t0 > kWaitCycles) {
+      *abort_flag = 1;
+      atomicExch(err, 1);
+      return false;
+    }
+  }
+}
+
+template <int MODE>
+__device__ __forceinline__ int4 get_item(const GemmArgs &a, int i) {
+  if (MODE == kRouter) {
+    const int mt = i % a.mt_static, t0 = (i / a.mt_static) * kBN;
+    return make_int4(0, t0, min(kBN, a.T - t0), mt);
+  }
+  return a.items[i];
+}
+
+// Position of element r inside its 8-chunk in the permuted K order (0,4,1,5,2,6,3,7).
+__device__ __forceinline__ int kpos(int r) {
+  return (r & ~7) | ((r & 3) * 2 + ((r >> 2) & 1));
+}
+
+// Dequantise 4 code words (32 codes) of one row into 4 16-byte chunks of bf16, each
+// chunk holding (q_j, q_j+4) pairs in the permuted K order.
+__device__ __forceinline__ uint4 dequant_word(uint32_t w, __nv_bfloat162 s2, __nv_bfloat162 b2) {
+  uint32_t out[4];
+  const __nv_bfloat162 c128 = __floats2bfloat162_rn(128.f, 128.f);
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    uint32_t v = ((w >> (4 * j)) & 0x000F000Fu) | 0x43004300u;
+    __nv_bfloat162 q = *reinterpret_cast<__nv_bfloat162 *>(&v);
+    q = __hsub2(q, c128);              // exact: small integers
+    __nv_bfloat162 d = __hfma2(q, s2, b2);  // s*q + b, one rounding to bf16
+    out[j] = *reinterpret_cast<uint32_t *>(&d);
+  }
+  return make_uint4(out[0], out[1], out[2], out[3]);
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const GemmArgs a) {
+  using C = Cfg<MODE>;
+  extern __shared__ uint8_t smem_dyn[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>(((uintptr_t)smem_dyn + 1023) & ~(uintptr_t)1023);
+  const uint32_t sbase = tc::smem_u32(smem);
+  const uint32_t bar0 = sbase + C::OFF_BAR;
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (C::S + s); };
+  auto accf_bar = [&](int b) { return bar0 + 8u * (2 * C::S + b); };
+  auto acce_bar = [&](int b) { return bar0 + 8u * (2 * C::S + 2 + b); };
+  const uint32_t done_bar = bar0 + 8u * (2 * C::S + 4);
+
+  __shared__ uint32_t s_taddr;
+  __shared__ volatile int s_abort;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n_items = MODE == kRouter ? a.n_items_static : *(volatile const int32_t *)a.n_items_ptr;
+  const int nkb = a.K / 64;
+  const int G = a.K / 64;  // groups per row
+
+  if (threadIdx.x == 0) {
+    s_abort = 0;
+    for (int s = 0; s < C::S; ++s) {
+      tc::mbar_init(full_bar(s), kAThreads + kBThreads);
+      tc::mbar_init(empty_bar(s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      tc::mbar_init(accf_bar(b), 1);
+      tc::mbar_init(acce_bar(b), 128);
+    }
+    tc::mbar_init(done_bar, 1);
+    tc::mbar_init_fence();
+  }
+  if (warp == kMmaWarp) {
+    tc::tmem_alloc(tc::smem_u32(&s_taddr), C::TMEM_COLS);
+    tc::tmem_relinquish();
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t taddr = s_taddr;
+  int32_t *err = a.hdr + kHdrError;
+
+  if (warp < 4) {
+    // ------------------------------------------------------------------ epilogue
+    const int r = warp * 32 + lane;
+    int j = 0;
+    for (int it = blockIdx.x; it < n_items; it += gridDim.x, ++j) {
+      const int4 item = get_item<MODE>(a, it);
+      const int b = j & 1;
+      if (!wait_bar(accf_bar(b), (j >> 1) & 1, &s_abort, err)) break;
+      tc::tc_fence_after();
+      const int ntok = item.z, npad = (ntok + 15) & ~15;
+      const int m = item.w * kBM + r;
+      const bool row_ok = m < a.a_rows;
+      const uint32_t tcol = taddr + ((uint32_t)(warp * 32) << 16) + (uint32_t)(b * C::ACC_COLS);
+      for (int c0 = 0; c0 < npad; c0 += 16) {
+        float d[16];
+        tc::tmem_ld16(tcol + c0, d);
+        if (MODE == kGateUp) {
+          float u[16];
+          tc::tmem_ld16(tcol + kBN + c0, u);
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const int n = c0 + i;
+            if (row_ok && n < ntok)
+              a.h_out[(size_t)(item.y + n) * a.a_rows + kpos(m)] = f2bf16_rne(silu_mul(d[i], u[i]));
+          }
+        } else if (MODE == kDown) {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const int n = c0 + i;
+            if (row_ok && n < ntok) {
+              const float w = a.pw[item.y + n];
+              a.o_out[(size_t)(item.y + n) * a.o_ld + m] = f2bf16_rne(w * d[i]);
+            }
+          }
+        } else {
+          const float bias = (row_ok && a.bias) ? a.bias[m] : 0.f;
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const int n = c0 + i;
+            if (row_ok && n < ntok) a.logits[(size_t)(item.y + n) * a.E + m] = d[i] + bias;
+          }
+        }
+      }
+      tc::tc_fence_before();
+      tc::mbar_arrive(acce_bar(b));
+    }
+  } else if (warp == kMmaWarp) {
+    // ------------------------------------------------------------------ MMA issue
+    if (lane == 0) {
+      int st = 0, j = 0;
+      bool ok = true;
+      for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x, ++j) {
+        const int4 item = get_item<MODE>(a, it);
+        const int b = j & 1;
+        if (!wait_bar(acce_bar(b), ((j >> 1) & 1) ^ 1, &s_abort, err)) break;
+        tc::tc_fence_after();
+        const int npad = (item.z + 15) & ~15;
+        const uint32_t idesc = tc::idesc_bf16_f32(kBM, npad);
+        const uint32_t d0 = taddr + (uint32_t)(b * C::ACC_COLS);
+        for (int kb = 0; kb < nkb; ++kb, ++st) {
+          const int s = st % C::S;
+          if (!wait_bar(full_bar(s), (st / C::S) & 1, &s_abort, err)) {
+            ok = false;
+            break;
+          }
+          tc::fence_proxy_async();
+          tc::tc_fence_after();
+          const uint32_t sA = sbase + s * C::STAGE;
+          const uint32_t sB = sA + C::NA * C::A_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint64_t bd = tc::desc_k128_sw128(sB + 32 * kk);
+            const uint32_t acc = (kb | kk) ? 1u : 0u;
+            tc::mma_bf16(d0, tc::desc_k128_sw128(sA + 32 * kk), bd, idesc, acc);
+            if (MODE == kGateUp)
+              tc::mma_bf16(d0 + kBN, tc::desc_k128_sw128(sA + C::A_BYTES + 32 * kk), bd, idesc,
+                           acc);
+          }
+          tc::mma_commit(empty_bar(s));
+        }
+        if (!ok) break;
+        tc::mma_commit(accf_bar(b));
+      }
+      // drain: all issued MMAs complete before TMEM is released
+      tc::mma_commit(done_bar);
+      wait_bar(done_bar, 0, &s_abort, err);
+    }
+    __syncwarp();
+  } else if (warp >= kBWarp0 && warp < kAWarp0) {
+    // ------------------------------------------------------------------ token-row gather
+    const int tb = threadIdx.x - kBWarp0 * 32;
+    int st = 0;
+    bool ok = true;
+    for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
+      const int4 item = get_item<MODE>(a, it);
+      const int ntok = item.z, npad = (ntok + 15) & ~15;
+      for (int kb = 0; kb < nkb; ++kb, ++st) {
+        const int s = st % C::S;
+        if (!wait_bar(empty_bar(s), ((st / C::S) & 1) ^ 1, &s_abort, err)) {
+          ok = false;
+          break;
+        }
+        const uint32_t sB = sbase + s * C::STAGE + C::NA * C::A_BYTES;
+        for (int q = tb; q < npad * 8; q += kBThreads) {
+          const int n = q >> 3, c = q & 7;
+          const uint16_t *src = a.b_src;
+          uint32_t bytes = 0;
+          if (n < ntok) {
+            size_t row;
+            if (MODE == kGateUp)
+              row = (size_t)__ldg(a.perm + item.y + n);
+            else
+              row = (size_t)(item.y + n);
+            src = a.b_src + row * a.K + kb * 64 + 8 * c;
+            bytes = 16;
+          }
+          tc::cp_async16(sB + tc::sw128(n, c), src, bytes);
+        }
+        tc::cp_async_arrive_noinc(full_bar(s));
+      }
+    }
+    tc::cp_async_wait_all();
+  } else {
+    // ------------------------------------------------------------------ weight producers
+    const int ta = threadIdx.x - kAWarp0 * 32;  // 0..255
+    const int row = ta & (kBM - 1);
+    const int half = ta >> 7;                   // GateUp: matrix; Down/Router: which half row
+    const int mat = C::NA == 2 ? half : 0;
+    bool ok = true;
+    if (MODE == kRouter) {
+      int st = 0;
+      for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
+        const int4 item = get_item<MODE>(a, it);
+        const int m = item.w * kBM + row;
+        const bool valid = m < a.a_rows;
+        for (int kb = 0; kb < nkb; ++kb, ++st) {
+          const int s = st % C::S;
+          if (!wait_bar(empty_bar(s), ((st / C::S) & 1) ^ 1, &s_abort, err)) {
+            ok = false;
+            break;
+          }
+          const uint32_t sA = sbase + s * C::STAGE;
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int c = 4 * half + i;
+            const uint16_t *src = valid ? a.a_bf16 + (size_t)m * a.K + kb * 64 + 8 * c : a.a_bf16;
+            tc::cp_async16(sA + tc::sw128(row, c), src, valid ? 16u : 0u);
+          }
+          tc::cp_async_arrive_noinc(full_bar(s));
+        }
+      }
+      tc::cp_async_wait_all();
+    } else {
+      // Continuous k-block stream over this CTA's items; the issue side runs kRing-1
+      // k-blocks ahead of the consume side.
+      constexpr int WPT = C::NA == 2 ? 8 : 4;  // code words per thread per k-block
+      const int woff = C::NA == 2 ? 0 : 4 * half;
+      const uint32_t raw0 = sbase + C::OFF_RAW;
+      const uint32_t sc0 = sbase + C::OFF_SC;
+      const uint8_t *raw_p = smem + C::OFF_RAW;
+      const uint8_t *sc_p = smem + C::OFF_SC;
+      // issue iterator
+      int i_it = blockIdx.x, i_kb = 0, i_g = 0, i_sg = 0;
+      auto issue = [&]() {
+        if (i_it < n_items) {
+          const int4 item = a.items[i_it];
+          const int e = item.x, m = item.w * kBM + row;
+          if (m < a.a_rows) {
+            const bool sh = (e == a.E);
+            const lily_q4_mat &W = sh ? (mat ? a.sh1 : a.sh0) : (mat ? a.a1 : a.a0);
+            const size_t wbase = (sh ? 0 : (size_t)e * a.a_rows * (a.K / 8)) + (size_t)m * (a.K / 8);
+            const size_t sbase_e = (sh ? 0 : (size_t)e * a.a_rows * G) + (size_t)m * G;
+            const uint32_t dst = raw0 + (i_g % kRing) * C::RAW_SLOT + (mat * kBM + row) * 32 + woff * 4;
+            const uint32_t *src = W.w + wbase + i_kb * 8 + woff;
+            tc::cp_async16(dst, src, 16);
+            if (WPT == 8) tc::cp_async16(dst + 16, src + 4, 16);
+            if ((i_kb & 7) == 0) {
+              // scale block: s and b of k-blocks i_kb .. i_kb+7 (fewer when G < 8)
+              const int nb = min(8, G - i_kb);
+              const uint32_t sdst = sc0 + (i_sg % kScSlots) * C::SC_SLOT;
+              for (int arr = 0; arr < 2; ++arr) {
+                const uint16_t *ssrc = (arr ? W.b : W.s) + sbase_e + i_kb;
+                const uint32_t d = sdst + ((half * 2 + arr) * kBM + row) * 16;
+                if (nb == 8) tc::cp_async16(d, ssrc, 16);
+                else if (nb == 4) tc::cp_async8(d, ssrc);
+                else tc::cp_async4(d, ssrc);
+              }
+            }
+          }
+          if ((i_kb & 7) == 0) ++i_sg;
+          ++i_g;
+          if (++i_kb == nkb) {
+            i_kb = 0;
+            i_it += gridDim.x;
+          }
+        }
+        tc::cp_async_commit();
+      };
+      for (int p = 0; p < kRing - 1; ++p) issue();
+      int st = 0, c_g = 0, c_sg = -1;
+      for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
+        const int4 item = a.items[it];
+        const int m = item.w * kBM + row;
+        const bool valid = m < a.a_rows;
+        for (int kb = 0; kb < nkb; ++kb, ++st, ++c_g) {
+          if ((kb & 7) == 0) ++c_sg;
+          issue();
+          tc::cp_async_wait<kRing - 1>();
+          uint4 outv[WPT];
+          if (valid) {
+            const uint8_t *rp = raw_p + (c_g % kRing) * C::RAW_SLOT + (mat * kBM + row) * 32 + woff * 4;
+            const uint4 w0 = *reinterpret_cast<const uint4 *>(rp);
+            uint4 w1 = make_uint4(0, 0, 0, 0);
+            if (WPT == 8) w1 = *reinterpret_cast<const uint4 *>(rp + 16);
+            const uint8_t *sp = sc_p + (c_sg % kScSlots) * C::SC_SLOT;
+            const int gi = kb & 7;
+            const uint16_t sbits =
+                *reinterpret_cast<const uint16_t *>(sp + ((half * 2 + 0) * kBM + row) * 16 + 2 * gi);
+            const uint16_t bbits =
+                *reinterpret_cast<const uint16_t *>(sp + ((half * 2 + 1) * kBM + row) * 16 + 2 * gi);
+            const __nv_bfloat162 s2 = __halves2bfloat162(*reinterpret_cast<const __nv_bfloat16 *>(&sbits),
+                                                         *reinterpret_cast<const __nv_bfloat16 *>(&sbits));
+            const __nv_bfloat162 b2 = __halves2bfloat162(*reinterpret_cast<const __nv_bfloat16 *>(&bbits),
+                                                         *reinterpret_cast<const __nv_bfloat16 *>(&bbits));
+            const uint32_t ws[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+#pragma unroll
+            for (int q = 0; q < WPT; ++q) outv[q] = dequant_word(ws[q], s2, b2);
+          } else {
+#pragma unroll
+            for (int q = 0; q < WPT; ++q) outv[q] = make_uint4(0, 0, 0, 0);
+          }
+          const int s = st % C::S;
+          if (!wait_bar(empty_bar(s), ((st / C::S) & 1) ^ 1, &s_abort, err)) {
+            ok = false;
+            break;
+          }
+          uint8_t *sA = smem + s * C::STAGE + mat * C::A_BYTES;
+#pragma unroll
+          for (int q = 0; q < WPT; ++q)
+            *reinterpret_cast<uint4 *>(sA + tc::sw128(row, woff + q)) = outv[q];
+          tc::fence_proxy_async();
+          tc::mbar_arrive(full_bar(s));
+        }
+      }
+      tc::cp_async_wait_all();
+    }
+  }
+
+  tc::tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc::tc_fence_after();
+    tc::tmem_dealloc(taddr, C::TMEM_COLS);
+  }
+}
+
+// -------------------------------------------------------------------------------------
+// small kernels around the GEMMs
+// -------------------------------------------------------------------------------------
+
+// x_perm[t][8c + pos(i)] = x[t][8c + i]
+__global__ void x_perm_kernel(const uint4 *__restrict__ x, uint4 *__restrict__ xp, int nchunks) {
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < nchunks; i += gridDim.x * blockDim.x) {
+    const uint4 v = __ldg(x + i);
+    uint4 o;
+    o.x = __byte_perm(v.x, v.z, 0x5410);
+    o.y = __byte_perm(v.x, v.z, 0x7632);
+    o.z = __byte_perm(v.y, v.w, 0x5410);
+    o.w = __byte_perm(v.y, v.w, 0x7632);
+    xp[i] = o;
+  }
+}
+
+struct TopkArgs {
+  const float *logits;
+  const uint16_t *x;
+  const uint16_t *shared_gate;
+  int T, E, H, k, has_shared;
+  int32_t *idx;
+  float *p;
+  float *sigma;
+  int32_t *counts;
+  int32_t *out_idx;
+  float *out_w;
+};
+
+// One warp per token: k rounds of a warp argmax (logit desc, index asc), softmax over
+// the k, shared-expert gate.
+__global__ void __launch_bounds__(256) topk_prefill_kernel(TopkArgs a) {
+  const int lane = threadIdx.x & 31;
+  const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (t >= a.T) return;
+  const float *lg = a.logits + (size_t)t * a.E;
+  uint32_t taken = 0;
+  float sel_v[16];
+  int sel_e[16];
+  for (int i = 0; i < a.k; ++i) {
+    float bv = -FLT_MAX;
+    int be = INT_MAX;
+    for (int j = 0; lane + 32 * j < a.E; ++j) {
+      if (taken & (1u << j)) continue;
+      const int e = lane + 32 * j;
+      const float v = lg[e];
+      if (better(v, e, bv, be)) {
+        bv = v;
+        be = e;
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+      const int oe = __shfl_xor_sync(0xffffffffu, be, o);
+      if (better(ov, oe, bv, be)) {
+        bv = ov;
+        be = oe;
+      }
+    }
+    if ((be & 31) == lane) taken |= 1u << (be >> 5);
+    sel_v[i] = bv;
+    sel_e[i] = be;
+  }
+  float sig = 0.f;
+  if (a.has_shared) {
+    const uint16_t *xt = a.x + (size_t)t * a.H;
+    float acc = 0.f;
+    for (int h = lane * 8; h < a.H; h += 256) {
+      const uint4 xv = __ldg(reinterpret_cast<const uint4 *>(xt + h));
+      const uint4 gv = __ldg(reinterpret_cast<const uint4 *>(a.shared_gate + h));
+      const uint32_t xx[4] = {xv.x, xv.y, xv.z, xv.w}, gg[4] = {gv.x, gv.y, gv.z, gv.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        acc = fmaf(__uint_as_float(xx[i] << 16), __uint_as_float(gg[i] << 16), acc);
+        acc = fmaf(__uint_as_float(xx[i] & 0xFFFF0000u), __uint_as_float(gg[i] & 0xFFFF0000u), acc);
+      }
+    }
+    acc = seg_sum<32>(acc);
+    sig = 1.0f / (1.0f + expf(-acc));
+  }
+  if (lane == 0) {
+    float denom = 0.f;
+    for (int i = 0; i < a.k; ++i) denom += expf(sel_v[i] - sel_v[0]);
+    for (int i = 0; i < a.k; ++i) {
+      const float pi = expf(sel_v[i] - sel_v[0]) / denom;
+      a.idx[t * a.k + i] = sel_e[i];
+      a.p[t * a.k + i] = pi;
+      if (a.out_idx) a.out_idx[t * a.k + i] = sel_e[i];
+      if (a.out_w) a.out_w[t * a.k + i] = pi;
+      atomicAdd(a.counts + sel_e[i], 1);
+    }
+    a.sigma[t] = sig;
+  }
+}
+
+struct ScanArgs {
+  int32_t *counts;   // [E] (zeroed again here)
+  int32_t *offsets;  // [E+2]
+  int4 *items_gu, *items_dn;
+  int32_t *hdr;
+  int T, E, k, has_shared, mt_gu, mt_dn;
+};
+
+// Single block: per-expert offsets, GEMM work lists, and re-zeroed counts.
+__global__ void __launch_bounds__(1024) scan_items_kernel(ScanArgs a) {
+  __shared__ int s_cnt[1025];
+  __shared__ int s_off[1026];
+  __shared__ int s_nt[1025];
+  __shared__ int s_ibase[1026];
+  const int nexp = a.E + a.has_shared;
+  for (int e = threadIdx.x; e < nexp; e += blockDim.x) {
+    const int c = e < a.E ? a.counts[e] : a.T;
+    s_cnt[e] = c;
+    s_nt[e] = (c + kBN - 1) / kBN;
+  }
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
+    const int per = (nexp + 31) / 32;
+    const int lo = lane * per, hi = min(nexp, lo + per);
+    int sc = 0, sn = 0;
+    for (int e = lo; e < hi; ++e) {
+      sc += s_cnt[e];
+      sn += s_nt[e];
+    }
+    int tc_, tn_;
+    int rc = warp_excl_scan(sc, &tc_);
+    int rn = warp_excl_scan(sn, &tn_);
+    for (int e = lo; e < hi; ++e) {
+      s_off[e] = rc;
+      s_ibase[e] = rn;
+      rc += s_cnt[e];
+      rn += s_nt[e];
+    }
+    if (lane == 31) {
+      s_off[nexp] = rc;
+      s_ibase[nexp] = rn;
+    }
+  }
+  __syncthreads();
+  const int ntiles = s_ibase[nexp];
+  for (int e = threadIdx.x; e < nexp; e += blockDim.x) {
+    a.offsets[e] = s_off[e];
+    for (int nt = 0; nt < s_nt[e]; ++nt) {
+      const int p0 = s_off[e] + nt * kBN;
+      const int n = min(kBN, s_cnt[e] - nt * kBN);
+      const int tile = s_ibase[e] + nt;
+      for (int mt = 0; mt < a.mt_gu; ++mt) a.items_gu[tile * a.mt_gu + mt] = make_int4(e, p0, n, mt);
+      for (int mt = 0; mt < a.mt_dn; ++mt) a.items_dn[tile * a.mt_dn + mt] = make_int4(e, p0, n, mt);
+    }
+    if (e < a.E) a.counts[e] = 0;
+  }
+  if (threadIdx.x == 0) {
+    a.offsets[nexp] = s_off[nexp];
+    a.hdr[kHdrItemsGU] = ntiles * a.mt_gu;
+    a.hdr[kHdrItemsDN] = ntiles * a.mt_dn;
+  }
+}
+
+struct PermArgs {
+  const int32_t *idx;
+  const float *p;
+  const float *sigma;
+  const int32_t *offsets;
+  int32_t *perm;
+  float *pw;
+  int32_t *inv;
+  int T, E, k;
+};
+
+// Block e: the pairs choosing expert e, in token order (stable bucketing).
+__global__ void __launch_bounds__(256) perm_kernel(PermArgs a) {
+  const int e = blockIdx.x;
+  const int kk = a.k + 1;
+  if (e == a.E) {  // shared expert: every token, in order
+    for (int t = threadIdx.x; t < a.T; t += blockDim.x) {
+      const int pos = a.offsets[a.E] + t;
+      a.perm[pos] = t;
+      a.pw[pos] = a.sigma[t];
+      a.inv[t * kk + a.k] = pos;
+    }
+    return;
+  }
+  __shared__ int s_wsum[8];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int n = a.T * a.k;
+  int running = a.offsets[e];
+  for (int base = 0; base < n; base += 256) {
+    const int j = base + threadIdx.x;
+    const bool f = j < n && __ldg(a.idx + j) == e;
+    const unsigned bal = __ballot_sync(0xffffffffu, f);
+    if (lane == 0) s_wsum[warp] = __popc(bal);
+    __syncthreads();
+    int before = 0, total = 0;
+    for (int w = 0; w < 8; ++w) {
+      if (w < warp) before += s_wsum[w];
+      total += s_wsum[w];
+    }
+    if (f) {
+      const int pos = running + before + __popc(bal & ((1u << lane) - 1));
+      const int t = j / a.k, i = j % a.k;
+      a.perm[pos] = t;
+      a.pw[pos] = a.p[j];
+      a.inv[t * kk + i] = pos;
+    }
+    running += total;
+    __syncthreads();
+  }
+}
+
+// y[t][8c..8c+7] = sum over t's slots of o[inv[t][slot]] (fixed slot order).
+__global__ void combine_kernel(const uint16_t *__restrict__ o, const int32_t *__restrict__ inv,
+                               uint16_t *__restrict__ y, int T, int H, int nslots, int kk) {
+  const int cpr = H / 8;
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < T * cpr; i += gridDim.x * blockDim.x) {
+    const int t = i / cpr, c = i % cpr;
+    float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+    for (int s = 0; s < nslots; ++s) {
+      const int pos = __ldg(inv + t * kk + s);
+      const uint4 v = __ldcg(reinterpret_cast<const uint4 *>(o + (size_t)pos * H) + c);
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        acc[2 * q] += __uint_as_float(w[q] << 16);
+        acc[2 * q + 1] += __uint_as_float(w[q] & 0xFFFF0000u);
+      }
+    }
+    uint4 r;
+    r.x = (uint32_t)f2bf16_rne(acc[0]) | ((uint32_t)f2bf16_rne(acc[1]) << 16);
+    r.y = (uint32_t)f2bf16_rne(acc[2]) | ((uint32_t)f2bf16_rne(acc[3]) << 16);
+    r.z = (uint32_t)f2bf16_rne(acc[4]) | ((uint32_t)f2bf16_rne(acc[5]) << 16);
+    r.w = (uint32_t)f2bf16_rne(acc[6]) | ((uint32_t)f2bf16_rne(acc[7]) << 16);
+    reinterpret_cast<uint4 *>(y + (size_t)t * H)[c] = r;
+  }
+}
+
+// -------------------------------------------------------------------------------------
+// host side
+// -------------------------------------------------------------------------------------
+
+PrefillWsLayout prefill_ws_layout(const lily_q4_moe_layer &L, int T) {
+  PrefillWsLayout l{};
+  l.T = T;
+  l.E = L.n_experts;
+  l.k = L.top_k;
+  l.I = L.inter;
+  l.H = L.hidden;
+  l.P = T * L.top_k + (L.has_shared ? T : 0);
+  const int nexp = l.E + (L.has_shared ? 1 : 0);
+  const int tiles = nexp + (l.P + kBN - 1) / kBN;
+  const int mt_gu = (l.I + kBM - 1) / kBM, mt_dn = (l.H + kBM - 1) / kBM;
+  l.max_items = tiles * (mt_gu + mt_dn);
+  size_t off = align_up(kHdrWords * sizeof(int32_t));
+  auto take = [&](size_t bytes) {
+    size_t o = off;
+    off = align_up(off + bytes);
+    return o;
+  };
+  l.off_logits = take(sizeof(float) * (size_t)T * l.E);
+  l.off_idx = take(sizeof(int32_t) * (size_t)T * l.k);
+  l.off_p = take(sizeof(float) * (size_t)T * l.k);
+  l.off_sigma = take(sizeof(float) * (size_t)T);
+  l.off_counts = take(sizeof(int32_t) * (size_t)(l.E + 1));
+  l.off_offsets = take(sizeof(int32_t) * (size_t)(l.E + 2));
+  l.off_perm = take(sizeof(int32_t) * (size_t)l.P);
+  l.off_pw = take(sizeof(float) * (size_t)l.P);
+  l.off_inv = take(sizeof(int32_t) * (size_t)T * (l.k + 1));
+  l.off_items = take(sizeof(int4) * (size_t)l.max_items);
+  l.off_xperm = take(sizeof(uint16_t) * (size_t)T * l.H);
+  l.off_h = take(sizeof(uint16_t) * (size_t)l.P * l.I);
+  l.off_o = take(sizeof(uint16_t) * (size_t)l.P * l.H);
+  l.total = off;
+  return l;
+}
+
+template <int MODE>
+static int launch_gemm(const GemmArgs &a, int grid, cudaStream_t st) {
+  const int bytes = Cfg<MODE>::BYTES;
+  static bool attr_set[3] = {false, false, false};
+  if (!attr_set[MODE]) {
+    if (cudaFuncSetAttribute(grouped_gemm_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             bytes) != cudaSuccess)
+      return LILY_Q4_ERR_CUDA;
+    attr_set[MODE] = true;
+  }
+  grouped_gemm_kernel<MODE><<<grid, kGemmThreads, bytes, st>>>(a);
+  return check_launch();
+}
+
+int launch_moe_prefill(const lily_q4_moe_layer &L, const uint16_t *x, int T, uint16_t *y,
+                       int32_t *topk_idx, float *topk_w, void *ws, cudaStream_t st) {
+  if (L.hidden < 128 || L.inter < 128) return LILY_Q4_ERR_UNSUPPORTED;
+  const PrefillWsLayout l = prefill_ws_layout(L, T);
+  char *b = static_cast<char *>(ws);
+  int32_t *hdr = reinterpret_cast<int32_t *>(b);
+  float *logits = reinterpret_cast<float *>(b + l.off_logits);
+  int32_t *idx = reinterpret_cast<int32_t *>(b + l.off_idx);
+  float *p = reinterpret_cast<float *>(b + l.off_p);
+  float *sigma = reinterpret_cast<float *>(b + l.off_sigma);
+  int32_t *counts = reinterpret_cast<int32_t *>(b + l.off_counts);
+  int32_t *offsets = reinterpret_cast<int32_t *>(b + l.off_offsets);
+  int32_t *perm = reinterpret_cast<int32_t *>(b + l.off_perm);
+  float *pw = reinterpret_cast<float *>(b + l.off_pw);
+  int32_t *inv = reinterpret_cast<int32_t *>(b + l.off_inv);
+  int4 *items = reinterpret_cast<int4 *>(b + l.off_items);
+  uint16_t *xperm = reinterpret_cast<uint16_t *>(b + l.off_xperm);
+  uint16_t *h = reinterpret_cast<uint16_t *>(b + l.off_h);
+  uint16_t *o = reinterpret_cast<uint16_t *>(b + l.off_o);
+  const int sms = sm_count() > 0 ? sm_count() : 1;
+  const int H = L.hidden, I = L.inter, E = L.n_experts, k = L.top_k;
+  const int nexp = E + L.has_shared;
+  const int mt_gu = (I + kBM - 1) / kBM, mt_dn = (H + kBM - 1) / kBM;
+  const int tiles = nexp + (l.P + kBN - 1) / kBN;
+  int4 *items_gu = items;
+  int4 *items_dn = items + (size_t)tiles * mt_gu;
+
+  const int nch = T * H / 8;
+  x_perm_kernel<<<(nch + 255) / 256 < 4 * sms ? (nch + 255) / 256 : 4 * sms, 256, 0, st>>>(
+      reinterpret_cast<const uint4 *>(x), reinterpret_cast<uint4 *>(xperm), nch);
+
+  // router GEMM
+  GemmArgs ra{};
+  ra.a_bf16 = L.router;
+  ra.a_rows = E;
+  ra.K = H;
+  ra.E = E;
+  ra.b_src = x;
+  ra.mt_static = (E + kBM - 1) / kBM;
+  ra.n_items_static = ra.mt_static * ((T + kBN - 1) / kBN);
+  ra.T = T;
+  ra.logits = logits;
+  ra.bias = L.router_bias;
+  ra.hdr = hdr;
+  int rc = launch_gemm<kRouter>(ra, ra.n_items_static < sms ? ra.n_items_static : sms, st);
+  if (rc != LILY_Q4_OK) return rc;
+
+  TopkArgs ta{logits, x, L.shared_gate, T, E, H, k, L.has_shared, idx, p, sigma, counts,
+              topk_idx, topk_w};
+  topk_prefill_kernel<<<(T + 7) / 8, 256, 0, st>>>(ta);
+
+  ScanArgs sa{counts, offsets, items_gu, items_dn, hdr, T, E, k, L.has_shared, mt_gu, mt_dn};
+  scan_items_kernel<<<1, 1024, 0, st>>>(sa);
+
+  PermArgs pa{idx, p, sigma, offsets, perm, pw, inv, T, E, k};
+  perm_kernel<<<nexp, 256, 0, st>>>(pa);
+
+  GemmArgs ga{};
+  ga.a0 = L.gate;
+  ga.a1 = L.up;
+  ga.sh0 = L.sh_gate;
+  ga.sh1 = L.sh_up;
+  ga.a_rows = I;
+  ga.K = H;
+  ga.E = E;
+  ga.b_src = xperm;
+  ga.perm = perm;
+  ga.items = items_gu;
+  ga.n_items_ptr = hdr + kHdrItemsGU;
+  ga.h_out = h;
+  ga.hdr = hdr;
+  rc = launch_gemm<kGateUp>(ga, sms, st);
+  if (rc != LILY_Q4_OK) return rc;
+
+  GemmArgs da{};
+  da.a0 = L.down;
+  da.sh0 = L.sh_down;
+  da.a_rows = H;
+  da.K = I;
+  da.E = E;
+  da.b_src = h;
+  da.items = items_dn;
+  da.n_items_ptr = hdr + kHdrItemsDN;
+  da.o_out = o;
+  da.o_ld = H;
+  da.pw = pw;
+  da.hdr = hdr;
+  rc = launch_gemm<kDown>(da, sms, st);
+  if (rc != LILY_Q4_OK) return rc;
+
+  const int cch = T * H / 8;
+  combine_kernel<<<(cch + 255) / 256 < 8 * sms ? (cch + 255) / 256 : 8 * sms, 256, 0, st>>>(
+      o, inv, y, T, H, k + L.has_shared, k + 1);
+  return check_launch();
+}
+
+}  // namespace lq4

@@ -1,0 +1,147 @@
+// Device helpers shared by the kernels of the Q4 library (not by the oracle).
+//
+// In-register dequantisation of the MLX-affine 4-bit format (Lily README,
+// "Requirements": "MLX affine 4-bit ... group size 64").  For one group of 64
+// weights with scale s and bias b:
+//
+//     sum_k (s*q_k + b) x_k  =  s * sum_k q_k x_k  +  b * sum_k x_k
+//
+// so the codes are multiplied with x as small integers and s, b are applied once
+// per group.  Codes become floats with the bf16 magic-number trick: OR-ing a
+// nibble into the low mantissa bits of bf16 128.0 (0x4300) gives exactly 128+q.
+// One LOP3 turns nibbles j and j+4 of a word into such a bf16 pair.  The low half,
+// shifted up, is the fp32 value 128+q_j exactly.  The word itself read as fp32 is
+// 128.26171875 + q_{j+4} + q_j/65536; the q_j/65536 term is cancelled exactly by
+// pre-subtracting x_{j+4}/65536 from the x that multiplies the low half.  Summing
+// (w32 * x_hi + lo32 * x_lo') over the group therefore gives
+//     sum q x + 128.259765625 * X_hi + 128 * X_lo
+// where X_hi / X_lo are the sums of x over nibble positions 4..7 / 0..3; those two
+// sums depend on x only and are computed once per lane.
+#pragma once
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace lq4 {
+
+constexpr int kGroup = 64;
+constexpr float kHiOffset = 128.259765625f;  // 128 + 17152/65536 - 128/65536
+constexpr float kLoOffset = 128.0f;
+
+__device__ __forceinline__ float bf16f(uint32_t bits16) { return __uint_as_float(bits16 << 16); }
+
+__device__ __forceinline__ uint16_t f2bf16_rne(float f) {
+  uint32_t u = __float_as_uint(f);
+  u += 0x7FFFu + ((u >> 16) & 1u);
+  return (uint16_t)(u >> 16);
+}
+
+// Streaming 16-byte load: read-only, no L1 allocation (weights are read once).
+__device__ __forceinline__ uint4 ld_stream(const void *p) {
+  uint4 r;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p));
+  return r;
+}
+
+__device__ __forceinline__ uint16_t ld_u16(const uint16_t *p) {
+  uint16_t r;
+  asm volatile("ld.global.nc.u16 %0, [%1];" : "=h"(r) : "l"(p));
+  return r;
+}
+
+// One lane's share of an activation row for one 64-wide group, prepared for q4_group_dot.
+struct XGroup {
+  float2 xv[32];  // [4*m + j] = (x[8m+j+4], x[8m+j] - x[8m+j+4] * 2^-16), m = word, j = 0..3
+  float C;        // 128.259765625 * X_hi + 128 * X_lo
+  float X;        // sum of the 64 x values
+};
+
+// Build an XGroup from 64 fp32 values (in K order).
+__device__ __forceinline__ void xgroup_from(XGroup &g, const float *v) {
+  float xh = 0.f, xl = 0.f;
+#pragma unroll
+  for (int m = 0; m < 8; ++m) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      float lo = v[8 * m + j], hi = v[8 * m + j + 4];
+      g.xv[4 * m + j] = make_float2(hi, lo - hi * (1.0f / 65536.0f));
+      xh += hi;
+      xl += lo;
+    }
+  }
+  g.C = kHiOffset * xh + kLoOffset * xl;
+  g.X = xh + xl;
+}
+
+// 64 bf16 values (8 x 16-byte chunks in K order) -> XGroup.
+__device__ __forceinline__ void xgroup_from_bf16(XGroup &g, const uint4 *chunks) {
+  float v[64];
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    const uint4 u = chunks[c];
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      v[8 * c + 2 * i] = __uint_as_float(w[i] << 16);
+      v[8 * c + 2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+    }
+  }
+  xgroup_from(g, v);
+}
+
+// sum_k q_k * x_k + C for one group of 8 words (accumulation only, s/b not applied).
+__device__ __forceinline__ float q4_group_raw(const uint4 w0, const uint4 w1, const XGroup &g) {
+  const uint32_t w[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+  float2 a0 = make_float2(0.f, 0.f), a1 = make_float2(0.f, 0.f);
+#pragma unroll
+  for (int m = 0; m < 8; ++m) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const uint32_t v = ((w[m] >> (4 * j)) & 0x000F000Fu) | 0x43004300u;
+      const float2 f = make_float2(__uint_as_float(v), __uint_as_float(v << 16));
+      if (j & 1)
+        a1 = __ffma2_rn(f, g.xv[4 * m + j], a1);
+      else
+        a0 = __ffma2_rn(f, g.xv[4 * m + j], a0);
+    }
+  }
+  return (a0.x + a1.x) + (a0.y + a1.y);
+}
+
+// Dot product of one dequantised 64-group with the prepared x: s*(sum q x) + b*(sum x).
+__device__ __forceinline__ float q4_group_dot(const uint4 w0, const uint4 w1, const XGroup &g,
+                                              float s, float b) {
+  const float A = q4_group_raw(w0, w1, g);
+  return fmaf(s, A - g.C, b * g.X);
+}
+
+// Sum over the lanes of a segment of `width` consecutive lanes (width a power of two).
+template <int W>
+__device__ __forceinline__ float seg_sum(float v) {
+#pragma unroll
+  for (int o = W / 2; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// Warp-wide exclusive scan of one int per lane; returns the lane's prefix, *total = sum.
+__device__ __forceinline__ int warp_excl_scan(int v, int *total) {
+  const int lane = threadIdx.x & 31;
+  int incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    int n = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += n;
+  }
+  *total = __shfl_sync(0xffffffffu, incl, 31);
+  return incl - v;
+}
+
+__device__ __forceinline__ float silu_mul(float g, float u) { return g / (1.0f + __expf(-g)) * u; }
+
+// (value, index) ordering used by every argmax / top-k: larger value first, then lower index.
+__device__ __forceinline__ bool better(float va, int ia, float vb, int ib) {
+  return va > vb || (va == vb && ia < ib);
+}
+
+}  // namespace lq4

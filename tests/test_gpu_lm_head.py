@@ -1,0 +1,90 @@
+"""GPU parity of lily_q4_gemv_argmax (Q4 LM-head GEMV + greedy argmax) against the oracle.
+
+Token ids must be identical; logits within the output tolerance (see helpers.py)."""
+import numpy as np
+import pytest
+
+import bit_affine_quantized_mlx_gb300 as q4
+from bit_affine_quantized_mlx_gb300 import synth
+from bit_affine_quantized_mlx_gb300.synth import Q4Matrix
+from helpers import assert_close
+from oracle import oracle as orc
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def torch_dev():
+    import torch
+    import __graft_entry__
+    __graft_entry__.build()
+    return torch, torch.device("cuda:0")
+
+
+def _run(torch, dev, W, x_bits, with_logits=True):
+    N, K = W.N, W.K
+    dW = q4.DeviceQ4.upload(W, dev)
+    xd = q4.to_device(x_bits, dev)
+    tok = torch.full((1,), -7, dtype=torch.int32, device=dev)
+    lg = torch.empty(N, dtype=torch.float32, device=dev) if with_logits else None
+    ws = q4.new_workspace(q4.lily_q4_gemv_argmax_workspace_bytes(N, K), dev)
+    q4.lily_q4_gemv_argmax(dW, xd, tok, logits=lg, ws=ws)
+    torch.cuda.synchronize()
+    return int(tok.item()), (lg.cpu().numpy().astype(np.float64) if with_logits else None)
+
+
+@pytest.mark.parametrize("N,K", [(1, 64), (37, 128), (1000, 256), (4097, 512), (333, 1024),
+                                 (50001, 2048)])
+def test_shapes(torch_dev, N, K):
+    torch, dev = torch_dev
+    W = synth.draw_q4(N, K, 60, N, K)
+    if N == 1:
+        x = synth.draw_x(K, (60, N), 0, 0)
+        tok, lg = orc.lm_head(W, x)
+    else:
+        x, _, tok, lg = orc.lm_x_without_near_tie(W, lambda a: synth.draw_x(K, (60, N), 0, a))
+    got_tok, got_lg = _run(torch, dev, W, x)
+    assert got_tok == tok
+    assert_close(got_lg, lg, f"logits N={N} K={K}")
+
+
+def test_full_size_lm_head(torch_dev):
+    """The LM-head workload at its full size (vocab 151,936 x hidden 2048), every logit checked."""
+    torch, dev = torch_dev
+    wl = synth.LMHEAD
+    W = synth.draw_lm_head(wl.V, wl.H)
+    x, attempt, tok, lg = orc.lm_x_without_near_tie(W, lambda a: synth.draw_lm_x(wl.H, attempt=a))
+    got_tok, got_lg = _run(torch, dev, W, x)
+    assert got_tok == tok
+    assert_close(got_lg, lg, "full LM head")
+    # without the logits output, same token
+    got_tok2, _ = _run(torch, dev, W, x, with_logits=False)
+    assert got_tok2 == tok
+
+
+def test_planted_tie_goes_to_lower_index(torch_dev):
+    torch, dev = torch_dev
+    N, K = 3000, 512
+    W = synth.draw_q4(N, K, 61, 0)
+    w, s, b = W.w.copy(), W.s.copy(), W.b.copy()
+    # rows 1234 and 2345 identical and dominant: all codes 15, scale +, bias 0
+    for r in (2345, 1234):
+        w[r] = 0xFFFFFFFF
+        s[r] = synth.bf16_from_f32(np.float32(0.05))
+        b[r] = 0
+    x = np.full(K, synth.bf16_from_f32(np.float32(0.5)).item(), np.uint16)
+    W2 = Q4Matrix(w, s, b)
+    tok, lg = orc.lm_head(W2, x)
+    assert tok == 1234 and lg[1234] == lg[2345]
+    got_tok, got_lg = _run(torch, dev, W2, x)
+    assert got_tok == 1234
+    assert got_lg[1234] == got_lg[2345]
+
+
+def test_deterministic(torch_dev):
+    torch, dev = torch_dev
+    W = synth.draw_q4(20000, 2048, 62, 0)
+    x = synth.draw_x(2048, (62, 0), 0, 0)
+    a = _run(torch, dev, W, x)
+    b = _run(torch, dev, W, x)
+    assert a[0] == b[0] and np.array_equal(a[1], b[1])

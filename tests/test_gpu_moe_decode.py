@@ -1,0 +1,115 @@
+"""GPU parity of lily_q4_moe_decode against the oracle.
+
+Top-k expert sets must be identical per token (weights per expert within 1e-5); y within
+the output tolerance.  Inputs are redrawn per token until the oracle's k-th and (k+1)-th
+router logits differ by at least 1e-3."""
+import numpy as np
+import pytest
+
+import bit_affine_quantized_mlx_gb300 as q4
+from bit_affine_quantized_mlx_gb300 import synth
+from helpers import assert_close, assert_topk_equal, bf16_bits_to_f64
+from oracle import oracle as orc
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def torch_dev():
+    import torch
+    import __graft_entry__
+    __graft_entry__.build()
+    return torch, torch.device("cuda:0")
+
+
+def _inputs(L, key, T):
+    return orc.tokens_without_near_ties(L, lambda t, a: synth.draw_x(L.H, key, t, a), T)[0]
+
+
+def run_decode(torch, dev, dl, x_bits, ws=None):
+    T = x_bits.shape[0]
+    xd = q4.to_device(x_bits, dev)
+    y = torch.empty_like(xd)
+    idx = torch.full((T, dl.k), -1, dtype=torch.int32, device=dev)
+    w = torch.empty((T, dl.k), dtype=torch.float32, device=dev)
+    if ws is None:
+        ws = q4.new_workspace(q4.lily_q4_moe_workspace_bytes(dl, T), dev)
+    q4.lily_q4_moe_decode(dl, xd, y, topk_idx=idx, topk_w=w, ws=ws)
+    torch.cuda.synchronize()
+    return bf16_bits_to_f64(y), idx.cpu().numpy(), w.cpu().numpy()
+
+
+def check(torch, dev, L, x, what, ws=None, dl=None):
+    ref = orc.moe(L, x)
+    dl = dl or q4.DeviceLayer.upload(L, dev)
+    y, idx, w = run_decode(torch, dev, dl, x, ws)
+    assert_topk_equal(idx, w, ref, what)
+    assert_close(y, ref["y"], what)
+    return y
+
+
+def test_tiny_workload_seed0(torch_dev):
+    """The tiny layer (hidden 256, 16 experts, top-2, intermediate 128, no shared), seed 0."""
+    torch, dev = torch_dev
+    wl = synth.TINY
+    L = wl.layer(0)
+    check(torch, dev, L, _inputs(L, wl.tokens_key(0), 1), "tiny")
+
+
+@pytest.mark.parametrize("H,E,k,I,shared,bias,T", [
+    (64, 4, 2, 64, False, False, 1),
+    (128, 8, 8, 64, True, True, 3),      # k == E: every expert
+    (256, 16, 2, 128, False, False, 16),  # largest batch
+    (512, 32, 4, 256, True, False, 5),
+    (1024, 64, 16, 128, True, True, 2),   # largest k
+    (2048, 40, 3, 2048, True, False, 2),  # widest intermediate
+    (256, 1024, 5, 128, True, False, 3),  # most experts
+])
+def test_shapes(torch_dev, H, E, k, I, shared, bias, T):
+    torch, dev = torch_dev
+    key = (70, H * 7 + E + T)
+    L = synth.draw_layer(H, E, k, I, shared=shared, router_std=0.05, router_bias=bias, key=key)
+    check(torch, dev, L, _inputs(L, key, T), f"H{H} E{E} k{k} I{I} T{T}")
+
+
+@pytest.mark.parametrize("layer,T", [(0, 1), (0, 4), (39, 1), (39, 4)])
+def test_decode_workload_full_size(torch_dev, layer, T):
+    """Decode layer at hidden 2048, 256 experts, top-8 + shared, intermediate 512."""
+    torch, dev = torch_dev
+    wl = synth.DECODE
+    L = wl.layer(layer)
+    check(torch, dev, L, _inputs(L, wl.tokens_key(layer), T), f"decode layer {layer} T{T}")
+
+
+@pytest.mark.parametrize("T", [1, 2, 4])
+def test_wide_workload_full_size(torch_dev, T):
+    """Wide layer at hidden 2048, 512 experts, top-10 + shared, intermediate 512."""
+    torch, dev = torch_dev
+    wl = synth.WIDE
+    L = wl.layer(47)
+    check(torch, dev, L, _inputs(L, wl.tokens_key(47), T), f"wide T{T}")
+
+
+def test_repeated_tokens_share_experts(torch_dev):
+    """Identical tokens choose identical experts: each expert serves several tokens."""
+    torch, dev = torch_dev
+    key = (71, 0)
+    L = synth.draw_layer(512, 16, 4, 256, shared=True, router_std=0.05, router_bias=False, key=key)
+    x1 = _inputs(L, key, 1)
+    x = np.repeat(x1, 6, axis=0)
+    y = check(torch, dev, L, x, "repeated")
+    assert np.all(y == y[0])
+
+
+def test_deterministic_and_workspace_reuse(torch_dev):
+    torch, dev = torch_dev
+    wl = synth.DECODE
+    L = wl.layer(1)
+    dl = q4.DeviceLayer.upload(L, dev)
+    x4 = _inputs(L, wl.tokens_key(1), 4)
+    ws = q4.new_workspace(q4.lily_q4_moe_workspace_bytes(dl, 4), dev)
+    a = run_decode(torch, dev, dl, x4, ws)
+    b = run_decode(torch, dev, dl, x4[:1], ws)   # smaller T in the same workspace
+    c = run_decode(torch, dev, dl, x4, ws)
+    assert np.array_equal(a[0], c[0]) and np.array_equal(a[1], c[1])
+    assert np.array_equal(a[0][0], b[0][0])

@@ -1,0 +1,115 @@
+"""GPU parity of lily_q4_moe_prefill (tcgen05 grouped GEMM) against the oracle.
+
+Top-k sets identical per token; y within the output tolerance.  At the full prompt-chunk
+size (2048 tokens) every token's routing is checked and y is checked on a sample of
+tokens the oracle computes one by one."""
+import numpy as np
+import pytest
+
+import bit_affine_quantized_mlx_gb300 as q4
+from bit_affine_quantized_mlx_gb300 import synth
+from helpers import assert_close, assert_topk_equal, bf16_bits_to_f64
+from oracle import oracle as orc
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def torch_dev():
+    import torch
+    import __graft_entry__
+    __graft_entry__.build()
+    return torch, torch.device("cuda:0")
+
+
+def _inputs(L, key, T):
+    return orc.tokens_without_near_ties(L, lambda t, a: synth.draw_x(L.H, key, t, a), T)[0]
+
+
+def run_prefill(torch, dev, dl, x_bits, ws=None):
+    T = x_bits.shape[0]
+    xd = q4.to_device(x_bits, dev)
+    y = torch.empty_like(xd)
+    idx = torch.full((T, dl.k), -1, dtype=torch.int32, device=dev)
+    w = torch.empty((T, dl.k), dtype=torch.float32, device=dev)
+    if ws is None:
+        ws = q4.new_workspace(q4.lily_q4_moe_workspace_bytes(dl, T, prefill=True), dev)
+    q4.lily_q4_moe_prefill(dl, xd, y, topk_idx=idx, topk_w=w, ws=ws)
+    torch.cuda.synchronize()
+    assert q4.lily_q4_workspace_status(ws) == 0, "a bounded device-side wait timed out"
+    return bf16_bits_to_f64(y), idx.cpu().numpy(), w.cpu().numpy()
+
+
+@pytest.mark.parametrize("H,E,k,I,shared,bias,T", [
+    (128, 8, 2, 128, True, True, 37),
+    (256, 16, 4, 256, True, False, 300),    # > 128 tokens per expert: several token tiles
+    (512, 32, 8, 128, False, True, 129),
+    (2048, 4, 2, 512, True, False, 1),      # a single token
+    (256, 64, 6, 1024, True, True, 200),
+])
+def test_shapes(torch_dev, H, E, k, I, shared, bias, T):
+    torch, dev = torch_dev
+    key = (80, H + E + T)
+    L = synth.draw_layer(H, E, k, I, shared=shared, router_std=0.05, router_bias=bias, key=key)
+    x = _inputs(L, key, T)
+    ref = orc.moe(L, x)
+    dl = q4.DeviceLayer.upload(L, dev)
+    y, idx, w = run_prefill(torch, dev, dl, x)
+    what = f"H{H} E{E} k{k} I{I} T{T}"
+    assert_topk_equal(idx, w, ref, what)
+    assert_close(y, ref["y"], what)
+
+
+def test_prefill_matches_decode_path(torch_dev):
+    """The tensor-core path and the decode path agree on the same tokens."""
+    torch, dev = torch_dev
+    key = (81, 0)
+    L = synth.draw_layer(512, 16, 4, 256, shared=True, router_std=0.05, router_bias=False, key=key)
+    x = _inputs(L, key, 16)
+    dl = q4.DeviceLayer.upload(L, dev)
+    yp, ip, _ = run_prefill(torch, dev, dl, x)
+    xd = q4.to_device(x, dev)
+    yd = torch.empty_like(xd)
+    ws = q4.new_workspace(q4.lily_q4_moe_workspace_bytes(dl, 16), dev)
+    q4.lily_q4_moe_decode(dl, xd, yd, ws=ws)
+    torch.cuda.synchronize()
+    assert_close(yp, bf16_bits_to_f64(yd), "prefill vs decode")
+
+
+def test_prefill_workload_full_size_sampled(torch_dev):
+    """2048-token chunk through a 256-expert top-8 + shared layer with skewed router offsets."""
+    torch, dev = torch_dev
+    wl = synth.PREFILL
+    L = wl.layer(0)
+    T = wl.tokens[0]
+    x = _inputs(L, wl.tokens_key(0), T)
+    dl = q4.DeviceLayer.upload(L, dev)
+    y, idx, w = run_prefill(torch, dev, dl, x)
+    # routing of every token
+    lg = orc.router_tokens(L, x)
+    for t in range(T):
+        ref_idx, ref_p = orc.topk(lg[t], L.k)
+        assert sorted(idx[t].tolist()) == sorted(ref_idx.tolist()), t
+    # load is skewed as intended (uneven tokens per expert)
+    counts = np.bincount(idx.ravel(), minlength=L.E)
+    assert counts.max() > 2 * counts.mean()
+    # outputs on a sample of tokens
+    rng = np.random.default_rng(0)
+    sample = np.sort(rng.choice(T, 96, replace=False))
+    ref = orc.moe(L, x[sample])
+    assert_topk_equal(idx[sample], w[sample], ref, "prefill sample")
+    assert_close(y[sample], ref["y"], "prefill full-size sample")
+
+
+def test_deterministic(torch_dev):
+    torch, dev = torch_dev
+    key = (82, 0)
+    L = synth.draw_layer(1024, 32, 4, 512, shared=True, router_std=0.05, router_bias=True, key=key)
+    x = _inputs(L, key, 400)
+    dl = q4.DeviceLayer.upload(L, dev)
+    ws = q4.new_workspace(q4.lily_q4_moe_workspace_bytes(dl, 400, prefill=True), dev)
+    a = run_prefill(torch, dev, dl, x, ws)
+    b = run_prefill(torch, dev, dl, x[:100], ws)
+    c = run_prefill(torch, dev, dl, x, ws)
+    assert np.array_equal(a[0], c[0]) and np.array_equal(a[1], c[1])
+    assert b[0].shape == (100, 1024)
