@@ -101,6 +101,136 @@ struct RouterArgs {
   float *out_w;
 };
 
+// Routing bookkeeping of T tokens by one block of NT threads: top-k per token (a warp per
+// token, logit desc / index asc), softmax over the k, the unique experts (ascending id, the
+// shared expert last, id E) and their (token, combine weight) pairs.  `logits` and `sigma`
+// were written by other blocks (read through L2).  Outputs go through generic pointers.
+struct RouteDst {
+  int32_t *idx;
+  float *p;
+  int32_t *U;
+  int32_t *uexp;
+  int32_t *ubase;
+  int32_t *pair_tok;
+  float *pair_w;
+  int32_t *pair_e;
+  int32_t *out_idx;
+  float *out_w;
+};
+
+template <int NT>
+__device__ void route_block(const float *logits, const float *sigma, int T, int E, int k,
+                            int has_shared, const RouteDst &d) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  __shared__ int s_idx[kMaxT * kMaxK];
+  __shared__ float s_p[kMaxT * kMaxK];
+  __shared__ int s_cnt[1024];
+  __shared__ int s_base[1024];
+
+  // top-k per token: warp per token, k rounds of a warp argmax over unselected experts
+  for (int t = warp; t < T; t += NT / 32) {
+    const float *lg = logits + (size_t)t * E;
+    uint32_t taken = 0;  // bit j: expert lane + 32 j already selected
+    float v0 = 0.f, denom = 0.f;
+    float sel_v[kMaxK];
+    int sel_e[kMaxK];
+    for (int i = 0; i < k; ++i) {
+      float bv = -FLT_MAX;
+      int be = INT_MAX;
+      for (int j = 0; lane + 32 * j < E; ++j) {
+        const int e = lane + 32 * j;
+        if (taken & (1u << j)) continue;
+        const float v = __ldcg(lg + e);
+        if (better(v, e, bv, be)) {
+          bv = v;
+          be = e;
+        }
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+        const int oe = __shfl_xor_sync(0xffffffffu, be, o);
+        if (better(ov, oe, bv, be)) {
+          bv = ov;
+          be = oe;
+        }
+      }
+      if ((be & 31) == lane) taken |= 1u << (be >> 5);
+      sel_v[i] = bv;
+      sel_e[i] = be;
+    }
+    v0 = sel_v[0];
+    for (int i = 0; i < k; ++i) denom += expf(sel_v[i] - v0);
+    if (lane == 0) {
+      for (int i = 0; i < k; ++i) {
+        const float pi = expf(sel_v[i] - v0) / denom;
+        s_idx[t * k + i] = sel_e[i];
+        s_p[t * k + i] = pi;
+        if (d.idx) d.idx[t * k + i] = sel_e[i];
+        if (d.p) d.p[t * k + i] = pi;
+        if (d.out_idx) d.out_idx[t * k + i] = sel_e[i];
+        if (d.out_w) d.out_w[t * k + i] = pi;
+      }
+    }
+  }
+  for (int e = threadIdx.x; e < E; e += NT) s_cnt[e] = 0;
+  __syncthreads();
+  for (int j = threadIdx.x; j < T * k; j += NT) atomicAdd(&s_cnt[s_idx[j]], 1);
+  __syncthreads();
+  if (warp == 0) {
+    // rank (exclusive count of present experts) and base (exclusive sum of counts)
+    const int per = (E + 31) / 32;
+    const int lo = lane * per, hi = min(E, lo + per);
+    int np = 0, nc = 0;
+    for (int e = lo; e < hi; ++e) {
+      np += s_cnt[e] > 0;
+      nc += s_cnt[e];
+    }
+    int totp, totc;
+    int rp = warp_excl_scan(np, &totp);
+    int rc = warp_excl_scan(nc, &totc);
+    for (int e = lo; e < hi; ++e) {
+      s_base[e] = rc;
+      if (s_cnt[e] > 0) {
+        d.uexp[rp] = e;
+        d.ubase[rp] = rc;
+        ++rp;
+      }
+      rc += s_cnt[e];
+    }
+    if (lane == 0) {
+      int U = totp;
+      if (has_shared) {
+        d.uexp[U] = E;  // the shared expert
+        d.ubase[U] = totc;
+        ++U;
+      }
+      d.ubase[U] = totc + (has_shared ? T : 0);
+      *d.U = U;
+    }
+  }
+  __syncthreads();
+  // pairs: (token t, slot i) -> position base[e] + (number of earlier tokens that chose e)
+  for (int j = threadIdx.x; j < T * k; j += NT) {
+    const int t = j / k, e = s_idx[j];
+    int pos = 0;
+    for (int jj = 0; jj < t * k; ++jj) pos += (s_idx[jj] == e);
+    const int pr = s_base[e] + pos;
+    d.pair_tok[pr] = t;
+    d.pair_w[pr] = s_p[j];
+    d.pair_e[pr] = e;
+  }
+  if (has_shared) {
+    for (int t = threadIdx.x; t < T; t += NT) {
+      const int pr = T * k + t;
+      d.pair_tok[pr] = t;
+      d.pair_w[pr] = __ldcg(sigma + t);
+      d.pair_e[pr] = E;
+    }
+  }
+  __syncthreads();
+}
+
 // ---------------------------------------------------------------------------------------
 // 1. router logits + shared gate; last block: top-k, gates, unique-expert pairs
 // ---------------------------------------------------------------------------------------
@@ -155,115 +285,9 @@ __global__ void __launch_bounds__(kRouterThreads)
   if (!is_last) return;
   __threadfence();
 
-  __shared__ int s_idx[kMaxT * kMaxK];
-  __shared__ float s_p[kMaxT * kMaxK];
-  __shared__ int s_cnt[1024];
-  __shared__ int s_base[1024];
-  __shared__ int s_rank[1024];
-  const int E = a.E, k = a.k, T = a.T;
-
-  // top-k per token: warp per token, k rounds of a warp argmax over unselected experts
-  for (int t = warp; t < T; t += kRouterThreads / 32) {
-    const float *lg = w.logits + (size_t)t * E;
-    uint32_t taken = 0;  // bit j: expert lane + 32 j already selected
-    float v0 = 0.f, denom = 0.f;
-    float sel_v[kMaxK];
-    int sel_e[kMaxK];
-    for (int i = 0; i < k; ++i) {
-      float bv = -FLT_MAX;
-      int be = INT_MAX;
-      for (int j = 0; lane + 32 * j < E; ++j) {
-        const int e = lane + 32 * j;
-        if (taken & (1u << j)) continue;
-        const float v = __ldcg(lg + e);
-        if (better(v, e, bv, be)) {
-          bv = v;
-          be = e;
-        }
-      }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-        const int oe = __shfl_xor_sync(0xffffffffu, be, o);
-        if (better(ov, oe, bv, be)) {
-          bv = ov;
-          be = oe;
-        }
-      }
-      if ((be & 31) == lane) taken |= 1u << (be >> 5);
-      sel_v[i] = bv;
-      sel_e[i] = be;
-    }
-    v0 = sel_v[0];
-    for (int i = 0; i < k; ++i) denom += expf(sel_v[i] - v0);
-    if (lane == 0) {
-      for (int i = 0; i < k; ++i) {
-        const float pi = expf(sel_v[i] - v0) / denom;
-        s_idx[t * k + i] = sel_e[i];
-        s_p[t * k + i] = pi;
-        w.idx[t * k + i] = sel_e[i];
-        w.p[t * k + i] = pi;
-        if (a.out_idx) a.out_idx[t * k + i] = sel_e[i];
-        if (a.out_w) a.out_w[t * k + i] = pi;
-      }
-    }
-  }
-  for (int e = threadIdx.x; e < E; e += kRouterThreads) s_cnt[e] = 0;
-  __syncthreads();
-  for (int j = threadIdx.x; j < T * k; j += kRouterThreads) atomicAdd(&s_cnt[s_idx[j]], 1);
-  __syncthreads();
-  if (warp == 0) {
-    // rank (exclusive count of present experts) and base (exclusive sum of counts)
-    const int per = (E + 31) / 32;
-    const int lo = lane * per, hi = min(E, lo + per);
-    int np = 0, nc = 0;
-    for (int e = lo; e < hi; ++e) {
-      np += s_cnt[e] > 0;
-      nc += s_cnt[e];
-    }
-    int totp, totc;
-    int rp = warp_excl_scan(np, &totp);
-    int rc = warp_excl_scan(nc, &totc);
-    for (int e = lo; e < hi; ++e) {
-      s_rank[e] = rp;
-      s_base[e] = rc;
-      if (s_cnt[e] > 0) {
-        w.uexp()[rp] = e;
-        w.ubase()[rp] = rc;
-        ++rp;
-      }
-      rc += s_cnt[e];
-    }
-    if (lane == 0) {
-      int U = totp;
-      if (a.has_shared) {
-        w.uexp()[U] = E;  // the shared expert
-        w.ubase()[U] = totc;
-        ++U;
-      }
-      w.ubase()[U] = totc + (a.has_shared ? T : 0);
-      w.meta[0] = U;
-    }
-  }
-  __syncthreads();
-  // pairs: (token t, slot i) -> position base[e] + (number of earlier tokens that chose e)
-  for (int j = threadIdx.x; j < T * k; j += kRouterThreads) {
-    const int t = j / k, e = s_idx[j];
-    int pos = 0;
-    for (int jj = 0; jj < t * k; ++jj) pos += (s_idx[jj] == e);
-    const int pr = s_base[e] + pos;
-    w.pair_tok[pr] = t;
-    w.pair_w[pr] = s_p[j];
-    w.pair_e()[pr] = e;
-  }
-  if (a.has_shared) {
-    for (int t = threadIdx.x; t < T; t += kRouterThreads) {
-      const int pr = T * k + t;
-      w.pair_tok[pr] = t;
-      w.pair_w[pr] = __ldcg(w.sigma + t);
-      w.pair_e()[pr] = E;
-    }
-  }
+  RouteDst d{w.idx, w.p, w.meta, w.uexp(), w.ubase(), w.pair_tok, w.pair_w, w.pair_e(),
+             a.out_idx, a.out_w};
+  route_block<kRouterThreads>(w.logits, w.sigma, a.T, a.E, a.k, a.has_shared, d);
   if (threadIdx.x == 0) w.hdr[kHdrCounterB] = 0;
 }
 
@@ -422,6 +446,314 @@ __global__ void __launch_bounds__(kDownThreads)
   }
 }
 
+
+// ---------------------------------------------------------------------------------------
+// Single-launch decode layer (cooperative, one block per SM, two grid barriers)
+//
+//   phase A: router rows (+ the shared gate row) and the shared expert's gate/up rows,
+//            none of which depends on the routing; down-row owners prefetch the shared
+//            expert's down rows into L2
+//   barrier
+//   phase B: every block takes the routing of all tokens from the logits (identical
+//            result in every block); routed gate/up rows; owners run the shared expert's
+//            down rows and prefetch their routed down rows into L2
+//   barrier
+//   phase C: h of every pair staged in shared memory; owners run the routed down rows,
+//            add them to the shared-expert partial in a fixed order and write y
+// ---------------------------------------------------------------------------------------
+constexpr int kFusedThreads = 256;
+constexpr int kFusedWarps = kFusedThreads / 32;
+constexpr size_t kFusedSmemMax = 100 * 1024;
+constexpr int kFusedMaxT = 4;
+constexpr long long kBarrierCycles = 2000000000LL;  // ~1 s
+
+struct FusedArgs {
+  lily_q4_mat gate, up, down, sh_gate, sh_up, sh_down;
+  const uint16_t *router;
+  const float *bias;
+  const uint16_t *shared_gate;
+  const uint16_t *x;
+  uint16_t *y;
+  int T, E, H, I, k, has_shared;
+  int32_t *out_idx;
+  float *out_w;
+};
+
+__device__ __forceinline__ int ld_acquire(const int32_t *p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void prefetch_l2(const void *p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
+// Self-resetting grid barrier (count word, generation word) with a bounded wait.
+__device__ bool grid_barrier(int32_t *hdr, volatile int *s_abort) {
+  __syncthreads();
+  if (threadIdx.x == 0 && !*s_abort) {
+    int32_t *cnt = hdr + kHdrCounterC, *gen = hdr + kHdrCounterC + 1;
+    const int g = ld_acquire(gen);
+    __threadfence();
+    if (atomicAdd(cnt, 1) == (int)gridDim.x - 1) {
+      *(volatile int32_t *)cnt = 0;
+      __threadfence();
+      atomicAdd(gen, 1);
+    } else {
+      const long long t0 = clock64();
+      while (ld_acquire(gen) == g) {
+        if (clock64() - t0 > kBarrierCycles) {
+          atomicExch(hdr + kHdrError, 2);
+          *s_abort = 1;
+          break;
+        }
+        __nanosleep(64);
+      }
+    }
+    __threadfence();
+  }
+  __syncthreads();
+  return !*s_abort;
+}
+
+template <int GH, int GI>
+__global__ void __launch_bounds__(kFusedThreads, 1)
+    moe_decode_fused_kernel(FusedArgs a, DecodePtrs w) {
+  extern __shared__ float s_h[];  // [P][I] (phase C) / [T][I] shared h (phase B)
+  __shared__ int32_t s_U;
+  __shared__ int32_t s_uexp[kMaxT * kMaxK + 1];
+  __shared__ int32_t s_ubase[kMaxT * kMaxK + 2];
+  __shared__ int32_t s_pair_tok[kMaxPairs];
+  __shared__ int32_t s_pair_e[kMaxPairs];
+  __shared__ float s_pair_w[kMaxPairs];
+  __shared__ volatile int s_abort;
+  constexpr int RPS_H = 32 / GH;  // rows per warp-step, K = H (gate/up)
+  constexpr int RPS_I = 32 / GI;  // rows per warp-step, K = I (down)
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int nw = gridDim.x * kFusedWarps;
+  const int gw = warp * gridDim.x + blockIdx.x;  // interleaved: consecutive tasks on different SMs
+  const int T = a.T, E = a.E, H = a.H, I = a.I, k = a.k;
+  const int nrouter = E + a.has_shared;
+  const int gh = lane % GH, rh = lane / GH;
+  const int gi = lane % GI, ri = lane / GI;
+  const int nquads = H / RPS_I;  // down row-steps
+  if (threadIdx.x == 0) s_abort = 0;
+  __syncthreads();
+
+  // ------------------------------------------------------------------ phase A
+  const int nshared_tasks = a.has_shared ? I / RPS_H : 0;
+  for (int task = gw; task < nrouter + nshared_tasks; task += nw) {
+    if (task < nrouter) {
+      const int row = task;
+      const uint16_t *wr = row < E ? a.router + (size_t)row * H : a.shared_gate;
+      const int nchunk = H / 8;
+      uint4 wv[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int c = lane + 32 * j;
+        wv[j] = c < nchunk ? ld_stream(wr + 8 * c) : make_uint4(0, 0, 0, 0);
+      }
+      for (int t = 0; t < T; ++t) {
+        const uint16_t *xt = a.x + (size_t)t * H;
+        float acc = 0.f;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const int c = lane + 32 * j;
+          if (c < nchunk) {
+            const uint4 xv = __ldg(reinterpret_cast<const uint4 *>(xt + 8 * c));
+            const uint32_t ww[4] = {wv[j].x, wv[j].y, wv[j].z, wv[j].w};
+            const uint32_t xx[4] = {xv.x, xv.y, xv.z, xv.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              acc = fmaf(__uint_as_float(ww[i] << 16), __uint_as_float(xx[i] << 16), acc);
+              acc = fmaf(__uint_as_float(ww[i] & 0xFFFF0000u), __uint_as_float(xx[i] & 0xFFFF0000u),
+                         acc);
+            }
+          }
+        }
+        acc = seg_sum<32>(acc);
+        if (lane == 0) {
+          if (row < E)
+            __stcg(w.logits + (size_t)t * E + row, acc + (a.bias ? a.bias[row] : 0.f));
+          else
+            __stcg(w.sigma + t, 1.0f / (1.0f + expf(-acc)));
+        }
+      }
+    } else {
+      // shared expert gate/up rows (one warp-step of RPS_H rows)
+      const int row = (task - nrouter) * RPS_H + rh;
+      const size_t wo = (size_t)row * (GH * 8) + 8 * gh, so = (size_t)row * GH + gh;
+      const uint4 g0 = ld_stream(a.sh_gate.w + wo), g1 = ld_stream(a.sh_gate.w + wo + 4);
+      const uint4 u0 = ld_stream(a.sh_up.w + wo), u1 = ld_stream(a.sh_up.w + wo + 4);
+      const float gs = bf16f(ld_u16(a.sh_gate.s + so)), gb = bf16f(ld_u16(a.sh_gate.b + so));
+      const float us = bf16f(ld_u16(a.sh_up.s + so)), ub = bf16f(ld_u16(a.sh_up.b + so));
+      for (int t = 0; t < T; ++t) {
+        XGroup xg;
+        uint4 c[8];
+        const uint4 *xp = reinterpret_cast<const uint4 *>(a.x + (size_t)t * H + kGroup * gh);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) c[i] = __ldg(xp + i);
+        xgroup_from_bf16(xg, c);
+        const float gd = seg_sum<GH>(q4_group_dot(g0, g1, xg, gs, gb));
+        const float ud = seg_sum<GH>(q4_group_dot(u0, u1, xg, us, ub));
+        // shared pairs sit after the T*k routed pairs
+        if (gh == 0) __stcg(w.h + (size_t)(T * k + t) * I + row, silu_mul(gd, ud));
+      }
+    }
+  }
+  // owners of down rows prefetch the shared expert's down rows
+  if (a.has_shared && lane == 0) {
+    for (int q = blockIdx.x + gridDim.x * warp; q < nquads; q += nw) {
+      const size_t r0 = (size_t)q * RPS_I;
+      prefetch_l2(a.sh_down.w + r0 * (GI * 8), RPS_I * GI * 32);
+      prefetch_l2(a.sh_down.s + r0 * GI, RPS_I * GI * 2 < 16 ? 16 : RPS_I * GI * 2);
+      prefetch_l2(a.sh_down.b + r0 * GI, RPS_I * GI * 2 < 16 ? 16 : RPS_I * GI * 2);
+    }
+  }
+  if (!grid_barrier(w.hdr, &s_abort)) return;
+
+  // ------------------------------------------------------------------ phase B
+  {
+    RouteDst d{nullptr, nullptr, &s_U, s_uexp, s_ubase, s_pair_tok, s_pair_w, s_pair_e,
+               blockIdx.x == 0 ? a.out_idx : nullptr, blockIdx.x == 0 ? a.out_w : nullptr};
+    route_block<kFusedThreads>(w.logits, w.sigma, T, E, k, a.has_shared, d);
+  }
+  const int U = s_U;
+  const int Ur = a.has_shared ? U - 1 : U;  // routed unique experts
+  const int Pr = s_ubase[Ur];               // routed pairs
+  // routed gate/up: tasks (unique expert, row-step)
+  const int steps_h = I / RPS_H;
+  for (int task = gw; task < Ur * steps_h; task += nw) {
+    const int u = task / steps_h;
+    const int row = (task % steps_h) * RPS_H + rh;
+    const int e = s_uexp[u];
+    const size_t wo = ((size_t)e * I + row) * (GH * 8) + 8 * gh;
+    const size_t so = ((size_t)e * I + row) * GH + gh;
+    const uint4 g0 = ld_stream(a.gate.w + wo), g1 = ld_stream(a.gate.w + wo + 4);
+    const uint4 u0 = ld_stream(a.up.w + wo), u1 = ld_stream(a.up.w + wo + 4);
+    const float gs = bf16f(ld_u16(a.gate.s + so)), gb = bf16f(ld_u16(a.gate.b + so));
+    const float us = bf16f(ld_u16(a.up.s + so)), ub = bf16f(ld_u16(a.up.b + so));
+    for (int pr = s_ubase[u]; pr < s_ubase[u + 1]; ++pr) {
+      const int t = s_pair_tok[pr];
+      XGroup xg;
+      uint4 c[8];
+      const uint4 *xp = reinterpret_cast<const uint4 *>(a.x + (size_t)t * H + kGroup * gh);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) c[i] = __ldg(xp + i);
+      xgroup_from_bf16(xg, c);
+      const float gd = seg_sum<GH>(q4_group_dot(g0, g1, xg, gs, gb));
+      const float ud = seg_sum<GH>(q4_group_dot(u0, u1, xg, us, ub));
+      if (gh == 0) __stcg(w.h + (size_t)pr * I + row, silu_mul(gd, ud));
+    }
+  }
+  // owners: shared-expert down rows (h_shared staged in shared memory first), routed prefetch
+  float yacc[kFusedMaxT];
+#pragma unroll
+  for (int t = 0; t < kFusedMaxT; ++t) yacc[t] = 0.f;
+  if (a.has_shared) {
+    for (int i = threadIdx.x; i < T * I; i += kFusedThreads)
+      s_h[i] = __ldcg(w.h + (size_t)Pr * I + i);
+  }
+  __syncthreads();
+  const int q_own = blockIdx.x + gridDim.x * warp;  // this warp's first owned row-step
+  for (int q = q_own; q < nquads; q += nw) {
+    const int row = q * RPS_I + ri;
+    if (a.has_shared) {
+      const size_t wo = (size_t)row * (GI * 8) + 8 * gi, so = (size_t)row * GI + gi;
+      const uint4 d0 = ld_stream(a.sh_down.w + wo), d1 = ld_stream(a.sh_down.w + wo + 4);
+      const float ds = bf16f(ld_u16(a.sh_down.s + so)), db = bf16f(ld_u16(a.sh_down.b + so));
+#pragma unroll
+      for (int t = 0; t < kFusedMaxT; ++t) {
+        if (t < T) {
+          XGroup xg;
+          xgroup_from(xg, s_h + (size_t)t * I + kGroup * gi);
+          const float dd = seg_sum<GI>(q4_group_dot(d0, d1, xg, ds, db));
+          if (q == q_own) yacc[t] = s_pair_w[Pr + t] * dd;
+        }
+      }
+    }
+    if (lane == 0) {
+      for (int u = 0; u < Ur; ++u) {
+        const size_t e = (size_t)s_uexp[u];
+        const size_t r0 = (size_t)q * RPS_I;
+        prefetch_l2(a.down.w + (e * H + r0) * (GI * 8), RPS_I * GI * 32);
+        const uint32_t sb = RPS_I * GI * 2 < 16 ? 16 : RPS_I * GI * 2;
+        prefetch_l2(a.down.s + (e * H + r0) * GI, sb);
+        prefetch_l2(a.down.b + (e * H + r0) * GI, sb);
+      }
+    }
+  }
+  if (!grid_barrier(w.hdr, &s_abort)) return;
+
+  // ------------------------------------------------------------------ phase C
+  for (int i = threadIdx.x; i < Pr * I; i += kFusedThreads) s_h[i] = __ldcg(w.h + i);
+  __syncthreads();
+  for (int q = q_own; q < nquads; q += nw) {
+    const int row = q * RPS_I + ri;
+    float acc[kFusedMaxT];
+#pragma unroll
+    for (int t = 0; t < kFusedMaxT; ++t) acc[t] = (q == q_own) ? yacc[t] : 0.f;
+    for (int pr = 0; pr < Pr; ++pr) {
+      const size_t e = (size_t)s_pair_e[pr];
+      const size_t wo = (e * H + row) * (GI * 8) + 8 * gi, so = (e * H + row) * GI + gi;
+      const uint4 d0 = ld_stream(a.down.w + wo), d1 = ld_stream(a.down.w + wo + 4);
+      const float ds = bf16f(ld_u16(a.down.s + so)), db = bf16f(ld_u16(a.down.b + so));
+      XGroup xg;
+      xgroup_from(xg, s_h + (size_t)pr * I + kGroup * gi);
+      const float dd = seg_sum<GI>(q4_group_dot(d0, d1, xg, ds, db));
+      const int t = s_pair_tok[pr];
+#pragma unroll
+      for (int tt = 0; tt < kFusedMaxT; ++tt)
+        if (tt == t) acc[tt] += s_pair_w[pr] * dd;
+    }
+    if (gi == 0) {
+#pragma unroll
+      for (int t = 0; t < kFusedMaxT; ++t)
+        if (t < T) a.y[(size_t)t * H + row] = f2bf16_rne(acc[t]);
+    }
+  }
+}
+
+static bool fused_ok(const lily_q4_moe_layer &L, int T) {
+  const int P = T * L.top_k + (L.has_shared ? T : 0);
+  if ((size_t)P * L.inter * sizeof(float) > kFusedSmemMax) return false;
+  if (T > kFusedMaxT) return false;
+  const int GH = L.hidden / kGroup, GI = L.inter / kGroup;
+  return (GH == 32 && GI == 8) || (GH == 4 && GI == 2);
+}
+
+template <int GH, int GI>
+static int launch_fused(const FusedArgs &fa, const DecodePtrs &p, size_t smem, cudaStream_t st) {
+  static int attr_done[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  auto fn = moe_decode_fused_kernel<GH, GI>;
+  if (dev < 64 && !attr_done[dev]) {
+    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kFusedSmemMax) !=
+        cudaSuccess)
+      return LILY_Q4_ERR_CUDA;
+    int nb = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, fn, kFusedThreads, kFusedSmemMax) !=
+            cudaSuccess ||
+        nb < 1)
+      return LILY_Q4_ERR_CUDA;
+    attr_done[dev] = 1;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(sm_count());
+  cfg.blockDim = dim3(kFusedThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, fn, fa, p) != cudaSuccess) return LILY_Q4_ERR_CUDA;
+  return check_launch();
+}
+
 template <int G>
 static void launch_gateup(const GateUpArgs &a, const DecodePtrs &p, int Umax, cudaStream_t st) {
   constexpr int RPS = 32 / G;
@@ -451,6 +783,14 @@ int launch_moe_decode(const lily_q4_moe_layer &L, const uint16_t *x, int T, uint
                       int32_t *topk_idx, float *topk_w, void *ws, cudaStream_t st) {
   const DecodeWsLayout l = decode_ws_layout(L, T);
   const DecodePtrs p = decode_ptrs(ws, l);
+  if (fused_ok(L, T) && sm_count() > 0) {
+    FusedArgs fa{L.gate, L.up, L.down, L.sh_gate, L.sh_up, L.sh_down, L.router, L.router_bias,
+                 L.shared_gate, x, y, T, L.n_experts, L.hidden, L.inter, L.top_k, L.has_shared,
+                 topk_idx, topk_w};
+    const size_t smem = (size_t)l.P * L.inter * sizeof(float);
+    if (L.hidden / kGroup == 32) return launch_fused<32, 8>(fa, p, smem, st);
+    return launch_fused<4, 2>(fa, p, smem, st);
+  }
   RouterArgs ra{L.router, L.router_bias, L.shared_gate, x, T, L.n_experts, L.hidden, L.top_k,
                 L.has_shared, topk_idx, topk_w};
   const int nrows = L.n_experts + L.has_shared;
