@@ -76,6 +76,7 @@ def load(path: Optional[str] = None):
     L.lily_q4_moe_workspace_bytes.restype = sz
     L.lily_q4_gemv_argmax_workspace_bytes.argtypes = [i32, i32]
     L.lily_q4_gemv_argmax_workspace_bytes.restype = sz
+    L.lily_q4_moe_launches.argtypes = [C.POINTER(lily_q4_moe_layer), i32, i32]
     L.lily_q4_workspace_init.argtypes = [vp, sz, vp]
     L.lily_q4_workspace_status.argtypes = [vp, vp]
     L.lily_q4_status_string.argtypes = [C.c_int]
@@ -84,7 +85,7 @@ def load(path: Optional[str] = None):
     L.lily_q4_unpack.argtypes = [vp, i32, i32, vp]
     for f in ("lily_q4_moe_decode", "lily_q4_moe_prefill", "lily_q4_gemv_argmax",
               "lily_q4_workspace_init", "lily_q4_workspace_status", "lily_q4_pack",
-              "lily_q4_unpack", "lily_q4_version"):
+              "lily_q4_unpack", "lily_q4_version", "lily_q4_moe_launches"):
         getattr(L, f).restype = C.c_int
     _lib = L
     return L
@@ -202,6 +203,10 @@ class DeviceLayer:
 
 def lily_q4_moe_workspace_bytes(layer: DeviceLayer, T: int, prefill: bool = False) -> int:
     return int(load().lily_q4_moe_workspace_bytes(C.byref(layer.c()), int(T), 1 if prefill else 0))
+
+
+def lily_q4_moe_launches(layer: DeviceLayer, T: int, prefill: bool = False) -> int:
+    return int(load().lily_q4_moe_launches(C.byref(layer.c()), int(T), 1 if prefill else 0))
 
 
 def lily_q4_gemv_argmax_workspace_bytes(N: int, K: int) -> int:

@@ -119,6 +119,12 @@ size_t lily_q4_moe_workspace_bytes(const lily_q4_moe_layer *layer, int32_t T, in
   return decode_ws_layout(*layer, T).total;
 }
 
+int lily_q4_moe_launches(const lily_q4_moe_layer *layer, int32_t T, int32_t prefill) {
+  if (check_layer(layer) != LILY_Q4_OK || T <= 0) return 0;
+  if (prefill) return T <= 8192 && layer->hidden >= 128 && layer->inter >= 128 ? 8 : 0;
+  return T <= 16 ? decode_launch_count(*layer, T) : 0;
+}
+
 int lily_q4_workspace_init(void *ws, size_t ws_bytes, lily_q4_stream_t stream) {
   if (!ws || ws_bytes < kAlign || !aligned(ws, kAlign)) return LILY_Q4_ERR_INVALID_ARG;
   return cudaMemsetAsync(ws, 0, ws_bytes, (cudaStream_t)stream) == cudaSuccess ? LILY_Q4_OK

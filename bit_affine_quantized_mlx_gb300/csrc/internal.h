@@ -43,6 +43,7 @@ struct DecodeWsLayout {
   size_t total;
 };
 DecodeWsLayout decode_ws_layout(const lily_q4_moe_layer &L, int T);
+int decode_launch_count(const lily_q4_moe_layer &L, int T);
 int launch_moe_decode(const lily_q4_moe_layer &L, const uint16_t *x, int T, uint16_t *y,
                       int32_t *topk_idx, float *topk_w, void *ws, cudaStream_t st);
 

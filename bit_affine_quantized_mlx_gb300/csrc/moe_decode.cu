@@ -720,6 +720,8 @@ static bool fused_ok(const lily_q4_moe_layer &L, int T) {
   if ((size_t)P * L.inter * sizeof(float) > kFusedSmemMax) return false;
   if (T > kFusedMaxT) return false;
   const int GH = L.hidden / kGroup, GI = L.inter / kGroup;
+  // each warp owns at most one down row-step (its shared-expert partial stays in registers)
+  if (L.hidden / (32 / GI) > sm_count() * kFusedWarps) return false;
   return (GH == 32 && GI == 8) || (GH == 4 && GI == 2);
 }
 
@@ -778,6 +780,10 @@ static void launch_down(const DownArgs &a, const DecodePtrs &p, cudaStream_t st)
     case 32: FN<32>(__VA_ARGS__); break;   \
     default: return LILY_Q4_ERR_UNSUPPORTED; \
   }
+
+int decode_launch_count(const lily_q4_moe_layer &L, int T) {
+  return fused_ok(L, T) && sm_count() > 0 ? 1 : 3;
+}
 
 int launch_moe_decode(const lily_q4_moe_layer &L, const uint16_t *x, int T, uint16_t *y,
                       int32_t *topk_idx, float *topk_w, void *ws, cudaStream_t st) {

@@ -143,6 +143,12 @@ LILY_Q4_API int lily_q4_gemv_argmax(const lily_q4_mat *W, int32_t N, int32_t K, 
 LILY_Q4_API size_t lily_q4_moe_workspace_bytes(const lily_q4_moe_layer *layer, int32_t T, int32_t prefill);
 LILY_Q4_API size_t lily_q4_gemv_argmax_workspace_bytes(int32_t N, int32_t K);
 
+/* Number of kernel launches one lily_q4_moe_decode (prefill = 0) or lily_q4_moe_prefill
+ * (prefill = 1) call enqueues for this layer and T; 0 when the arguments are invalid.
+ * Decode uses one cooperative launch when its single-launch kernel covers the shapes and
+ * batch, three launches otherwise. */
+LILY_Q4_API int lily_q4_moe_launches(const lily_q4_moe_layer *layer, int32_t T, int32_t prefill);
+
 /* Zero-fill a workspace on `stream` (asynchronous). */
 LILY_Q4_API int lily_q4_workspace_init(void *ws, size_t ws_bytes, lily_q4_stream_t stream);
 
