@@ -70,6 +70,7 @@ struct DecodePtrs {
   float *pair_w;
   float *h;
   int Umax;
+  int P;  // pairs the workspace holds
   __host__ __device__ int32_t *uexp() const { return meta + 1; }
   __host__ __device__ int32_t *ubase() const { return meta + 1 + Umax; }
   __host__ __device__ int32_t *pair_e() const { return meta + 1 + Umax + Umax + 1; }
@@ -88,6 +89,7 @@ static DecodePtrs decode_ptrs(void *ws, const DecodeWsLayout &l) {
   p.pair_w = reinterpret_cast<float *>(b + l.off_pair_w);
   p.h = reinterpret_cast<float *>(b + l.off_h);
   p.Umax = l.Umax;
+  p.P = l.P;
   return p;
 }
 
@@ -308,11 +310,12 @@ __global__ void __launch_bounds__(kGateUpThreads)
   constexpr int ROWS = (kGateUpThreads / 32) * kGateUpSteps * RPS;
   const int u = blockIdx.y;
   const int U = w.meta[0];
-  if (u >= U) return;
+  if (u >= U || U > w.Umax) return;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int g = lane % G, rsub = lane / G;
   const int e = w.uexp()[u];
-  const int pb = w.ubase()[u], pe = w.ubase()[u + 1];
+  const int pb = max(w.ubase()[u], 0), pe = min(w.ubase()[u + 1], w.P);
+  if (e < 0 || e > a.E) return;
   const bool shared = (e == a.E);
   const size_t eoff_w = shared ? 0 : (size_t)e * a.I * K8;
   const size_t eoff_s = shared ? 0 : (size_t)e * a.I * G;
@@ -384,12 +387,12 @@ __global__ void __launch_bounds__(kDownThreads)
   __shared__ int s_tok[kMaxPairs];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int g = lane % G, rsub = lane / G;
-  const int U = w.meta[0];
-  const int P = w.ubase()[U];
+  const int U = min(max(w.meta[0], 0), w.Umax);
+  const int P = min(max(w.ubase()[U], 0), w.P);
   const int r0 = blockIdx.x * kDownRows;
 
   for (int pr = warp; pr < P; pr += kDownThreads / 32) {
-    const int e = w.pair_e()[pr];
+    const int e = min(max(w.pair_e()[pr], 0), a.E);
     const bool shared = (e == a.E);
     const uint32_t *dw = shared ? a.sh_down.w : a.down.w + (size_t)e * a.H * K8;
     const uint16_t *ds = shared ? a.sh_down.s : a.down.s + (size_t)e * a.H * G;

@@ -438,8 +438,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const Gem
 // small kernels around the GEMMs
 // -------------------------------------------------------------------------------------
 
-// x_perm[t][8c + pos(i)] = x[t][8c + i]
-__global__ void x_perm_kernel(const uint4 *__restrict__ x, uint4 *__restrict__ xp, int nchunks) {
+// x_perm[t][8c + pos(i)] = x[t][8c + i]; also clears the per-expert counts that the top-k
+// kernel accumulates (the workspace layout depends on T, so nothing is assumed about them).
+__global__ void x_perm_kernel(const uint4 *__restrict__ x, uint4 *__restrict__ xp, int nchunks,
+                              int32_t *__restrict__ counts, int ncounts) {
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < ncounts; i += gridDim.x * blockDim.x)
+    counts[i] = 0;
   for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < nchunks; i += gridDim.x * blockDim.x) {
     const uint4 v = __ldg(x + i);
     uint4 o;
@@ -532,14 +536,14 @@ __global__ void __launch_bounds__(256) topk_prefill_kernel(TopkArgs a) {
 }
 
 struct ScanArgs {
-  int32_t *counts;   // [E] (zeroed again here)
+  const int32_t *counts;  // [E]
   int32_t *offsets;  // [E+2]
   int4 *items_gu, *items_dn;
   int32_t *hdr;
   int T, E, k, has_shared, mt_gu, mt_dn;
 };
 
-// Single block: per-expert offsets, GEMM work lists, and re-zeroed counts.
+// Single block: per-expert offsets and the GEMM work lists.
 __global__ void __launch_bounds__(1024) scan_items_kernel(ScanArgs a) {
   __shared__ int s_cnt[1025];
   __shared__ int s_off[1026];
@@ -547,7 +551,7 @@ __global__ void __launch_bounds__(1024) scan_items_kernel(ScanArgs a) {
   __shared__ int s_ibase[1026];
   const int nexp = a.E + a.has_shared;
   for (int e = threadIdx.x; e < nexp; e += blockDim.x) {
-    const int c = e < a.E ? a.counts[e] : a.T;
+    const int c = e < a.E ? min(max(a.counts[e], 0), a.T) : a.T;
     s_cnt[e] = c;
     s_nt[e] = (c + kBN - 1) / kBN;
   }
@@ -586,7 +590,6 @@ __global__ void __launch_bounds__(1024) scan_items_kernel(ScanArgs a) {
       for (int mt = 0; mt < a.mt_gu; ++mt) a.items_gu[tile * a.mt_gu + mt] = make_int4(e, p0, n, mt);
       for (int mt = 0; mt < a.mt_dn; ++mt) a.items_dn[tile * a.mt_dn + mt] = make_int4(e, p0, n, mt);
     }
-    if (e < a.E) a.counts[e] = 0;
   }
   if (threadIdx.x == 0) {
     a.offsets[nexp] = s_off[nexp];
@@ -754,7 +757,7 @@ int launch_moe_prefill(const lily_q4_moe_layer &L, const uint16_t *x, int T, uin
 
   const int nch = T * H / 8;
   x_perm_kernel<<<(nch + 255) / 256 < 4 * sms ? (nch + 255) / 256 : 4 * sms, 256, 0, st>>>(
-      reinterpret_cast<const uint4 *>(x), reinterpret_cast<uint4 *>(xperm), nch);
+      reinterpret_cast<const uint4 *>(x), reinterpret_cast<uint4 *>(xperm), nch, counts, E);
 
   // router GEMM
   GemmArgs ra{};
