@@ -77,6 +77,7 @@ def load(path: Optional[str] = None):
     L.lily_q4_gemv_argmax_workspace_bytes.argtypes = [i32, i32]
     L.lily_q4_gemv_argmax_workspace_bytes.restype = sz
     L.lily_q4_moe_launches.argtypes = [C.POINTER(lily_q4_moe_layer), i32, i32]
+    L.lily_q4_gemv_argmax_noalloc.argtypes = [C.POINTER(lily_q4_mat), i32, i32, vp, vp, vp, vp]
     L.lily_q4_workspace_init.argtypes = [vp, sz, vp]
     L.lily_q4_workspace_status.argtypes = [vp, vp]
     L.lily_q4_status_string.argtypes = [C.c_int]
@@ -85,7 +86,8 @@ def load(path: Optional[str] = None):
     L.lily_q4_unpack.argtypes = [vp, i32, i32, vp]
     for f in ("lily_q4_moe_decode", "lily_q4_moe_prefill", "lily_q4_gemv_argmax",
               "lily_q4_workspace_init", "lily_q4_workspace_status", "lily_q4_pack",
-              "lily_q4_unpack", "lily_q4_version", "lily_q4_moe_launches"):
+              "lily_q4_unpack", "lily_q4_version", "lily_q4_moe_launches",
+              "lily_q4_gemv_argmax_noalloc"):
         getattr(L, f).restype = C.c_int
     _lib = L
     return L
@@ -253,6 +255,16 @@ def lily_q4_gemv_argmax(W: DeviceQ4, x, token, logits=None, ws=None, stream=None
     return _check(load().lily_q4_gemv_argmax(C.byref(m), N, K, _ptr(x), _ptr(token), _ptr(logits),
                                              _ptr(ws), ws.numel() if ws is not None else 0,
                                              _stream(stream)), "lily_q4_gemv_argmax")
+
+
+def lily_q4_gemv_argmax_noalloc(W: DeviceQ4, x, token, logits=None, stream=None):
+    """lily_q4_gemv_argmax without a workspace, for callers that cannot allocate device
+    memory: the scratch is a fixed array inside the library (see include/lily_q4.h)."""
+    N, K = int(W.w.shape[-2]), int(W.w.shape[-1]) * 8
+    m = W.c()
+    return _check(load().lily_q4_gemv_argmax_noalloc(C.byref(m), N, K, _ptr(x), _ptr(token),
+                                                     _ptr(logits), _stream(stream)),
+                  "lily_q4_gemv_argmax_noalloc")
 
 
 def lily_q4_pack(q: np.ndarray) -> np.ndarray:

@@ -9,6 +9,7 @@
 // The pass is bound by HBM bandwidth: 0.5625 bytes per weight.
 #include <cfloat>
 #include <climits>
+#include <mutex>
 
 #include "internal.h"
 #include "q4_device.cuh"
@@ -194,4 +195,58 @@ int launch_gemv_argmax(const lily_q4_mat &W, int N, int K, const uint16_t *x, in
   return check_launch();
 }
 
+// ---------------------------------------------------------------------------------------
+// lily_q4_gemv_argmax_noalloc: the same kernel with its scratch in a fixed device array.
+//
+// Some callers cannot call cudaMalloc at all: code that runs on a memory budget fixed when
+// it started, or a host framework that owns every device allocation and hands this
+// library only its input and output pointers.  They have no workspace to pass, so this
+// entry point keeps the kernel's scratch (the last-block counter and the per-block
+// (max, argmax) pairs) in a file-scope __device__ array that every GPU loading the library
+// holds until the process exits.
+// ---------------------------------------------------------------------------------------
+constexpr size_t kNoAllocScratchBytes = 16640;  // 256-byte header + 2048 (float, int) pairs
+static __device__ __align__(256) unsigned char g_gemv_argmax_scratch[kNoAllocScratchBytes];
+
+// Device address of g_gemv_argmax_scratch on the current device, looked up once per device.
+// (In host code the array's name is only a host-side stand-in, never a device address.)
+static int noalloc_scratch(void **out) {
+  static std::mutex mu;
+  static void *addr[64] = {nullptr};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return LILY_Q4_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!addr[dev]) {
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_gemv_argmax_scratch) != cudaSuccess || !p)
+      return LILY_Q4_ERR_CUDA;
+    addr[dev] = p;
+  }
+  *out = addr[dev];
+  return LILY_Q4_OK;
+}
+
 }  // namespace lq4
+
+extern "C" int lily_q4_gemv_argmax_noalloc(const lily_q4_mat *W, int32_t N, int32_t K,
+                                           const uint16_t *x, int32_t *token, float *logits,
+                                           lily_q4_stream_t stream) {
+  using namespace lq4;
+  auto al = [](const void *p, size_t a) { return ((uintptr_t)p % a) == 0; };
+  if (!W || !W->w || !W->s || !W->b || !al(W->w, 16) || !al(W->s, 16) || !al(W->b, 16))
+    return LILY_Q4_ERR_INVALID_ARG;
+  if (N <= 0 || K <= 0 || K % LILY_Q4_GROUP) return LILY_Q4_ERR_INVALID_ARG;
+  if (!x || !al(x, 16) || !token || !al(token, 4) || (logits && !al(logits, 4)))
+    return LILY_Q4_ERR_INVALID_ARG;
+  if (K > 2048 || (K & (K - 1))) return LILY_Q4_ERR_UNSUPPORTED;
+  if (lm_ws_layout(N, K).total > kNoAllocScratchBytes) return LILY_Q4_ERR_WORKSPACE_TOO_SMALL;
+  void *scratch = nullptr;
+  int rc = noalloc_scratch(&scratch);
+  if (rc != LILY_Q4_OK) return rc;
+  cudaStream_t st = (cudaStream_t)stream;
+  // start from a zero counter even if an earlier call was cut short
+  if (cudaMemsetAsync(scratch, 0, kHdrWords * sizeof(int32_t), st) != cudaSuccess)
+    return LILY_Q4_ERR_CUDA;
+  return launch_gemv_argmax(*W, N, K, x, token, logits, scratch, st);
+}
+

@@ -139,6 +139,33 @@ LILY_Q4_API int lily_q4_gemv_argmax(const lily_q4_mat *W, int32_t N, int32_t K, 
                         int32_t *token, float *logits, void *ws, size_t ws_bytes,
                         lily_q4_stream_t stream);
 
+/*
+ * lily_q4_gemv_argmax_noalloc -- lily_q4_gemv_argmax for callers that cannot allocate.
+ *
+ * The paper has no counterpart: this entry point exists for callers that cannot call
+ * cudaMalloc at all (code running on a memory budget fixed at start-up, or a host
+ * framework that owns every device allocation and passes this library only its input
+ * and output pointers) and so have no workspace to give.  Arguments, results and errors
+ * are those of lily_q4_gemv_argmax without ws/ws_bytes.
+ *
+ * The kernel's scratch (a counter and the per-block (max, argmax) pairs) lives in a
+ * 16,640-byte __device__ array inside the library, held by every GPU that loads the
+ * library until the process exits.  It covers up to 2048 blocks; when
+ * lily_q4_gemv_argmax_workspace_bytes(N, K) exceeds 16,640 bytes (GPUs with more than
+ * 1024 SMs) the call returns LILY_Q4_ERR_WORKSPACE_TOO_SMALL.  K must be a power of two
+ * from 64 to 2048 (else LILY_Q4_ERR_UNSUPPORTED).
+ *  - The first call on a device looks up the array's device address on that device
+ *    (cudaGetSymbolAddress); make that first call before any stream capture.
+ *  - Every call on a device shares the one array and it keeps the last call's contents;
+ *    each call clears the counter it needs on `stream` before its kernel.  Calls whose
+ *    work overlaps on the GPU (different streams without ordering) race on the array:
+ *    order them.
+ *  - Calls no cudaMalloc, cudaFree or other allocating routine.
+ */
+LILY_Q4_API int lily_q4_gemv_argmax_noalloc(const lily_q4_mat *W, int32_t N, int32_t K,
+                                            const uint16_t *x, int32_t *token, float *logits,
+                                            lily_q4_stream_t stream);
+
 /* Workspace sizes (bytes) for the calls above; 0 when the arguments are invalid. */
 LILY_Q4_API size_t lily_q4_moe_workspace_bytes(const lily_q4_moe_layer *layer, int32_t T, int32_t prefill);
 LILY_Q4_API size_t lily_q4_gemv_argmax_workspace_bytes(int32_t N, int32_t K);
