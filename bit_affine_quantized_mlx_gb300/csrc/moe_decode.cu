@@ -120,7 +120,7 @@ struct RouteDst {
   float *out_w;
 };
 
-template <int NT>
+template <int NT, int EC>
 __device__ void route_block(const float *logits, const float *sigma, int T, int E, int k,
                             int has_shared, const RouteDst &d) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -129,22 +129,24 @@ __device__ void route_block(const float *logits, const float *sigma, int T, int 
   __shared__ int s_cnt[1024];
   __shared__ int s_base[1024];
 
-  // top-k per token: warp per token, k rounds of a warp argmax over unselected experts
+  // top-k per token: warp per token; each lane holds its EC logits in registers, then k
+  // rounds of a warp argmax over the unselected ones
   for (int t = warp; t < T; t += NT / 32) {
     const float *lg = logits + (size_t)t * E;
+    float lv[EC];
+#pragma unroll
+    for (int j = 0; j < EC; ++j) lv[j] = (lane + 32 * j < E) ? __ldcg(lg + lane + 32 * j) : -FLT_MAX;
     uint32_t taken = 0;  // bit j: expert lane + 32 j already selected
-    float v0 = 0.f, denom = 0.f;
     float sel_v[kMaxK];
     int sel_e[kMaxK];
     for (int i = 0; i < k; ++i) {
       float bv = -FLT_MAX;
       int be = INT_MAX;
-      for (int j = 0; lane + 32 * j < E; ++j) {
+#pragma unroll
+      for (int j = 0; j < EC; ++j) {
         const int e = lane + 32 * j;
-        if (taken & (1u << j)) continue;
-        const float v = __ldcg(lg + e);
-        if (better(v, e, bv, be)) {
-          bv = v;
+        if (e < E && !(taken & (1u << j)) && better(lv[j], e, bv, be)) {
+          bv = lv[j];
           be = e;
         }
       }
@@ -161,9 +163,10 @@ __device__ void route_block(const float *logits, const float *sigma, int T, int 
       sel_v[i] = bv;
       sel_e[i] = be;
     }
-    v0 = sel_v[0];
-    for (int i = 0; i < k; ++i) denom += expf(sel_v[i] - v0);
     if (lane == 0) {
+      const float v0 = sel_v[0];
+      float denom = 0.f;
+      for (int i = 0; i < k; ++i) denom += expf(sel_v[i] - v0);
       for (int i = 0; i < k; ++i) {
         const float pi = expf(sel_v[i] - v0) / denom;
         s_idx[t * k + i] = sel_e[i];
@@ -236,6 +239,7 @@ __device__ void route_block(const float *logits, const float *sigma, int T, int 
 // ---------------------------------------------------------------------------------------
 // 1. router logits + shared gate; last block: top-k, gates, unique-expert pairs
 // ---------------------------------------------------------------------------------------
+template <int EC>
 __global__ void __launch_bounds__(kRouterThreads)
     router_topk_kernel(RouterArgs a, DecodePtrs w) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -289,7 +293,7 @@ __global__ void __launch_bounds__(kRouterThreads)
 
   RouteDst d{w.idx, w.p, w.meta, w.uexp(), w.ubase(), w.pair_tok, w.pair_w, w.pair_e(),
              a.out_idx, a.out_w};
-  route_block<kRouterThreads>(w.logits, w.sigma, a.T, a.E, a.k, a.has_shared, d);
+  route_block<kRouterThreads, EC>(w.logits, w.sigma, a.T, a.E, a.k, a.has_shared, d);
   if (threadIdx.x == 0) w.hdr[kHdrCounterB] = 0;
 }
 
@@ -520,7 +524,7 @@ __device__ bool grid_barrier(int32_t *hdr, volatile int *s_abort) {
   return !*s_abort;
 }
 
-template <int GH, int GI>
+template <int GH, int GI, int EC>
 __global__ void __launch_bounds__(kFusedThreads, 1)
     moe_decode_fused_kernel(FusedArgs a, DecodePtrs w) {
   extern __shared__ float s_h[];  // [P][I] (phase C) / [T][I] shared h (phase B)
@@ -620,7 +624,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
   {
     RouteDst d{nullptr, nullptr, &s_U, s_uexp, s_ubase, s_pair_tok, s_pair_w, s_pair_e,
                blockIdx.x == 0 ? a.out_idx : nullptr, blockIdx.x == 0 ? a.out_w : nullptr};
-    route_block<kFusedThreads>(w.logits, w.sigma, T, E, k, a.has_shared, d);
+    route_block<kFusedThreads, EC>(w.logits, w.sigma, T, E, k, a.has_shared, d);
   }
   const int U = s_U;
   const int Ur = a.has_shared ? U - 1 : U;  // routed unique experts
@@ -725,15 +729,15 @@ static bool fused_ok(const lily_q4_moe_layer &L, int T) {
   const int GH = L.hidden / kGroup, GI = L.inter / kGroup;
   // each warp owns at most one down row-step (its shared-expert partial stays in registers)
   if (L.hidden / (32 / GI) > sm_count() * kFusedWarps) return false;
-  return (GH == 32 && GI == 8) || (GH == 4 && GI == 2);
+  return (GH == 32 && GI == 8) || (GH == 4 && GI == 2 && L.n_experts <= 256);
 }
 
-template <int GH, int GI>
+template <int GH, int GI, int EC>
 static int launch_fused(const FusedArgs &fa, const DecodePtrs &p, size_t smem, cudaStream_t st) {
-  static int attr_done[64] = {0};
+  static int attr_done[64] = {0};  // per instantiation and device
   int dev = 0;
   cudaGetDevice(&dev);
-  auto fn = moe_decode_fused_kernel<GH, GI>;
+  auto fn = moe_decode_fused_kernel<GH, GI, EC>;
   if (dev < 64 && !attr_done[dev]) {
     if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kFusedSmemMax) !=
         cudaSuccess)
@@ -797,14 +801,23 @@ int launch_moe_decode(const lily_q4_moe_layer &L, const uint16_t *x, int T, uint
                  L.shared_gate, x, y, T, L.n_experts, L.hidden, L.inter, L.top_k, L.has_shared,
                  topk_idx, topk_w};
     const size_t smem = (size_t)l.P * L.inter * sizeof(float);
-    if (L.hidden / kGroup == 32) return launch_fused<32, 8>(fa, p, smem, st);
-    return launch_fused<4, 2>(fa, p, smem, st);
+    if (L.hidden / kGroup == 32) {
+      if (L.n_experts <= 256) return launch_fused<32, 8, 8>(fa, p, smem, st);
+      if (L.n_experts <= 512) return launch_fused<32, 8, 16>(fa, p, smem, st);
+      return launch_fused<32, 8, 32>(fa, p, smem, st);
+    }
+    return launch_fused<4, 2, 8>(fa, p, smem, st);
   }
   RouterArgs ra{L.router, L.router_bias, L.shared_gate, x, T, L.n_experts, L.hidden, L.top_k,
                 L.has_shared, topk_idx, topk_w};
   const int nrows = L.n_experts + L.has_shared;
   const int rgrid = (nrows + kRouterThreads / 32 - 1) / (kRouterThreads / 32);
-  router_topk_kernel<<<rgrid, kRouterThreads, 0, st>>>(ra, p);
+  if (L.n_experts <= 256)
+    router_topk_kernel<8><<<rgrid, kRouterThreads, 0, st>>>(ra, p);
+  else if (L.n_experts <= 512)
+    router_topk_kernel<16><<<rgrid, kRouterThreads, 0, st>>>(ra, p);
+  else
+    router_topk_kernel<32><<<rgrid, kRouterThreads, 0, st>>>(ra, p);
 
   GateUpArgs ga{L.gate, L.up, L.sh_gate, L.sh_up, x, L.n_experts, L.hidden, L.inter};
   LQ4_DISPATCH_G(L.hidden / kGroup, launch_gateup, ga, p, l.Umax, st);
