@@ -18,7 +18,7 @@ namespace lq4 {
 
 constexpr int kLmThreads = 256;
 constexpr int kLmWarps = kLmThreads / 32;
-constexpr int kLmBlocksPerSm = 2;
+constexpr int kLmBlocksPerSm = 1;
 
 LmWsLayout lm_ws_layout(int N, int K) {
   (void)K;
@@ -39,7 +39,8 @@ LmWsLayout lm_ws_layout(int N, int K) {
   return l;
 }
 
-// G = groups per row (K/64), U = row-steps issued together (bytes in flight).
+// G = groups per row (K/64), U = row-steps per iteration: a warp issues the loads of U
+// row-steps (U*32 bytes of codes per lane) before computing them.
 template <int G, int U>
 __global__ void __launch_bounds__(kLmThreads, kLmBlocksPerSm)
     gemv_argmax_kernel(const uint32_t *__restrict__ w, const uint16_t *__restrict__ s,
@@ -67,6 +68,7 @@ __global__ void __launch_bounds__(kLmThreads, kLmBlocksPerSm)
   const int nwarps = gridDim.x * kLmWarps;
   constexpr int RPI = RPS * U;  // rows per warp-iteration
 
+#pragma unroll 1
   for (int r0 = gwarp * RPI; r0 < N; r0 += nwarps * RPI) {
     uint4 wa[U], wb[U];
     float sv[U], bv[U];
@@ -174,7 +176,7 @@ template <int G>
 static void launch_g(const lily_q4_mat &W, int N, const uint16_t *x, int32_t *token,
                      float *logits, void *ws, const LmWsLayout &l, cudaStream_t st) {
   char *base = static_cast<char *>(ws);
-  gemv_argmax_kernel<G, (G >= 16 ? 2 : 4)><<<l.grid, kLmThreads, 0, st>>>(
+  gemv_argmax_kernel<G, (G >= 16 ? 8 : 4)><<<l.grid, kLmThreads, 0, st>>>(
       W.w, W.s, W.b, N, x, logits, token, reinterpret_cast<int32_t *>(base),
       reinterpret_cast<float *>(base + l.off_partial_v),
       reinterpret_cast<int32_t *>(base + l.off_partial_i));

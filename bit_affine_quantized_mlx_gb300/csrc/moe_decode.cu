@@ -458,20 +458,24 @@ __global__ void __launch_bounds__(kDownThreads)
 // Single-launch decode layer (cooperative, one block per SM, two grid barriers)
 //
 //   phase A: router rows (+ the shared gate row) and the shared expert's gate/up rows,
-//            none of which depends on the routing; down-row owners prefetch the shared
-//            expert's down rows into L2
+//            none of which depends on the routing; each block prefetches the shared
+//            expert's down rows it will need into L2
 //   barrier
 //   phase B: every block takes the routing of all tokens from the logits (identical
-//            result in every block); routed gate/up rows; owners run the shared expert's
-//            down rows and prefetch their routed down rows into L2
+//            result in every block); routed gate/up rows, each warp issuing the loads of
+//            a batch of rows before computing; each block prefetches its routed down rows
 //   barrier
-//   phase C: h of every pair staged in shared memory; owners run the routed down rows,
-//            add them to the shared-expert partial in a fixed order and write y
+//   phase C: h of every pair staged in shared memory; block b owns down row-steps
+//            b, b + grid, ...; its warps split the pairs, each warp loading its pairs' rows
+//            for all of the block's row-steps at once; partials meet in shared memory and
+//            are summed per token in a fixed order (deterministic)
 // ---------------------------------------------------------------------------------------
-constexpr int kFusedThreads = 256;
+constexpr int kFusedThreads = 384;
 constexpr int kFusedWarps = kFusedThreads / 32;
 constexpr size_t kFusedSmemMax = 100 * 1024;
 constexpr int kFusedMaxT = 4;
+constexpr int kFusedMaxQ = 4;   // down row-steps per block
+constexpr int kFusedBatch = 3;  // gate/up rows whose loads a warp issues together
 constexpr long long kBarrierCycles = 2000000000LL;  // ~1 s
 
 struct FusedArgs {
@@ -494,6 +498,27 @@ __device__ __forceinline__ int ld_acquire(const int32_t *p) {
 
 __device__ __forceinline__ void prefetch_l2(const void *p, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
+// Copy n floats (n a multiple of 4, 16-byte aligned) from L2 to shared memory, 8 float4
+// loads in flight per thread.
+__device__ __forceinline__ void stage_rows(float *dst, const float *src, int n) {
+  const int n4 = n / 4;
+  const float4 *s4 = reinterpret_cast<const float4 *>(src);
+  float4 *d4 = reinterpret_cast<float4 *>(dst);
+  for (int base = threadIdx.x; base < n4; base += kFusedThreads * 8) {
+    float4 v[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int j = base + i * kFusedThreads;
+      if (j < n4) v[i] = __ldcg(s4 + j);
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int j = base + i * kFusedThreads;
+      if (j < n4) d4[j] = v[i];
+    }
+  }
 }
 
 // Self-resetting grid barrier (count word, generation word) with a bounded wait.
@@ -522,6 +547,45 @@ __device__ bool grid_barrier(int32_t *hdr, volatile int *s_abort) {
   }
   __syncthreads();
   return !*s_abort;
+}
+
+// One row of a routed expert's gate and up matrices (lane's group) and one down row.
+struct RowPair {
+  uint4 a0, a1, b0, b1;
+  float as, ab, bs, bb;
+};
+struct DownRow {
+  uint4 w0, w1;
+  float s, b;
+};
+
+template <int GH>
+__device__ __forceinline__ void load_gateup(const FusedArgs &a, const int32_t *uexp, int task,
+                                            int steps_h, int I, int gh, int rh, RowPair &r) {
+  constexpr int RPS_H = 32 / GH;
+  const int u = task / steps_h;
+  const int row = (task % steps_h) * RPS_H + rh;
+  const size_t e = (size_t)uexp[u];
+  const size_t wo = (e * I + row) * (GH * 8) + 8 * gh, so = (e * I + row) * GH + gh;
+  r.a0 = ld_stream(a.gate.w + wo);
+  r.a1 = ld_stream(a.gate.w + wo + 4);
+  r.b0 = ld_stream(a.up.w + wo);
+  r.b1 = ld_stream(a.up.w + wo + 4);
+  r.as = bf16f(ld_u16(a.gate.s + so));
+  r.ab = bf16f(ld_u16(a.gate.b + so));
+  r.bs = bf16f(ld_u16(a.up.s + so));
+  r.bb = bf16f(ld_u16(a.up.b + so));
+}
+
+template <int GI>
+__device__ __forceinline__ void load_down_mat(const lily_q4_mat &m, int e, int row, int H, int gi,
+                                              DownRow &r) {
+  const size_t wo = ((size_t)e * H + row) * (GI * 8) + 8 * gi;
+  const size_t so = ((size_t)e * H + row) * GI + gi;
+  r.w0 = ld_stream(m.w + wo);
+  r.w1 = ld_stream(m.w + wo + 4);
+  r.s = bf16f(ld_u16(m.s + so));
+  r.b = bf16f(ld_u16(m.b + so));
 }
 
 template <int GH, int GI, int EC>
@@ -609,14 +673,14 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
       }
     }
   }
-  // owners of down rows prefetch the shared expert's down rows
-  if (a.has_shared && lane == 0) {
-    for (int q = blockIdx.x + gridDim.x * warp; q < nquads; q += nw) {
-      const size_t r0 = (size_t)q * RPS_I;
-      prefetch_l2(a.sh_down.w + r0 * (GI * 8), RPS_I * GI * 32);
-      prefetch_l2(a.sh_down.s + r0 * GI, RPS_I * GI * 2 < 16 ? 16 : RPS_I * GI * 2);
-      prefetch_l2(a.sh_down.b + r0 * GI, RPS_I * GI * 2 < 16 ? 16 : RPS_I * GI * 2);
-    }
+  // the shared expert's down rows of this block's row-steps, into L2
+  const int nq_cta = (nquads - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x;
+  const uint32_t sb_bytes = RPS_I * GI * 2 < 16 ? 16 : RPS_I * GI * 2;
+  if (a.has_shared && threadIdx.x < nq_cta) {
+    const size_t r0 = (size_t)(blockIdx.x + threadIdx.x * gridDim.x) * RPS_I;
+    prefetch_l2(a.sh_down.w + r0 * (GI * 8), RPS_I * GI * 32);
+    prefetch_l2(a.sh_down.s + r0 * GI, sb_bytes);
+    prefetch_l2(a.sh_down.b + r0 * GI, sb_bytes);
   }
   if (!grid_barrier(w.hdr, &s_abort)) return;
 
@@ -628,97 +692,91 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
   }
   const int U = s_U;
   const int Ur = a.has_shared ? U - 1 : U;  // routed unique experts
-  const int Pr = s_ubase[Ur];               // routed pairs
-  // routed gate/up: tasks (unique expert, row-step)
+  // routed gate/up: tasks (unique expert, row-step), a batch of kFusedBatch per warp with
+  // all of the batch's loads issued before any is computed
   const int steps_h = I / RPS_H;
-  for (int task = gw; task < Ur * steps_h; task += nw) {
-    const int u = task / steps_h;
-    const int row = (task % steps_h) * RPS_H + rh;
-    const int e = s_uexp[u];
-    const size_t wo = ((size_t)e * I + row) * (GH * 8) + 8 * gh;
-    const size_t so = ((size_t)e * I + row) * GH + gh;
-    const uint4 g0 = ld_stream(a.gate.w + wo), g1 = ld_stream(a.gate.w + wo + 4);
-    const uint4 u0 = ld_stream(a.up.w + wo), u1 = ld_stream(a.up.w + wo + 4);
-    const float gs = bf16f(ld_u16(a.gate.s + so)), gb = bf16f(ld_u16(a.gate.b + so));
-    const float us = bf16f(ld_u16(a.up.s + so)), ub = bf16f(ld_u16(a.up.b + so));
-    for (int pr = s_ubase[u]; pr < s_ubase[u + 1]; ++pr) {
-      const int t = s_pair_tok[pr];
-      XGroup xg;
-      uint4 c[8];
-      const uint4 *xp = reinterpret_cast<const uint4 *>(a.x + (size_t)t * H + kGroup * gh);
+  const int ntasks_b = Ur * steps_h;
+  for (int base = gw; base < ntasks_b; base += nw * kFusedBatch) {
+    RowPair rp[kFusedBatch];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) c[i] = __ldg(xp + i);
-      xgroup_from_bf16(xg, c);
-      const float gd = seg_sum<GH>(q4_group_dot(g0, g1, xg, gs, gb));
-      const float ud = seg_sum<GH>(q4_group_dot(u0, u1, xg, us, ub));
-      if (gh == 0) __stcg(w.h + (size_t)pr * I + row, silu_mul(gd, ud));
-    }
-  }
-  // owners: shared-expert down rows (h_shared staged in shared memory first), routed prefetch
-  float yacc[kFusedMaxT];
+    for (int i = 0; i < kFusedBatch; ++i)
+      if (base + i * nw < ntasks_b) load_gateup<GH>(a, s_uexp, base + i * nw, steps_h, I, gh, rh, rp[i]);
+    int xg_tok = -1;
+    XGroup xg;
 #pragma unroll
-  for (int t = 0; t < kFusedMaxT; ++t) yacc[t] = 0.f;
-  if (a.has_shared) {
-    for (int i = threadIdx.x; i < T * I; i += kFusedThreads)
-      s_h[i] = __ldcg(w.h + (size_t)Pr * I + i);
-  }
-  __syncthreads();
-  const int q_own = blockIdx.x + gridDim.x * warp;  // this warp's first owned row-step
-  for (int q = q_own; q < nquads; q += nw) {
-    const int row = q * RPS_I + ri;
-    if (a.has_shared) {
-      const size_t wo = (size_t)row * (GI * 8) + 8 * gi, so = (size_t)row * GI + gi;
-      const uint4 d0 = ld_stream(a.sh_down.w + wo), d1 = ld_stream(a.sh_down.w + wo + 4);
-      const float ds = bf16f(ld_u16(a.sh_down.s + so)), db = bf16f(ld_u16(a.sh_down.b + so));
+    for (int i = 0; i < kFusedBatch; ++i) {
+      const int task = base + i * nw;
+      if (task < ntasks_b) {
+        const int u = task / steps_h;
+        const int row = (task % steps_h) * RPS_H + rh;
+#pragma unroll 1
+        for (int pr = s_ubase[u]; pr < s_ubase[u + 1]; ++pr) {
+          const int t = s_pair_tok[pr];
+          if (t != xg_tok) {
+            uint4 c[8];
+            const uint4 *xp = reinterpret_cast<const uint4 *>(a.x + (size_t)t * H + kGroup * gh);
 #pragma unroll
-      for (int t = 0; t < kFusedMaxT; ++t) {
-        if (t < T) {
-          XGroup xg;
-          xgroup_from(xg, s_h + (size_t)t * I + kGroup * gi);
-          const float dd = seg_sum<GI>(q4_group_dot(d0, d1, xg, ds, db));
-          if (q == q_own) yacc[t] = s_pair_w[Pr + t] * dd;
+            for (int q = 0; q < 8; ++q) c[q] = __ldg(xp + q);
+            xgroup_from_bf16(xg, c);
+            xg_tok = t;
+          }
+          const float gd = seg_sum<GH>(q4_group_dot(rp[i].a0, rp[i].a1, xg, rp[i].as, rp[i].ab));
+          const float ud = seg_sum<GH>(q4_group_dot(rp[i].b0, rp[i].b1, xg, rp[i].bs, rp[i].bb));
+          if (gh == 0) __stcg(w.h + (size_t)pr * I + row, silu_mul(gd, ud));
         }
       }
     }
-    if (lane == 0) {
-      for (int u = 0; u < Ur; ++u) {
-        const size_t e = (size_t)s_uexp[u];
-        const size_t r0 = (size_t)q * RPS_I;
-        prefetch_l2(a.down.w + (e * H + r0) * (GI * 8), RPS_I * GI * 32);
-        const uint32_t sb = RPS_I * GI * 2 < 16 ? 16 : RPS_I * GI * 2;
-        prefetch_l2(a.down.s + (e * H + r0) * GI, sb);
-        prefetch_l2(a.down.b + (e * H + r0) * GI, sb);
-      }
-    }
+  }
+  // this block's routed down rows, into L2
+  for (int j = threadIdx.x; j < nq_cta * Ur; j += kFusedThreads) {
+    const size_t e = (size_t)s_uexp[j % Ur];
+    const size_t r0 = (size_t)(blockIdx.x + (j / Ur) * gridDim.x) * RPS_I;
+    prefetch_l2(a.down.w + (e * H + r0) * (GI * 8), RPS_I * GI * 32);
+    prefetch_l2(a.down.s + (e * H + r0) * GI, sb_bytes);
+    prefetch_l2(a.down.b + (e * H + r0) * GI, sb_bytes);
   }
   if (!grid_barrier(w.hdr, &s_abort)) return;
 
   // ------------------------------------------------------------------ phase C
-  for (int i = threadIdx.x; i < Pr * I; i += kFusedThreads) s_h[i] = __ldcg(w.h + i);
+  const int P = s_ubase[U];  // routed pairs, then the shared expert's T pairs
+  stage_rows(s_h, w.h, P * I);
   __syncthreads();
-  for (int q = q_own; q < nquads; q += nw) {
-    const int row = q * RPS_I + ri;
-    float acc[kFusedMaxT];
+  constexpr int ROWS = kFusedMaxQ * RPS_I;  // rows of this block, at most
+  __shared__ float s_part[kFusedMaxT * (kMaxK + 1)][ROWS];
+  for (int pr = warp; pr < P; pr += kFusedWarps) {
+    const int e = s_pair_e[pr];
+    const bool sh = (e == E);
+    DownRow dr[kFusedMaxQ];
 #pragma unroll
-    for (int t = 0; t < kFusedMaxT; ++t) acc[t] = (q == q_own) ? yacc[t] : 0.f;
-    for (int pr = 0; pr < Pr; ++pr) {
-      const size_t e = (size_t)s_pair_e[pr];
-      const size_t wo = (e * H + row) * (GI * 8) + 8 * gi, so = (e * H + row) * GI + gi;
-      const uint4 d0 = ld_stream(a.down.w + wo), d1 = ld_stream(a.down.w + wo + 4);
-      const float ds = bf16f(ld_u16(a.down.s + so)), db = bf16f(ld_u16(a.down.b + so));
-      XGroup xg;
-      xgroup_from(xg, s_h + (size_t)pr * I + kGroup * gi);
-      const float dd = seg_sum<GI>(q4_group_dot(d0, d1, xg, ds, db));
-      const int t = s_pair_tok[pr];
-#pragma unroll
-      for (int tt = 0; tt < kFusedMaxT; ++tt)
-        if (tt == t) acc[tt] += s_pair_w[pr] * dd;
+    for (int qi = 0; qi < kFusedMaxQ; ++qi) {
+      if (qi < nq_cta) {
+        const int row = (blockIdx.x + qi * gridDim.x) * RPS_I + ri;
+        if (sh)
+          load_down_mat<GI>(a.sh_down, 0, row, H, gi, dr[qi]);
+        else
+          load_down_mat<GI>(a.down, e, row, H, gi, dr[qi]);
+      }
     }
-    if (gi == 0) {
+    XGroup xg;
+    xgroup_from(xg, s_h + (size_t)pr * I + kGroup * gi);
+    const float pw = s_pair_w[pr];
 #pragma unroll
-      for (int t = 0; t < kFusedMaxT; ++t)
-        if (t < T) a.y[(size_t)t * H + row] = f2bf16_rne(acc[t]);
+    for (int qi = 0; qi < kFusedMaxQ; ++qi) {
+      if (qi < nq_cta) {
+        const float dd = seg_sum<GI>(q4_group_dot(dr[qi].w0, dr[qi].w1, xg, dr[qi].s, dr[qi].b));
+        if (gi == 0) s_part[pr][qi * RPS_I + ri] = pw * dd;
+      }
     }
+  }
+  __syncthreads();
+  const int nrows_cta = nq_cta * RPS_I;
+  for (int j = threadIdx.x; j < T * nrows_cta; j += kFusedThreads) {
+    const int t = j / nrows_cta, rr = j % nrows_cta;
+    const int row = (blockIdx.x + (rr / RPS_I) * gridDim.x) * RPS_I + rr % RPS_I;
+    float acc = 0.f;
+    for (int pr = 0; pr < P; ++pr)
+      if (s_pair_tok[pr] == t) acc += s_part[pr][rr];
+    a.y[(size_t)t * H + row] = f2bf16_rne(acc);
   }
 }
 
@@ -727,8 +785,8 @@ static bool fused_ok(const lily_q4_moe_layer &L, int T) {
   if ((size_t)P * L.inter * sizeof(float) > kFusedSmemMax) return false;
   if (T > kFusedMaxT) return false;
   const int GH = L.hidden / kGroup, GI = L.inter / kGroup;
-  // each warp owns at most one down row-step (its shared-expert partial stays in registers)
-  if (L.hidden / (32 / GI) > sm_count() * kFusedWarps) return false;
+  // each block owns at most kFusedMaxQ down row-steps
+  if (L.hidden / (32 / GI) > sm_count() * kFusedMaxQ) return false;
   return (GH == 32 && GI == 8) || (GH == 4 && GI == 2 && L.n_experts <= 256);
 }
 

@@ -50,6 +50,10 @@ constexpr int kScSlots = 4;    // scale-block slots
 constexpr long long kWaitCycles = 4000000000LL;  // ~2 s at GB300 clocks
 constexpr int kHdrItemsGU = 8, kHdrItemsDN = 9;
 
+// The router GEMM splits K so that more SMs share its few tiles; the partial logits are
+// summed in a fixed order by the top-k kernel.
+__host__ __device__ constexpr int kRouterSplit(int H) { return H >= 1024 ? 4 : 1; }
+
 enum { kRouter = 0, kGateUp = 1, kDown = 2 };
 
 template <int MODE>
@@ -81,6 +85,7 @@ struct GemmArgs {
   const int4 *items;
   const int32_t *n_items_ptr;
   int n_items_static, mt_static, T;
+  int ksplit;                    // router: K is split in ksplit parts (partial logits)
   uint16_t *h_out;
   uint16_t *o_out;
   int o_ld;                      // H
@@ -107,9 +112,10 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
 
 template <int MODE>
 __device__ __forceinline__ int4 get_item(const GemmArgs &a, int i) {
-  if (MODE == kRouter) {
-    const int mt = i % a.mt_static, t0 = (i / a.mt_static) * kBN;
-    return make_int4(0, t0, min(kBN, a.T - t0), mt);
+  if (MODE == kRouter) {  // (k split, first token, tokens, m-tile)
+    const int mt = i % a.mt_static, rest = i / a.mt_static;
+    const int split = rest % a.ksplit, t0 = (rest / a.ksplit) * kBN;
+    return make_int4(split, t0, min(kBN, a.T - t0), mt);
   }
   return a.items[i];
 }
@@ -152,8 +158,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const Gem
   __shared__ volatile int s_abort;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n_items = MODE == kRouter ? a.n_items_static : *(volatile const int32_t *)a.n_items_ptr;
-  const int nkb = a.K / 64;
   const int G = a.K / 64;  // groups per row
+  const int nkb = MODE == kRouter ? G / a.ksplit : G;  // k-blocks per item
 
   if (threadIdx.x == 0) {
     s_abort = 0;
@@ -213,11 +219,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const Gem
             }
           }
         } else {
-          const float bias = (row_ok && a.bias) ? a.bias[m] : 0.f;
+          float *part = a.logits + (size_t)item.x * a.T * a.E;  // partial of k split item.x
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
             const int n = c0 + i;
-            if (row_ok && n < ntok) a.logits[(size_t)(item.y + n) * a.E + m] = d[i] + bias;
+            if (row_ok && n < ntok) part[(size_t)(item.y + n) * a.E + m] = d[i];
           }
         }
       }
@@ -268,35 +274,45 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const Gem
     __syncwarp();
   } else if (warp >= kBWarp0 && warp < kAWarp0) {
     // ------------------------------------------------------------------ token-row gather
+    constexpr int QB = (kBN * 8 + kBThreads - 1) / kBThreads;  // 16-byte chunks per thread
     const int tb = threadIdx.x - kBWarp0 * 32;
-    int st = 0;
+    int stage = 0;
+    uint32_t phase = 0;
     bool ok = true;
     for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
       const int4 item = get_item<MODE>(a, it);
-      const int ntok = item.z, npad = (ntok + 15) & ~15;
-      for (int kb = 0; kb < nkb; ++kb, ++st) {
-        const int s = st % C::S;
-        if (!wait_bar(empty_bar(s), ((st / C::S) & 1) ^ 1, &s_abort, err)) {
+      const int ntok = item.z, nchunk = ((ntok + 15) & ~15) * 8;
+      const int kb0 = MODE == kRouter ? item.x * nkb : 0;
+      const uint16_t *srcp[QB];
+      uint32_t dsto[QB], nbytes[QB];
+#pragma unroll
+      for (int i = 0; i < QB; ++i) {
+        const int q = tb + i * kBThreads;
+        const int n = q >> 3, c = q & 7;
+        srcp[i] = a.b_src;
+        nbytes[i] = 0;
+        if (n < ntok) {
+          const size_t r = MODE == kGateUp ? (size_t)__ldg(a.perm + item.y + n) : (size_t)(item.y + n);
+          srcp[i] = a.b_src + r * a.K + (size_t)kb0 * 64 + 8 * c;
+          nbytes[i] = 16;
+        }
+        dsto[i] = tc::sw128((uint32_t)n, (uint32_t)c);
+      }
+      for (int kb = 0; kb < nkb; ++kb) {
+        if (!wait_bar(empty_bar(stage), phase ^ 1, &s_abort, err)) {
           ok = false;
           break;
         }
-        const uint32_t sB = sbase + s * C::STAGE + C::NA * C::A_BYTES;
-        for (int q = tb; q < npad * 8; q += kBThreads) {
-          const int n = q >> 3, c = q & 7;
-          const uint16_t *src = a.b_src;
-          uint32_t bytes = 0;
-          if (n < ntok) {
-            size_t row;
-            if (MODE == kGateUp)
-              row = (size_t)__ldg(a.perm + item.y + n);
-            else
-              row = (size_t)(item.y + n);
-            src = a.b_src + row * a.K + kb * 64 + 8 * c;
-            bytes = 16;
-          }
-          tc::cp_async16(sB + tc::sw128(n, c), src, bytes);
+        const uint32_t sB = sbase + stage * C::STAGE + C::NA * C::A_BYTES;
+#pragma unroll
+        for (int i = 0; i < QB; ++i)
+          if (tb + i * kBThreads < nchunk)
+            tc::cp_async16(sB + dsto[i], srcp[i] + (nbytes[i] ? kb * 64 : 0), nbytes[i]);
+        tc::cp_async_arrive_noinc(full_bar(stage));
+        if (++stage == C::S) {
+          stage = 0;
+          phase ^= 1;
         }
-        tc::cp_async_arrive_noinc(full_bar(s));
       }
     }
     tc::cp_async_wait_all();
@@ -323,7 +339,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const Gem
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
             const int c = 4 * half + i;
-            const uint16_t *src = valid ? a.a_bf16 + (size_t)m * a.K + kb * 64 + 8 * c : a.a_bf16;
+            const uint16_t *src =
+                valid ? a.a_bf16 + (size_t)m * a.K + (item.x * nkb + kb) * 64 + 8 * c : a.a_bf16;
             tc::cp_async16(sA + tc::sw128(row, c), src, valid ? 16u : 0u);
           }
           tc::cp_async_arrive_noinc(full_bar(s));
@@ -332,38 +349,59 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const Gem
       tc::cp_async_wait_all();
     } else {
       // Continuous k-block stream over this CTA's items; the issue side runs kRing-1
-      // k-blocks ahead of the consume side.
+      // k-blocks ahead of the consume side.  Per-item pointers are computed once per item.
       constexpr int WPT = C::NA == 2 ? 8 : 4;  // code words per thread per k-block
       const int woff = C::NA == 2 ? 0 : 4 * half;
-      const uint32_t raw0 = sbase + C::OFF_RAW;
-      const uint32_t sc0 = sbase + C::OFF_SC;
-      const uint8_t *raw_p = smem + C::OFF_RAW;
-      const uint8_t *sc_p = smem + C::OFF_SC;
+      const uint32_t raw_off = (uint32_t)((mat * kBM + row) * 32 + woff * 4);
+      const uint32_t raw0 = sbase + C::OFF_RAW + raw_off;
+      const uint32_t sc0 = sbase + C::OFF_SC + (uint32_t)(((half * 2) * kBM + row) * 16);
+      const uint8_t *raw_p = smem + C::OFF_RAW + raw_off;
+      const uint8_t *sc_p = smem + C::OFF_SC + ((half * 2) * kBM + row) * 16;
+      const uint32_t a_row_off = (uint32_t)(mat * C::A_BYTES + row * 128);
+      const uint32_t rsw = (uint32_t)(row & 7);
       // issue iterator
-      int i_it = blockIdx.x, i_kb = 0, i_g = 0, i_sg = 0;
-      auto issue = [&]() {
+      int i_it = blockIdx.x, i_kb = 0;
+      uint32_t i_g = 0, i_sg = 0;
+      bool i_valid = false;
+      const uint32_t *i_w = nullptr;
+      const uint16_t *i_s = nullptr, *i_b = nullptr;
+      auto issue_item = [&]() {
+        i_valid = false;
         if (i_it < n_items) {
           const int4 item = a.items[i_it];
           const int e = item.x, m = item.w * kBM + row;
           if (m < a.a_rows) {
             const bool sh = (e == a.E);
             const lily_q4_mat &W = sh ? (mat ? a.sh1 : a.sh0) : (mat ? a.a1 : a.a0);
-            const size_t wbase = (sh ? 0 : (size_t)e * a.a_rows * (a.K / 8)) + (size_t)m * (a.K / 8);
-            const size_t sbase_e = (sh ? 0 : (size_t)e * a.a_rows * G) + (size_t)m * G;
-            const uint32_t dst = raw0 + (i_g % kRing) * C::RAW_SLOT + (mat * kBM + row) * 32 + woff * 4;
-            const uint32_t *src = W.w + wbase + i_kb * 8 + woff;
+            const size_t r = (sh ? 0 : (size_t)e * a.a_rows) + (size_t)m;
+            i_w = W.w + r * (size_t)(a.K / 8) + woff;
+            i_s = W.s + r * (size_t)G;
+            i_b = W.b + r * (size_t)G;
+            i_valid = true;
+          }
+        }
+      };
+      issue_item();
+      auto issue = [&]() {
+        if (i_it < n_items) {
+          if (i_valid) {
+            const uint32_t dst = raw0 + (i_g & (kRing - 1)) * C::RAW_SLOT;
+            const uint32_t *src = i_w + i_kb * 8;
             tc::cp_async16(dst, src, 16);
             if (WPT == 8) tc::cp_async16(dst + 16, src + 4, 16);
             if ((i_kb & 7) == 0) {
               // scale block: s and b of k-blocks i_kb .. i_kb+7 (fewer when G < 8)
               const int nb = min(8, G - i_kb);
-              const uint32_t sdst = sc0 + (i_sg % kScSlots) * C::SC_SLOT;
-              for (int arr = 0; arr < 2; ++arr) {
-                const uint16_t *ssrc = (arr ? W.b : W.s) + sbase_e + i_kb;
-                const uint32_t d = sdst + ((half * 2 + arr) * kBM + row) * 16;
-                if (nb == 8) tc::cp_async16(d, ssrc, 16);
-                else if (nb == 4) tc::cp_async8(d, ssrc);
-                else tc::cp_async4(d, ssrc);
+              const uint32_t sdst = sc0 + (i_sg & (kScSlots - 1)) * C::SC_SLOT;
+              if (nb == 8) {
+                tc::cp_async16(sdst, i_s + i_kb, 16);
+                tc::cp_async16(sdst + kBM * 16, i_b + i_kb, 16);
+              } else if (nb == 4) {
+                tc::cp_async8(sdst, i_s + i_kb);
+                tc::cp_async8(sdst + kBM * 16, i_b + i_kb);
+              } else {
+                tc::cp_async4(sdst, i_s + i_kb);
+                tc::cp_async4(sdst + kBM * 16, i_b + i_kb);
               }
             }
           }
@@ -372,36 +410,33 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const Gem
           if (++i_kb == nkb) {
             i_kb = 0;
             i_it += gridDim.x;
+            issue_item();
           }
         }
         tc::cp_async_commit();
       };
       for (int p = 0; p < kRing - 1; ++p) issue();
-      int st = 0, c_g = 0, c_sg = -1;
+      int stage = 0;
+      uint32_t phase = 0, c_g = 0, c_sg = 0xFFFFFFFFu;
       for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
         const int4 item = a.items[it];
-        const int m = item.w * kBM + row;
-        const bool valid = m < a.a_rows;
-        for (int kb = 0; kb < nkb; ++kb, ++st, ++c_g) {
+        const bool valid = item.w * kBM + row < a.a_rows;
+        for (int kb = 0; kb < nkb; ++kb, ++c_g) {
           if ((kb & 7) == 0) ++c_sg;
           issue();
           tc::cp_async_wait<kRing - 1>();
           uint4 outv[WPT];
           if (valid) {
-            const uint8_t *rp = raw_p + (c_g % kRing) * C::RAW_SLOT + (mat * kBM + row) * 32 + woff * 4;
+            const uint8_t *rp = raw_p + (c_g & (kRing - 1)) * C::RAW_SLOT;
             const uint4 w0 = *reinterpret_cast<const uint4 *>(rp);
             uint4 w1 = make_uint4(0, 0, 0, 0);
             if (WPT == 8) w1 = *reinterpret_cast<const uint4 *>(rp + 16);
-            const uint8_t *sp = sc_p + (c_sg % kScSlots) * C::SC_SLOT;
-            const int gi = kb & 7;
-            const uint16_t sbits =
-                *reinterpret_cast<const uint16_t *>(sp + ((half * 2 + 0) * kBM + row) * 16 + 2 * gi);
-            const uint16_t bbits =
-                *reinterpret_cast<const uint16_t *>(sp + ((half * 2 + 1) * kBM + row) * 16 + 2 * gi);
-            const __nv_bfloat162 s2 = __halves2bfloat162(*reinterpret_cast<const __nv_bfloat16 *>(&sbits),
-                                                         *reinterpret_cast<const __nv_bfloat16 *>(&sbits));
-            const __nv_bfloat162 b2 = __halves2bfloat162(*reinterpret_cast<const __nv_bfloat16 *>(&bbits),
-                                                         *reinterpret_cast<const __nv_bfloat16 *>(&bbits));
+            const uint8_t *sp = sc_p + (c_sg & (kScSlots - 1)) * C::SC_SLOT + 2 * (kb & 7);
+            const uint32_t sbits = *reinterpret_cast<const uint16_t *>(sp);
+            const uint32_t bbits = *reinterpret_cast<const uint16_t *>(sp + kBM * 16);
+            uint32_t s2u = sbits | (sbits << 16), b2u = bbits | (bbits << 16);
+            const __nv_bfloat162 s2 = *reinterpret_cast<__nv_bfloat162 *>(&s2u);
+            const __nv_bfloat162 b2 = *reinterpret_cast<__nv_bfloat162 *>(&b2u);
             const uint32_t ws[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
 #pragma unroll
             for (int q = 0; q < WPT; ++q) outv[q] = dequant_word(ws[q], s2, b2);
@@ -409,17 +444,20 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const Gem
 #pragma unroll
             for (int q = 0; q < WPT; ++q) outv[q] = make_uint4(0, 0, 0, 0);
           }
-          const int s = st % C::S;
-          if (!wait_bar(empty_bar(s), ((st / C::S) & 1) ^ 1, &s_abort, err)) {
+          if (!wait_bar(empty_bar(stage), phase ^ 1, &s_abort, err)) {
             ok = false;
             break;
           }
-          uint8_t *sA = smem + s * C::STAGE + mat * C::A_BYTES;
+          uint8_t *sA = smem + stage * C::STAGE + a_row_off;
 #pragma unroll
           for (int q = 0; q < WPT; ++q)
-            *reinterpret_cast<uint4 *>(sA + tc::sw128(row, woff + q)) = outv[q];
+            *reinterpret_cast<uint4 *>(sA + ((((uint32_t)(woff + q)) ^ rsw) << 4)) = outv[q];
           tc::fence_proxy_async();
-          tc::mbar_arrive(full_bar(s));
+          tc::mbar_arrive(full_bar(stage));
+          if (++stage == C::S) {
+            stage = 0;
+            phase ^= 1;
+          }
         }
       }
       tc::cp_async_wait_all();
@@ -456,7 +494,9 @@ __global__ void x_perm_kernel(const uint4 *__restrict__ x, uint4 *__restrict__ x
 }
 
 struct TopkArgs {
-  const float *logits;
+  const float *logits;  // [nsplit][T][E] partials
+  const float *bias;    // [E] or NULL
+  int nsplit;
   const uint16_t *x;
   const uint16_t *shared_gate;
   int T, E, H, k, has_shared;
@@ -468,25 +508,37 @@ struct TopkArgs {
   float *out_w;
 };
 
-// One warp per token: k rounds of a warp argmax (logit desc, index asc), softmax over
-// the k, shared-expert gate.
+// One warp per token: logits = fixed-order sum of the router GEMM's K-split partials plus
+// the per-expert offsets, held in registers (EC per lane); k rounds of a warp argmax
+// (logit desc, index asc); softmax over the k; shared gate sigmoid(x . g).
+template <int EC>
 __global__ void __launch_bounds__(256) topk_prefill_kernel(TopkArgs a) {
   const int lane = threadIdx.x & 31;
   const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
   if (t >= a.T) return;
-  const float *lg = a.logits + (size_t)t * a.E;
+  float lv[EC];
+#pragma unroll
+  for (int j = 0; j < EC; ++j) {
+    const int e = lane + 32 * j;
+    float v = -FLT_MAX;
+    if (e < a.E) {
+      v = 0.f;
+      for (int sp = 0; sp < a.nsplit; ++sp) v += a.logits[((size_t)sp * a.T + t) * a.E + e];
+      if (a.bias) v += a.bias[e];
+    }
+    lv[j] = v;
+  }
   uint32_t taken = 0;
   float sel_v[16];
   int sel_e[16];
   for (int i = 0; i < a.k; ++i) {
     float bv = -FLT_MAX;
     int be = INT_MAX;
-    for (int j = 0; lane + 32 * j < a.E; ++j) {
-      if (taken & (1u << j)) continue;
+#pragma unroll
+    for (int j = 0; j < EC; ++j) {
       const int e = lane + 32 * j;
-      const float v = lg[e];
-      if (better(v, e, bv, be)) {
-        bv = v;
+      if (e < a.E && !(taken & (1u << j)) && better(lv[j], e, bv, be)) {
+        bv = lv[j];
         be = e;
       }
     }
@@ -609,8 +661,11 @@ struct PermArgs {
   int T, E, k;
 };
 
-// Block e: the pairs choosing expert e, in token order (stable bucketing).
-__global__ void __launch_bounds__(256) perm_kernel(PermArgs a) {
+// Block e: the pairs choosing expert e, in token order (stable bucketing).  Each of the
+// 32 warps owns a contiguous slice of the (token, slot) entries: it counts its matches with
+// ballots, the warps' counts are scanned, then each warp places its matches in order.
+constexpr int kPermThreads = 1024;
+__global__ void __launch_bounds__(kPermThreads) perm_kernel(PermArgs a) {
   const int e = blockIdx.x;
   const int kk = a.k + 1;
   if (e == a.E) {  // shared expert: every token, in order
@@ -622,30 +677,38 @@ __global__ void __launch_bounds__(256) perm_kernel(PermArgs a) {
     }
     return;
   }
-  __shared__ int s_wsum[8];
+  __shared__ int s_cnt[32];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int n = a.T * a.k;
-  int running = a.offsets[e];
-  for (int base = 0; base < n; base += 256) {
-    const int j = base + threadIdx.x;
-    const bool f = j < n && __ldg(a.idx + j) == e;
+  const int slice = ((n + 31) / 32 + 31) & ~31;  // entries per warp, a multiple of 32
+  const int lo = warp * slice, hi = min(n, lo + slice);
+  int cnt = 0;
+  for (int j0 = lo; j0 < hi; j0 += 32) {
+    const int j = j0 + lane;
+    cnt += __popc(__ballot_sync(0xffffffffu, j < hi && __ldg(a.idx + j) == e));
+  }
+  if (lane == 0) s_cnt[warp] = cnt;
+  __syncthreads();
+  if (warp == 0) {
+    int tot;
+    const int ex = warp_excl_scan(s_cnt[lane], &tot);
+    __syncwarp();
+    s_cnt[lane] = ex;
+  }
+  __syncthreads();
+  int pos0 = a.offsets[e] + s_cnt[warp];
+  for (int j0 = lo; j0 < hi; j0 += 32) {
+    const int j = j0 + lane;
+    const bool f = j < hi && __ldg(a.idx + j) == e;
     const unsigned bal = __ballot_sync(0xffffffffu, f);
-    if (lane == 0) s_wsum[warp] = __popc(bal);
-    __syncthreads();
-    int before = 0, total = 0;
-    for (int w = 0; w < 8; ++w) {
-      if (w < warp) before += s_wsum[w];
-      total += s_wsum[w];
-    }
     if (f) {
-      const int pos = running + before + __popc(bal & ((1u << lane) - 1));
+      const int pos = pos0 + __popc(bal & ((1u << lane) - 1));
       const int t = j / a.k, i = j % a.k;
       a.perm[pos] = t;
       a.pw[pos] = a.p[j];
       a.inv[t * kk + i] = pos;
     }
-    running += total;
-    __syncthreads();
+    pos0 += __popc(bal);
   }
 }
 
@@ -697,7 +760,7 @@ PrefillWsLayout prefill_ws_layout(const lily_q4_moe_layer &L, int T) {
     off = align_up(off + bytes);
     return o;
   };
-  l.off_logits = take(sizeof(float) * (size_t)T * l.E);
+  l.off_logits = take(sizeof(float) * (size_t)kRouterSplit(l.H) * T * l.E);
   l.off_idx = take(sizeof(int32_t) * (size_t)T * l.k);
   l.off_p = take(sizeof(float) * (size_t)T * l.k);
   l.off_sigma = take(sizeof(float) * (size_t)T);
@@ -767,23 +830,28 @@ int launch_moe_prefill(const lily_q4_moe_layer &L, const uint16_t *x, int T, uin
   ra.E = E;
   ra.b_src = x;
   ra.mt_static = (E + kBM - 1) / kBM;
-  ra.n_items_static = ra.mt_static * ((T + kBN - 1) / kBN);
+  ra.ksplit = kRouterSplit(H);
+  ra.n_items_static = ra.mt_static * ((T + kBN - 1) / kBN) * ra.ksplit;
   ra.T = T;
-  ra.logits = logits;
-  ra.bias = L.router_bias;
+  ra.logits = logits;  // partial logits [ksplit][T][E]
   ra.hdr = hdr;
   int rc = launch_gemm<kRouter>(ra, ra.n_items_static < sms ? ra.n_items_static : sms, st);
   if (rc != LILY_Q4_OK) return rc;
 
-  TopkArgs ta{logits, x, L.shared_gate, T, E, H, k, L.has_shared, idx, p, sigma, counts,
-              topk_idx, topk_w};
-  topk_prefill_kernel<<<(T + 7) / 8, 256, 0, st>>>(ta);
+  TopkArgs ta{logits, L.router_bias, ra.ksplit, x, L.shared_gate, T, E, H, k, L.has_shared,
+              idx, p, sigma, counts, topk_idx, topk_w};
+  if (E <= 256)
+    topk_prefill_kernel<8><<<(T + 7) / 8, 256, 0, st>>>(ta);
+  else if (E <= 512)
+    topk_prefill_kernel<16><<<(T + 7) / 8, 256, 0, st>>>(ta);
+  else
+    topk_prefill_kernel<32><<<(T + 7) / 8, 256, 0, st>>>(ta);
 
   ScanArgs sa{counts, offsets, items_gu, items_dn, hdr, T, E, k, L.has_shared, mt_gu, mt_dn};
   scan_items_kernel<<<1, 1024, 0, st>>>(sa);
 
   PermArgs pa{idx, p, sigma, offsets, perm, pw, inv, T, E, k};
-  perm_kernel<<<nexp, 256, 0, st>>>(pa);
+  perm_kernel<<<nexp, kPermThreads, 0, st>>>(pa);
 
   GemmArgs ga{};
   ga.a0 = L.gate;

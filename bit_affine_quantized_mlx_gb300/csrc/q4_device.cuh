@@ -10,7 +10,7 @@
 // per group.  Codes become floats with the bf16 magic-number trick: OR-ing a
 // nibble into the low mantissa bits of bf16 128.0 (0x4300) gives exactly 128+q.
 // One LOP3 turns nibbles j and j+4 of a word into such a bf16 pair.  The low half,
-// shifted up, is the fp32 value 128+q_j exactly.  The word itself read as fp32 is
+// moved to the high half, is the fp32 value 128+q_j exactly.  The word itself read as fp32 is
 // 128.26171875 + q_{j+4} + q_j/65536; the q_j/65536 term is cancelled exactly by
 // pre-subtracting x_{j+4}/65536 from the x that multiplies the low half.  Summing
 // (w32 * x_hi + lo32 * x_lo') over the group therefore gives
@@ -91,22 +91,36 @@ __device__ __forceinline__ void xgroup_from_bf16(XGroup &g, const uint4 *chunks)
 }
 
 // sum_k q_k * x_k + C for one group of 8 words (accumulation only, s/b not applied).
+// Per word: three shifts and four LOP3 on the integer pipe; the low half of each pair is
+// moved up with an integer multiply, which issues on the FMA pipe, leaving the integer
+// pipe (the bottleneck of this loop) with under one operation per weight.
 __device__ __forceinline__ float q4_group_raw(const uint4 w0, const uint4 w1, const XGroup &g) {
   const uint32_t w[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
-  float2 a0 = make_float2(0.f, 0.f), a1 = make_float2(0.f, 0.f);
+  float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
 #pragma unroll
   for (int m = 0; m < 8; ++m) {
+    uint32_t ws[4];
+    ws[0] = w[m];
+    asm("shr.b32 %0, %1, 4;" : "=r"(ws[1]) : "r"(w[m]));
+    asm("shr.b32 %0, %1, 8;" : "=r"(ws[2]) : "r"(w[m]));
+    asm("shr.b32 %0, %1, 12;" : "=r"(ws[3]) : "r"(w[m]));
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      const uint32_t v = ((w[m] >> (4 * j)) & 0x000F000Fu) | 0x43004300u;
-      const float2 f = make_float2(__uint_as_float(v), __uint_as_float(v << 16));
-      if (j & 1)
-        a1 = __ffma2_rn(f, g.xv[4 * m + j], a1);
-      else
-        a0 = __ffma2_rn(f, g.xv[4 * m + j], a0);
+      uint32_t v, lo;
+      // v = (ws & 0x000F000F) | 0x43004300: the bf16 pair (128 + q_j, 128 + q_j+4)
+      asm("lop3.b32 %0, %1, 0x000F000F, 0x43004300, 0xEA;" : "=r"(v) : "r"(ws[j]));
+      asm("mul.lo.u32 %0, %1, 65536;" : "=r"(lo) : "r"(v));
+      const float2 xv = g.xv[4 * m + j];
+      if (j & 1) {
+        a0 = fmaf(__uint_as_float(v), xv.x, a0);
+        a1 = fmaf(__uint_as_float(lo), xv.y, a1);
+      } else {
+        a2 = fmaf(__uint_as_float(v), xv.x, a2);
+        a3 = fmaf(__uint_as_float(lo), xv.y, a3);
+      }
     }
   }
-  return (a0.x + a1.x) + (a0.y + a1.y);
+  return (a0 + a2) + (a1 + a3);
 }
 
 // Dot product of one dequantised 64-group with the prepared x: s*(sum q x) + b*(sum x).
