@@ -17,6 +17,7 @@ enum HeaderWord : int {
   kHdrCounterA = 1, // last-block-done counters (self-resetting)
   kHdrCounterB = 2,
   kHdrCounterC = 3,
+  kHdrBarrier64 = 4,  // words 4-5: 64-bit grid-barrier arrival count
   kHdrWords = 64,
 };
 

@@ -53,13 +53,13 @@ __global__ void __launch_bounds__(kLmThreads, kLmBlocksPerSm)
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int g = lane % G, rsub = lane / G;
 
-  XGroup xg;
+  XGroupB xg;
   {
     uint4 c[8];
     const uint4 *xp = reinterpret_cast<const uint4 *>(x + kGroup * g);
 #pragma unroll
     for (int i = 0; i < 8; ++i) c[i] = __ldg(xp + i);
-    xgroup_from_bf16(xg, c);
+    xgroupb_from_bf16(xg, c);
   }
 
   float best_v = -FLT_MAX;
@@ -88,7 +88,7 @@ __global__ void __launch_bounds__(kLmThreads, kLmBlocksPerSm)
     }
 #pragma unroll
     for (int u = 0; u < U; ++u) {
-      float d = seg_sum<G>(q4_group_dot(wa[u], wb[u], xg, sv[u], bv[u]));
+      float d = seg_sum<G>(q4_group_dot_b(wa[u], wb[u], xg, sv[u], bv[u]));
       const int row = r0 + u * RPS + rsub;
       if (g == 0 && row < N) {
         if (logits) logits[row] = d;

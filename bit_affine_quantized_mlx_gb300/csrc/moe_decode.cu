@@ -354,18 +354,18 @@ __global__ void __launch_bounds__(kGateUpThreads)
   }
   for (int pr = pb; pr < pe; ++pr) {
     const int t = w.pair_tok[pr];
-    XGroup xg;
+    XGroupB xg;
     {
       uint4 c[8];
       const uint4 *xp = reinterpret_cast<const uint4 *>(a.x + (size_t)t * a.H + kGroup * g);
 #pragma unroll
       for (int i = 0; i < 8; ++i) c[i] = __ldg(xp + i);
-      xgroup_from_bf16(xg, c);
+      xgroupb_from_bf16(xg, c);
     }
 #pragma unroll
     for (int st = 0; st < kGateUpSteps; ++st) {
-      const float gd = seg_sum<G>(q4_group_dot(ga[st], gb2[st], xg, gsv[st], gbv[st]));
-      const float ud = seg_sum<G>(q4_group_dot(ua[st], ub2[st], xg, usv[st], ubv[st]));
+      const float gd = seg_sum<G>(q4_group_dot_b(ga[st], gb2[st], xg, gsv[st], gbv[st]));
+      const float ud = seg_sum<G>(q4_group_dot_b(ua[st], ub2[st], xg, usv[st], ubv[st]));
       const int row = row0 + st * RPS + rsub;
       if (g == 0 && row < a.I) w.h[(size_t)pr * a.I + row] = silu_mul(gd, ud);
     }
@@ -521,32 +521,170 @@ __device__ __forceinline__ void stage_rows(float *dst, const float *src, int n) 
   }
 }
 
-// Self-resetting grid barrier (count word, generation word) with a bounded wait.
-__device__ bool grid_barrier(int32_t *hdr, volatile int *s_abort) {
+// Grid barrier on a 64-bit arrival counter that only grows: each block adds 1 per barrier
+// (a fire-and-forget release reduction) and polls until the count reaches its target.  The
+// count after a completed launch is a multiple of the grid size, so a block derives this
+// launch's base from the value it reads before its first arrival (no block can pass the
+// first barrier before every block has arrived).  After a timed-out wait the count is off
+// and the workspace must be re-initialised.
+__device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long *p) {
+  unsigned long long v;
+  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ unsigned long long barrier_base(int32_t *hdr) {
+  const unsigned long long c =
+      ld_acquire_u64(reinterpret_cast<unsigned long long *>(hdr + kHdrBarrier64));
+  return c - c % gridDim.x;
+}
+
+__device__ bool grid_barrier(int32_t *hdr, unsigned long long target, volatile int *s_abort) {
   __syncthreads();
   if (threadIdx.x == 0 && !*s_abort) {
-    int32_t *cnt = hdr + kHdrCounterC, *gen = hdr + kHdrCounterC + 1;
-    const int g = ld_acquire(gen);
+    unsigned long long *cnt = reinterpret_cast<unsigned long long *>(hdr + kHdrBarrier64);
     __threadfence();
-    if (atomicAdd(cnt, 1) == (int)gridDim.x - 1) {
-      *(volatile int32_t *)cnt = 0;
-      __threadfence();
-      atomicAdd(gen, 1);
-    } else {
-      const long long t0 = clock64();
-      while (ld_acquire(gen) == g) {
-        if (clock64() - t0 > kBarrierCycles) {
-          atomicExch(hdr + kHdrError, 2);
-          *s_abort = 1;
-          break;
-        }
-        __nanosleep(64);
+    asm volatile("red.release.gpu.global.add.u64 [%0], 1;" ::"l"(cnt) : "memory");
+    const long long t0 = clock64();
+    while (ld_acquire_u64(cnt) < target) {
+      if (clock64() - t0 > kBarrierCycles) {
+        atomicExch(hdr + kHdrError, 2);
+        *s_abort = 1;
+        break;
       }
     }
-    __threadfence();
   }
   __syncthreads();
   return !*s_abort;
+}
+
+// Routing of up to 4 tokens by one block, for the single-launch path: warps 0..T-1 take
+// the top-k of one token each; warp 0 then builds the unique-expert table with a bitmap
+// of selected experts (ascending id) and places the (token, weight) pairs.
+template <int EC>
+__device__ void route_small(const float *logits, const float *sigma, int T, int E, int k,
+                            int has_shared, const RouteDst &d) {
+  __shared__ int s_idx[4 * kMaxK];
+  __shared__ float s_p[4 * kMaxK];
+  __shared__ int s_cnt[4 * kMaxK + 1];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (warp < T) {
+    const int t = warp;
+    const float *lg = logits + (size_t)t * E;
+    float lv[EC];
+#pragma unroll
+    for (int j = 0; j < EC; ++j) lv[j] = (lane + 32 * j < E) ? __ldcg(lg + lane + 32 * j) : -FLT_MAX;
+    uint32_t taken = 0;
+    float v0 = 0.f, denom = 0.f, myv = 0.f;
+    int mye = 0;
+    for (int i = 0; i < k; ++i) {
+      float bv = -FLT_MAX;
+      int be = INT_MAX;
+#pragma unroll
+      for (int j = 0; j < EC; ++j) {
+        const int e = lane + 32 * j;
+        if (e < E && !(taken & (1u << j)) && better(lv[j], e, bv, be)) {
+          bv = lv[j];
+          be = e;
+        }
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+        const int oe = __shfl_xor_sync(0xffffffffu, be, o);
+        if (better(ov, oe, bv, be)) {
+          bv = ov;
+          be = oe;
+        }
+      }
+      if ((be & 31) == lane) taken |= 1u << (be >> 5);
+      if (i == 0) v0 = bv;
+      denom += expf(bv - v0);
+      if (lane == i) {  // lane i keeps selection i
+        myv = bv;
+        mye = be;
+      }
+    }
+    if (lane < k) {
+      const float pi = expf(myv - v0) / denom;
+      s_idx[t * k + lane] = mye;
+      s_p[t * k + lane] = pi;
+      if (d.out_idx) d.out_idx[t * k + lane] = mye;
+      if (d.out_w) d.out_w[t * k + lane] = pi;
+    }
+  }
+  __syncthreads();
+  if (warp == 0) {
+    const int n = T * k;  // <= 64
+    uint32_t word = 0;    // lane's 32 experts: bit set if selected
+    for (int j = 0; j < n; ++j) {
+      const int e = s_idx[j];
+      if ((e >> 5) == lane) word |= 1u << (e & 31);
+    }
+    int total;
+    const int prefix = warp_excl_scan(__popc(word), &total);
+    // unique experts in ascending id
+    {
+      uint32_t wb = word;
+      int r = prefix;
+      while (wb) {
+        const int b = __ffs(wb) - 1;
+        wb &= wb - 1;
+        d.uexp[r++] = lane * 32 + b;
+      }
+    }
+    for (int r = lane; r <= 4 * kMaxK; r += 32) s_cnt[r] = 0;
+    __syncwarp();
+    int rk[2], ek[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int j = lane + 32 * h;
+      const int e = j < n ? s_idx[j] : 0;
+      const uint32_t wsrc = __shfl_sync(0xffffffffu, word, (e >> 5) & 31);
+      const int psrc = __shfl_sync(0xffffffffu, prefix, (e >> 5) & 31);
+      rk[h] = psrc + __popc(wsrc & ((1u << (e & 31)) - 1u));
+      ek[h] = e;
+      if (j < n) atomicAdd(&s_cnt[rk[h]], 1);
+    }
+    __syncwarp();
+    // exclusive scan of the counts of the (<= 64) unique experts: two per lane
+    const int c0 = lane * 2 < total ? s_cnt[lane * 2] : 0;
+    const int c1 = lane * 2 + 1 < total ? s_cnt[lane * 2 + 1] : 0;
+    int dummy;
+    const int b0 = warp_excl_scan(c0 + c1, &dummy);
+    if (lane * 2 < total) d.ubase[lane * 2] = b0;
+    if (lane * 2 + 1 < total) d.ubase[lane * 2 + 1] = b0 + c0;
+    __syncwarp();
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int j = lane + 32 * h;
+      if (j < n) {
+        const int t = j / k, e = ek[h];
+        int before = 0;  // earlier tokens that chose e
+        for (int jj = 0; jj < t * k; ++jj) before += (s_idx[jj] == e);
+        const int pos = d.ubase[rk[h]] + before;
+        d.pair_tok[pos] = t;
+        d.pair_w[pos] = s_p[j];
+        d.pair_e[pos] = e;
+      }
+    }
+    if (lane == 0) {
+      int U = total;
+      if (has_shared) {
+        d.uexp[U] = E;
+        d.ubase[U] = n;
+        ++U;
+      }
+      d.ubase[U] = n + (has_shared ? T : 0);
+      *d.U = U;
+    }
+    if (has_shared && lane < T) {
+      d.pair_tok[n + lane] = lane;
+      d.pair_w[n + lane] = __ldcg(sigma + lane);
+      d.pair_e[n + lane] = E;
+    }
+  }
+  __syncthreads();
 }
 
 // One row of a routed expert's gate and up matrices (lane's group) and one down row.
@@ -609,8 +747,13 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
   const int gh = lane % GH, rh = lane / GH;
   const int gi = lane % GI, ri = lane / GI;
   const int nquads = H / RPS_I;  // down row-steps
-  if (threadIdx.x == 0) s_abort = 0;
+  __shared__ unsigned long long s_bbase;
+  if (threadIdx.x == 0) {
+    s_abort = 0;
+    s_bbase = barrier_base(w.hdr);
+  }
   __syncthreads();
+  const unsigned long long bbase = s_bbase;
 
   // ------------------------------------------------------------------ phase A
   const int nshared_tasks = a.has_shared ? I / RPS_H : 0;
@@ -660,14 +803,14 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
       const float gs = bf16f(ld_u16(a.sh_gate.s + so)), gb = bf16f(ld_u16(a.sh_gate.b + so));
       const float us = bf16f(ld_u16(a.sh_up.s + so)), ub = bf16f(ld_u16(a.sh_up.b + so));
       for (int t = 0; t < T; ++t) {
-        XGroup xg;
+        XGroupB xg;
         uint4 c[8];
         const uint4 *xp = reinterpret_cast<const uint4 *>(a.x + (size_t)t * H + kGroup * gh);
 #pragma unroll
         for (int i = 0; i < 8; ++i) c[i] = __ldg(xp + i);
-        xgroup_from_bf16(xg, c);
-        const float gd = seg_sum<GH>(q4_group_dot(g0, g1, xg, gs, gb));
-        const float ud = seg_sum<GH>(q4_group_dot(u0, u1, xg, us, ub));
+        xgroupb_from_bf16(xg, c);
+        const float gd = seg_sum<GH>(q4_group_dot_b(g0, g1, xg, gs, gb));
+        const float ud = seg_sum<GH>(q4_group_dot_b(u0, u1, xg, us, ub));
         // shared pairs sit after the T*k routed pairs
         if (gh == 0) __stcg(w.h + (size_t)(T * k + t) * I + row, silu_mul(gd, ud));
       }
@@ -682,13 +825,13 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
     prefetch_l2(a.sh_down.s + r0 * GI, sb_bytes);
     prefetch_l2(a.sh_down.b + r0 * GI, sb_bytes);
   }
-  if (!grid_barrier(w.hdr, &s_abort)) return;
+  if (!grid_barrier(w.hdr, bbase + gridDim.x, &s_abort)) return;
 
   // ------------------------------------------------------------------ phase B
   {
     RouteDst d{nullptr, nullptr, &s_U, s_uexp, s_ubase, s_pair_tok, s_pair_w, s_pair_e,
                blockIdx.x == 0 ? a.out_idx : nullptr, blockIdx.x == 0 ? a.out_w : nullptr};
-    route_block<kFusedThreads, EC>(w.logits, w.sigma, T, E, k, a.has_shared, d);
+    route_small<EC>(w.logits, w.sigma, T, E, k, a.has_shared, d);
   }
   const int U = s_U;
   const int Ur = a.has_shared ? U - 1 : U;  // routed unique experts
@@ -702,7 +845,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
     for (int i = 0; i < kFusedBatch; ++i)
       if (base + i * nw < ntasks_b) load_gateup<GH>(a, s_uexp, base + i * nw, steps_h, I, gh, rh, rp[i]);
     int xg_tok = -1;
-    XGroup xg;
+    XGroupB xg;
 #pragma unroll
     for (int i = 0; i < kFusedBatch; ++i) {
       const int task = base + i * nw;
@@ -717,11 +860,11 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
             const uint4 *xp = reinterpret_cast<const uint4 *>(a.x + (size_t)t * H + kGroup * gh);
 #pragma unroll
             for (int q = 0; q < 8; ++q) c[q] = __ldg(xp + q);
-            xgroup_from_bf16(xg, c);
+            xgroupb_from_bf16(xg, c);
             xg_tok = t;
           }
-          const float gd = seg_sum<GH>(q4_group_dot(rp[i].a0, rp[i].a1, xg, rp[i].as, rp[i].ab));
-          const float ud = seg_sum<GH>(q4_group_dot(rp[i].b0, rp[i].b1, xg, rp[i].bs, rp[i].bb));
+          const float gd = seg_sum<GH>(q4_group_dot_b(rp[i].a0, rp[i].a1, xg, rp[i].as, rp[i].ab));
+          const float ud = seg_sum<GH>(q4_group_dot_b(rp[i].b0, rp[i].b1, xg, rp[i].bs, rp[i].bb));
           if (gh == 0) __stcg(w.h + (size_t)pr * I + row, silu_mul(gd, ud));
         }
       }
@@ -735,7 +878,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
     prefetch_l2(a.down.s + (e * H + r0) * GI, sb_bytes);
     prefetch_l2(a.down.b + (e * H + r0) * GI, sb_bytes);
   }
-  if (!grid_barrier(w.hdr, &s_abort)) return;
+  if (!grid_barrier(w.hdr, bbase + 2ull * gridDim.x, &s_abort)) return;
 
   // ------------------------------------------------------------------ phase C
   const int P = s_ubase[U];  // routed pairs, then the shared expert's T pairs

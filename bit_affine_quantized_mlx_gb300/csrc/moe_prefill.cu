@@ -45,8 +45,6 @@ constexpr int kGemmThreads = 512;
 constexpr int kMmaWarp = 4;
 constexpr int kBWarp0 = 5, kBThreads = 96;
 constexpr int kAWarp0 = 8, kAThreads = 256;
-constexpr int kRing = 4;       // raw-code ring depth (k-blocks)
-constexpr int kScSlots = 4;    // scale-block slots
 constexpr long long kWaitCycles = 4000000000LL;  // ~2 s at GB300 clocks
 constexpr int kHdrItemsGU = 8, kHdrItemsDN = 9;
 
@@ -58,19 +56,17 @@ enum { kRouter = 0, kGateUp = 1, kDown = 2 };
 
 template <int MODE>
 struct Cfg {
-  static constexpr int NA = MODE == kGateUp ? 2 : 1;  // A tiles per stage
-  static constexpr int S = MODE == kGateUp ? 3 : 4;   // operand stages
+  static constexpr int NA = MODE == kGateUp ? 2 : 1;  // A tiles per k-block
+  static constexpr int SA = MODE == kGateUp ? 3 : 4;  // A (weight) stages
+  static constexpr int SB = 6;                        // B (token) stages
   static constexpr int A_BYTES = kBM * 128;
   static constexpr int B_BYTES = kBN * 128;
-  static constexpr int STAGE = NA * A_BYTES + B_BYTES;
-  static constexpr int RAW_SLOT = NA * kBM * 32;
-  static constexpr int SC_SLOT = 2 * 2 * kBM * 16;  // [copy][s|b][row][8 groups]
+  static constexpr int A_STAGE = NA * A_BYTES;
   static constexpr int ACC_COLS = NA * kBN;
   static constexpr int TMEM_COLS = 2 * ACC_COLS;  // double buffer
-  static constexpr int OFF_RAW = S * STAGE;
-  static constexpr int OFF_SC = OFF_RAW + (MODE == kRouter ? 0 : kRing * RAW_SLOT);
-  static constexpr int OFF_BAR = OFF_SC + (MODE == kRouter ? 0 : kScSlots * SC_SLOT);
-  static constexpr int NBARS = 2 * S + 4 + 1;
+  static constexpr int OFF_B = SA * A_STAGE;
+  static constexpr int OFF_BAR = OFF_B + SB * B_BYTES;
+  static constexpr int NBARS = 2 * SA + 2 * SB + 5;
   static constexpr int BYTES = OFF_BAR + NBARS * 8 + 1024;
 };
 
@@ -95,12 +91,15 @@ struct GemmArgs {
   int32_t *hdr;
 };
 
+// Bounded wait on an mbarrier phase.  sleep_ns > 0 lets a waiting thread off the critical
+// path be suspended instead of spinning (its issue slots go to the producers).
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int *abort_flag,
-                                         int32_t *err) {
+                                         int32_t *err, uint32_t sleep_ns = 0) {
   if (tc::mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   while (true) {
-    if (tc::mbar_try_wait(bar, parity)) return true;
+    if (sleep_ns ? tc::mbar_try_wait_sleep(bar, parity, sleep_ns) : tc::mbar_try_wait(bar, parity))
+      return true;
     if (*abort_flag) return false;
     if (clock64() - t0 > kWaitCycles) {
       *abort_flag = 1;
@@ -110,14 +109,18 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
   }
 }
 
+constexpr int kSmemItems = 256;  // work items of one block staged in shared memory
+
+// Work item it of this block (it = blockIdx.x + i * gridDim.x).
 template <int MODE>
-__device__ __forceinline__ int4 get_item(const GemmArgs &a, int i) {
+__device__ __forceinline__ int4 get_item(const GemmArgs &a, int it, const int4 *s_items) {
   if (MODE == kRouter) {  // (k split, first token, tokens, m-tile)
-    const int mt = i % a.mt_static, rest = i / a.mt_static;
+    const int mt = it % a.mt_static, rest = it / a.mt_static;
     const int split = rest % a.ksplit, t0 = (rest / a.ksplit) * kBN;
     return make_int4(split, t0, min(kBN, a.T - t0), mt);
   }
-  return a.items[i];
+  const int i = (it - (int)blockIdx.x) / (int)gridDim.x;
+  return i < kSmemItems ? s_items[i] : a.items[it];
 }
 
 // Position of element r inside its 8-chunk in the permuted K order (0,4,1,5,2,6,3,7).
@@ -125,47 +128,85 @@ __device__ __forceinline__ int kpos(int r) {
   return (r & ~7) | ((r & 3) * 2 + ((r >> 2) & 1));
 }
 
-// Dequantise 4 code words (32 codes) of one row into 4 16-byte chunks of bf16, each
-// chunk holding (q_j, q_j+4) pairs in the permuted K order.
-__device__ __forceinline__ uint4 dequant_word(uint32_t w, __nv_bfloat162 s2, __nv_bfloat162 b2) {
-  uint32_t out[4];
-  const __nv_bfloat162 c128 = __floats2bfloat162_rn(128.f, 128.f);
+// Dequantise one code word (8 codes) of one row into one 16-byte chunk of bf16 holding the
+// pairs (q_j, q_j+4) -- the permuted K order.  s*q + b is formed with two bf16x2 FMAs:
+// (128 + q) - 128 is exact, then s*q + b rounds once.
+__device__ __forceinline__ uint4 dequant_word(uint32_t w, uint32_t s2, uint32_t b2) {
+  uint32_t ws[4], out[4];
+  ws[0] = w;
+  asm("shr.b32 %0, %1, 4;" : "=r"(ws[1]) : "r"(w));
+  asm("shr.b32 %0, %1, 8;" : "=r"(ws[2]) : "r"(w));
+  asm("shr.b32 %0, %1, 12;" : "=r"(ws[3]) : "r"(w));
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
-    uint32_t v = ((w >> (4 * j)) & 0x000F000Fu) | 0x43004300u;
-    __nv_bfloat162 q = *reinterpret_cast<__nv_bfloat162 *>(&v);
-    q = __hsub2(q, c128);              // exact: small integers
-    __nv_bfloat162 d = __hfma2(q, s2, b2);  // s*q + b, one rounding to bf16
-    out[j] = *reinterpret_cast<uint32_t *>(&d);
+    uint32_t v, q;  // q = v * 1 - 128
+    asm("lop3.b32 %0, %1, 0x000F000F, 0x43004300, 0xEA;" : "=r"(v) : "r"(ws[j]));
+    asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(q) : "r"(v), "r"(0x3F803F80u), "r"(0xC300C300u));
+    asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(out[j]) : "r"(q), "r"(s2), "r"(b2));
   }
   return make_uint4(out[0], out[1], out[2], out[3]);
 }
 
-template <int MODE>
+// KG k-blocks of per-group scales (or biases) of one row: 2*KG bytes.
+template <int KG>
+struct ScaleVec {
+  uint32_t v[KG / 2];
+  __device__ __forceinline__ void load(const uint16_t *p) {
+    if constexpr (KG == 8) {
+      const uint4 u = __ldg(reinterpret_cast<const uint4 *>(p));
+      v[0] = u.x; v[1] = u.y; v[2] = u.z; v[3] = u.w;
+    } else if constexpr (KG == 4) {
+      const uint2 u = __ldg(reinterpret_cast<const uint2 *>(p));
+      v[0] = u.x; v[1] = u.y;
+    } else {
+      v[0] = __ldg(reinterpret_cast<const uint32_t *>(p));
+    }
+  }
+  // bf16 i broadcast to both halves
+  __device__ __forceinline__ uint32_t pair(int i) const {
+    const uint32_t h = (i & 1) ? (v[i >> 1] >> 16) : (v[i >> 1] & 0xFFFFu);
+    return h | (h << 16);
+  }
+};
+
+template <int MODE, int KG>
 __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const GemmArgs a) {
   using C = Cfg<MODE>;
   extern __shared__ uint8_t smem_dyn[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(((uintptr_t)smem_dyn + 1023) & ~(uintptr_t)1023);
   const uint32_t sbase = tc::smem_u32(smem);
   const uint32_t bar0 = sbase + C::OFF_BAR;
-  auto full_bar = [&](int s) { return bar0 + 8u * s; };
-  auto empty_bar = [&](int s) { return bar0 + 8u * (C::S + s); };
-  auto accf_bar = [&](int b) { return bar0 + 8u * (2 * C::S + b); };
-  auto acce_bar = [&](int b) { return bar0 + 8u * (2 * C::S + 2 + b); };
-  const uint32_t done_bar = bar0 + 8u * (2 * C::S + 4);
+  auto afull = [&](int s) { return bar0 + 8u * s; };
+  auto aempty = [&](int s) { return bar0 + 8u * (C::SA + s); };
+  auto bfull = [&](int s) { return bar0 + 8u * (2 * C::SA + s); };
+  auto bempty = [&](int s) { return bar0 + 8u * (2 * C::SA + C::SB + s); };
+  auto accf_bar = [&](int b) { return bar0 + 8u * (2 * C::SA + 2 * C::SB + b); };
+  auto acce_bar = [&](int b) { return bar0 + 8u * (2 * C::SA + 2 * C::SB + 2 + b); };
+  const uint32_t done_bar = bar0 + 8u * (2 * C::SA + 2 * C::SB + 4);
 
   __shared__ uint32_t s_taddr;
   __shared__ volatile int s_abort;
+  __shared__ int4 s_items[MODE == kRouter ? 1 : kSmemItems];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n_items = MODE == kRouter ? a.n_items_static : *(volatile const int32_t *)a.n_items_ptr;
+  if (MODE != kRouter) {
+    for (int i = threadIdx.x; i < kSmemItems; i += kGemmThreads) {
+      const int it = (int)blockIdx.x + i * (int)gridDim.x;
+      if (it < n_items) s_items[i] = a.items[it];
+    }
+  }
   const int G = a.K / 64;  // groups per row
   const int nkb = MODE == kRouter ? G / a.ksplit : G;  // k-blocks per item
 
   if (threadIdx.x == 0) {
     s_abort = 0;
-    for (int s = 0; s < C::S; ++s) {
-      tc::mbar_init(full_bar(s), kAThreads + kBThreads);
-      tc::mbar_init(empty_bar(s), 1);
+    for (int s = 0; s < C::SA; ++s) {
+      tc::mbar_init(afull(s), kAThreads);
+      tc::mbar_init(aempty(s), 1);
+    }
+    for (int s = 0; s < C::SB; ++s) {
+      tc::mbar_init(bfull(s), kBThreads);
+      tc::mbar_init(bempty(s), 1);
     }
     for (int b = 0; b < 2; ++b) {
       tc::mbar_init(accf_bar(b), 1);
@@ -189,7 +230,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const Gem
     const int r = warp * 32 + lane;
     int j = 0;
     for (int it = blockIdx.x; it < n_items; it += gridDim.x, ++j) {
-      const int4 item = get_item<MODE>(a, it);
+      const int4 item = get_item<MODE>(a, it, s_items);
       const int b = j & 1;
       if (!wait_bar(accf_bar(b), (j >> 1) & 1, &s_abort, err)) break;
       tc::tc_fence_after();
@@ -233,26 +274,26 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const Gem
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------------ MMA issue
     if (lane == 0) {
-      int st = 0, j = 0;
+      int sa = 0, sb = 0, j = 0;
+      uint32_t pa = 0, pb = 0;
       bool ok = true;
       for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x, ++j) {
-        const int4 item = get_item<MODE>(a, it);
+        const int4 item = get_item<MODE>(a, it, s_items);
         const int b = j & 1;
         if (!wait_bar(acce_bar(b), ((j >> 1) & 1) ^ 1, &s_abort, err)) break;
         tc::tc_fence_after();
         const int npad = (item.z + 15) & ~15;
         const uint32_t idesc = tc::idesc_bf16_f32(kBM, npad);
         const uint32_t d0 = taddr + (uint32_t)(b * C::ACC_COLS);
-        for (int kb = 0; kb < nkb; ++kb, ++st) {
-          const int s = st % C::S;
-          if (!wait_bar(full_bar(s), (st / C::S) & 1, &s_abort, err)) {
+        for (int kb = 0; kb < nkb; ++kb) {
+          if (!wait_bar(afull(sa), pa, &s_abort, err) || !wait_bar(bfull(sb), pb, &s_abort, err)) {
             ok = false;
             break;
           }
           tc::fence_proxy_async();
           tc::tc_fence_after();
-          const uint32_t sA = sbase + s * C::STAGE;
-          const uint32_t sB = sA + C::NA * C::A_BYTES;
+          const uint32_t sA = sbase + sa * C::A_STAGE;
+          const uint32_t sB = sbase + C::OFF_B + sb * C::B_BYTES;
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
             const uint64_t bd = tc::desc_k128_sw128(sB + 32 * kk);
@@ -262,7 +303,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const Gem
               tc::mma_bf16(d0 + kBN, tc::desc_k128_sw128(sA + C::A_BYTES + 32 * kk), bd, idesc,
                            acc);
           }
-          tc::mma_commit(empty_bar(s));
+          tc::mma_commit(aempty(sa));
+          tc::mma_commit(bempty(sb));
+          if (++sa == C::SA) { sa = 0; pa ^= 1; }
+          if (++sb == C::SB) { sb = 0; pb ^= 1; }
         }
         if (!ok) break;
         tc::mma_commit(accf_bar(b));
@@ -276,11 +320,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const Gem
     // ------------------------------------------------------------------ token-row gather
     constexpr int QB = (kBN * 8 + kBThreads - 1) / kBThreads;  // 16-byte chunks per thread
     const int tb = threadIdx.x - kBWarp0 * 32;
-    int stage = 0;
-    uint32_t phase = 0;
+    int sb = 0;
+    uint32_t pb = 0;
     bool ok = true;
     for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
-      const int4 item = get_item<MODE>(a, it);
+      const int4 item = get_item<MODE>(a, it, s_items);
       const int ntok = item.z, nchunk = ((ntok + 15) & ~15) * 8;
       const int kb0 = MODE == kRouter ? item.x * nkb : 0;
       const uint16_t *srcp[QB];
@@ -299,20 +343,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const Gem
         dsto[i] = tc::sw128((uint32_t)n, (uint32_t)c);
       }
       for (int kb = 0; kb < nkb; ++kb) {
-        if (!wait_bar(empty_bar(stage), phase ^ 1, &s_abort, err)) {
+        if (!wait_bar(bempty(sb), pb ^ 1, &s_abort, err)) {
           ok = false;
           break;
         }
-        const uint32_t sB = sbase + stage * C::STAGE + C::NA * C::A_BYTES;
+        const uint32_t sB = sbase + C::OFF_B + sb * C::B_BYTES;
 #pragma unroll
         for (int i = 0; i < QB; ++i)
           if (tb + i * kBThreads < nchunk)
             tc::cp_async16(sB + dsto[i], srcp[i] + (nbytes[i] ? kb * 64 : 0), nbytes[i]);
-        tc::cp_async_arrive_noinc(full_bar(stage));
-        if (++stage == C::S) {
-          stage = 0;
-          phase ^= 1;
-        }
+        tc::cp_async_arrive_noinc(bfull(sb));
+        if (++sb == C::SB) { sb = 0; pb ^= 1; }
       }
     }
     tc::cp_async_wait_all();
@@ -320,22 +361,22 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const Gem
     // ------------------------------------------------------------------ weight producers
     const int ta = threadIdx.x - kAWarp0 * 32;  // 0..255
     const int row = ta & (kBM - 1);
-    const int half = ta >> 7;                   // GateUp: matrix; Down/Router: which half row
+    const int half = ta >> 7;                   // GateUp: matrix; Down/Router: half of the row
     const int mat = C::NA == 2 ? half : 0;
+    int sa = 0;
+    uint32_t pa = 0;
     bool ok = true;
     if (MODE == kRouter) {
-      int st = 0;
       for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
-        const int4 item = get_item<MODE>(a, it);
+        const int4 item = get_item<MODE>(a, it, s_items);
         const int m = item.w * kBM + row;
         const bool valid = m < a.a_rows;
-        for (int kb = 0; kb < nkb; ++kb, ++st) {
-          const int s = st % C::S;
-          if (!wait_bar(empty_bar(s), ((st / C::S) & 1) ^ 1, &s_abort, err)) {
+        for (int kb = 0; kb < nkb; ++kb) {
+          if (!wait_bar(aempty(sa), pa ^ 1, &s_abort, err)) {
             ok = false;
             break;
           }
-          const uint32_t sA = sbase + s * C::STAGE;
+          const uint32_t sA = sbase + sa * C::A_STAGE;
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
             const int c = 4 * half + i;
@@ -343,124 +384,108 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const Gem
                 valid ? a.a_bf16 + (size_t)m * a.K + (item.x * nkb + kb) * 64 + 8 * c : a.a_bf16;
             tc::cp_async16(sA + tc::sw128(row, c), src, valid ? 16u : 0u);
           }
-          tc::cp_async_arrive_noinc(full_bar(s));
+          tc::cp_async_arrive_noinc(afull(sa));
+          if (++sa == C::SA) { sa = 0; pa ^= 1; }
         }
       }
       tc::cp_async_wait_all();
     } else {
-      // Continuous k-block stream over this CTA's items; the issue side runs kRing-1
-      // k-blocks ahead of the consume side.  Per-item pointers are computed once per item.
-      constexpr int WPT = C::NA == 2 ? 8 : 4;  // code words per thread per k-block
+      // Codes of the next group of KG k-blocks are loaded into registers while the current
+      // group is dequantised (prefetch distance KG k-blocks); per-item addressing is done
+      // once per item.
+      constexpr int NV = C::NA == 2 ? 2 : 1;  // 16-byte code vectors per thread per k-block
       const int woff = C::NA == 2 ? 0 : 4 * half;
-      const uint32_t raw_off = (uint32_t)((mat * kBM + row) * 32 + woff * 4);
-      const uint32_t raw0 = sbase + C::OFF_RAW + raw_off;
-      const uint32_t sc0 = sbase + C::OFF_SC + (uint32_t)(((half * 2) * kBM + row) * 16);
-      const uint8_t *raw_p = smem + C::OFF_RAW + raw_off;
-      const uint8_t *sc_p = smem + C::OFF_SC + ((half * 2) * kBM + row) * 16;
       const uint32_t a_row_off = (uint32_t)(mat * C::A_BYTES + row * 128);
       const uint32_t rsw = (uint32_t)(row & 7);
-      // issue iterator
-      int i_it = blockIdx.x, i_kb = 0;
-      uint32_t i_g = 0, i_sg = 0;
-      bool i_valid = false;
-      const uint32_t *i_w = nullptr;
-      const uint16_t *i_s = nullptr, *i_b = nullptr;
-      auto issue_item = [&]() {
-        i_valid = false;
-        if (i_it < n_items) {
-          const int4 item = a.items[i_it];
-          const int e = item.x, m = item.w * kBM + row;
-          if (m < a.a_rows) {
-            const bool sh = (e == a.E);
-            const lily_q4_mat &W = sh ? (mat ? a.sh1 : a.sh0) : (mat ? a.a1 : a.a0);
-            const size_t r = (sh ? 0 : (size_t)e * a.a_rows) + (size_t)m;
-            i_w = W.w + r * (size_t)(a.K / 8) + woff;
-            i_s = W.s + r * (size_t)G;
-            i_b = W.b + r * (size_t)G;
-            i_valid = true;
-          }
-        }
+      const int ngrp = nkb / KG;
+      struct Src {
+        const uint32_t *w;
+        const uint16_t *s, *b;
+        bool valid;
       };
-      issue_item();
-      auto issue = [&]() {
-        if (i_it < n_items) {
-          if (i_valid) {
-            const uint32_t dst = raw0 + (i_g & (kRing - 1)) * C::RAW_SLOT;
-            const uint32_t *src = i_w + i_kb * 8;
-            tc::cp_async16(dst, src, 16);
-            if (WPT == 8) tc::cp_async16(dst + 16, src + 4, 16);
-            if ((i_kb & 7) == 0) {
-              // scale block: s and b of k-blocks i_kb .. i_kb+7 (fewer when G < 8)
-              const int nb = min(8, G - i_kb);
-              const uint32_t sdst = sc0 + (i_sg & (kScSlots - 1)) * C::SC_SLOT;
-              if (nb == 8) {
-                tc::cp_async16(sdst, i_s + i_kb, 16);
-                tc::cp_async16(sdst + kBM * 16, i_b + i_kb, 16);
-              } else if (nb == 4) {
-                tc::cp_async8(sdst, i_s + i_kb);
-                tc::cp_async8(sdst + kBM * 16, i_b + i_kb);
-              } else {
-                tc::cp_async4(sdst, i_s + i_kb);
-                tc::cp_async4(sdst + kBM * 16, i_b + i_kb);
-              }
-            }
-          }
-          if ((i_kb & 7) == 0) ++i_sg;
-          ++i_g;
-          if (++i_kb == nkb) {
-            i_kb = 0;
-            i_it += gridDim.x;
-            issue_item();
-          }
+      auto item_src = [&](int it) {
+        Src r{nullptr, nullptr, nullptr, false};
+        const int4 item = get_item<MODE>(a, it, s_items);
+        const int e = item.x, m = item.w * kBM + row;
+        if (m < a.a_rows) {
+          const bool sh = (e == a.E);
+          const lily_q4_mat &W = sh ? (mat ? a.sh1 : a.sh0) : (mat ? a.a1 : a.a0);
+          const size_t rr = (sh ? 0 : (size_t)e * a.a_rows) + (size_t)m;
+          r.w = W.w + rr * (size_t)(a.K / 8) + woff;
+          r.s = W.s + rr * (size_t)G;
+          r.b = W.b + rr * (size_t)G;
+          r.valid = true;
         }
-        tc::cp_async_commit();
+        return r;
       };
-      for (int p = 0; p < kRing - 1; ++p) issue();
-      int stage = 0;
-      uint32_t phase = 0, c_g = 0, c_sg = 0xFFFFFFFFu;
-      for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
-        const int4 item = a.items[it];
-        const bool valid = item.w * kBM + row < a.a_rows;
-        for (int kb = 0; kb < nkb; ++kb, ++c_g) {
-          if ((kb & 7) == 0) ++c_sg;
-          issue();
-          tc::cp_async_wait<kRing - 1>();
-          uint4 outv[WPT];
-          if (valid) {
-            const uint8_t *rp = raw_p + (c_g & (kRing - 1)) * C::RAW_SLOT;
-            const uint4 w0 = *reinterpret_cast<const uint4 *>(rp);
-            uint4 w1 = make_uint4(0, 0, 0, 0);
-            if (WPT == 8) w1 = *reinterpret_cast<const uint4 *>(rp + 16);
-            const uint8_t *sp = sc_p + (c_sg & (kScSlots - 1)) * C::SC_SLOT + 2 * (kb & 7);
-            const uint32_t sbits = *reinterpret_cast<const uint16_t *>(sp);
-            const uint32_t bbits = *reinterpret_cast<const uint16_t *>(sp + kBM * 16);
-            uint32_t s2u = sbits | (sbits << 16), b2u = bbits | (bbits << 16);
-            const __nv_bfloat162 s2 = *reinterpret_cast<__nv_bfloat162 *>(&s2u);
-            const __nv_bfloat162 b2 = *reinterpret_cast<__nv_bfloat162 *>(&b2u);
-            const uint32_t ws[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+      uint4 raw[KG][NV];
+      ScaleVec<KG> sc, bc, scn, bcn;
+      int c_it = blockIdx.x, c_grp = 0;
+      Src cur{nullptr, nullptr, nullptr, false};
+      if (c_it < n_items) {
+        cur = item_src(c_it);
+        if (cur.valid) {
 #pragma unroll
-            for (int q = 0; q < WPT; ++q) outv[q] = dequant_word(ws[q], s2, b2);
+          for (int i = 0; i < KG; ++i)
+#pragma unroll
+            for (int v = 0; v < NV; ++v) raw[i][v] = ld_stream(cur.w + i * 8 + 4 * v);
+          sc.load(cur.s);
+          bc.load(cur.b);
+        }
+      }
+      while (c_it < n_items && ok) {
+        // next group
+        int n_it = c_it, n_grp = c_grp + 1;
+        Src nxt = cur;
+        if (n_grp == ngrp) {
+          n_grp = 0;
+          n_it += gridDim.x;
+          if (n_it < n_items) nxt = item_src(n_it);
+        }
+        const bool have_next = n_it < n_items && nxt.valid;
+        if (have_next) {
+          scn.load(nxt.s + n_grp * KG);
+          bcn.load(nxt.b + n_grp * KG);
+        }
+#pragma unroll
+        for (int i = 0; i < KG; ++i) {
+          uint4 outv[NV * 4];
+          if (cur.valid) {
+            const uint32_t s2 = sc.pair(i), b2 = bc.pair(i);
+#pragma unroll
+            for (int v = 0; v < NV; ++v) {
+              outv[4 * v + 0] = dequant_word(raw[i][v].x, s2, b2);
+              outv[4 * v + 1] = dequant_word(raw[i][v].y, s2, b2);
+              outv[4 * v + 2] = dequant_word(raw[i][v].z, s2, b2);
+              outv[4 * v + 3] = dequant_word(raw[i][v].w, s2, b2);
+            }
           } else {
 #pragma unroll
-            for (int q = 0; q < WPT; ++q) outv[q] = make_uint4(0, 0, 0, 0);
+            for (int q = 0; q < NV * 4; ++q) outv[q] = make_uint4(0, 0, 0, 0);
           }
-          if (!wait_bar(empty_bar(stage), phase ^ 1, &s_abort, err)) {
+          if (have_next) {
+#pragma unroll
+            for (int v = 0; v < NV; ++v)
+              raw[i][v] = ld_stream(nxt.w + (n_grp * KG + i) * 8 + 4 * v);
+          }
+          if (!wait_bar(aempty(sa), pa ^ 1, &s_abort, err)) {
             ok = false;
             break;
           }
-          uint8_t *sA = smem + stage * C::STAGE + a_row_off;
+          uint8_t *sA = smem + sa * C::A_STAGE + a_row_off;
 #pragma unroll
-          for (int q = 0; q < WPT; ++q)
+          for (int q = 0; q < NV * 4; ++q)
             *reinterpret_cast<uint4 *>(sA + ((((uint32_t)(woff + q)) ^ rsw) << 4)) = outv[q];
           tc::fence_proxy_async();
-          tc::mbar_arrive(full_bar(stage));
-          if (++stage == C::S) {
-            stage = 0;
-            phase ^= 1;
-          }
+          tc::mbar_arrive(afull(sa));
+          if (++sa == C::SA) { sa = 0; pa ^= 1; }
         }
+        c_it = n_it;
+        c_grp = n_grp;
+        cur = nxt;
+        sc = scn;
+        bc = bcn;
       }
-      tc::cp_async_wait_all();
     }
   }
 
@@ -777,18 +802,27 @@ PrefillWsLayout prefill_ws_layout(const lily_q4_moe_layer &L, int T) {
   return l;
 }
 
+template <int MODE, int KG>
+static int launch_gemm_kg(const GemmArgs &a, int grid, cudaStream_t st) {
+  const int bytes = Cfg<MODE>::BYTES;
+  static bool attr_set = false;  // per instantiation
+  if (!attr_set) {
+    if (cudaFuncSetAttribute(grouped_gemm_kernel<MODE, KG>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess)
+      return LILY_Q4_ERR_CUDA;
+    attr_set = true;
+  }
+  grouped_gemm_kernel<MODE, KG><<<grid, kGemmThreads, bytes, st>>>(a);
+  return check_launch();
+}
+
+// KG = k-blocks per register group of the weight producers: min(8, K/64).
 template <int MODE>
 static int launch_gemm(const GemmArgs &a, int grid, cudaStream_t st) {
-  const int bytes = Cfg<MODE>::BYTES;
-  static bool attr_set[3] = {false, false, false};
-  if (!attr_set[MODE]) {
-    if (cudaFuncSetAttribute(grouped_gemm_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             bytes) != cudaSuccess)
-      return LILY_Q4_ERR_CUDA;
-    attr_set[MODE] = true;
-  }
-  grouped_gemm_kernel<MODE><<<grid, kGemmThreads, bytes, st>>>(a);
-  return check_launch();
+  const int G = a.K / 64;
+  if (MODE == kRouter || G >= 8) return launch_gemm_kg<MODE, 8>(a, grid, st);
+  if (G == 4) return launch_gemm_kg<MODE, 4>(a, grid, st);
+  return launch_gemm_kg<MODE, 2>(a, grid, st);
 }
 
 int launch_moe_prefill(const lily_q4_moe_layer &L, const uint16_t *x, int T, uint16_t *y,

@@ -123,6 +123,71 @@ __device__ __forceinline__ float q4_group_raw(const uint4 w0, const uint4 w1, co
   return (a0 + a2) + (a1 + a3);
 }
 
+// bf16 activations: one lane's 64 x values kept as the bf16 pairs (x_j, x_j+4) matching the
+// code pairs an unpack produces, plus their sum.  Half the registers of XGroup.
+struct XGroupB {
+  uint32_t xp[32];  // [4*m + j] = x[8m+j] | x[8m+j+4] << 16 (bf16 bits)
+  float X128;       // 128 * sum of the 64 x values
+  float X;          // sum of the 64 x values
+};
+
+// 64 bf16 values (8 x 16-byte chunks in K order) -> XGroupB.
+__device__ __forceinline__ void xgroupb_from_bf16(XGroupB &g, const uint4 *chunks) {
+  float sum = 0.f;
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    const uint32_t w[4] = {chunks[c].x, chunks[c].y, chunks[c].z, chunks[c].w};
+    // w[i] holds x[8c+2i] (low) and x[8c+2i+1] (high)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const uint32_t lo = (j & 1) ? (w[j >> 1] >> 16) : (w[j >> 1] & 0xFFFFu);          // x[8c+j]
+      const uint32_t hi = (j & 1) ? (w[2 + (j >> 1)] >> 16) : (w[2 + (j >> 1)] & 0xFFFFu);  // x[8c+j+4]
+      g.xp[4 * c + j] = lo | (hi << 16);
+      sum += __uint_as_float(lo << 16) + __uint_as_float(hi << 16);
+    }
+  }
+  g.X = sum;
+  g.X128 = 128.0f * sum;
+}
+
+// sum_k (128 + q_k) x_k for one group: each bf16 pair (128 + q_j, 128 + q_j+4) from the
+// unpack multiplies the matching bf16 x pair in mixed-precision FMAs (bf16 operands, fp32
+// accumulation; the products are exact).  Per word: three shifts, four LOP3, eight FMAs.
+__device__ __forceinline__ float q4_group_raw_b(const uint4 w0, const uint4 w1, const XGroupB &g) {
+  const uint32_t w[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+  float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+#pragma unroll
+  for (int m = 0; m < 8; ++m) {
+    uint32_t ws[4];
+    ws[0] = w[m];
+    asm("shr.b32 %0, %1, 4;" : "=r"(ws[1]) : "r"(w[m]));
+    asm("shr.b32 %0, %1, 8;" : "=r"(ws[2]) : "r"(w[m]));
+    asm("shr.b32 %0, %1, 12;" : "=r"(ws[3]) : "r"(w[m]));
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      uint32_t v;
+      asm("lop3.b32 %0, %1, 0x000F000F, 0x43004300, 0xEA;" : "=r"(v) : "r"(ws[j]));
+      if (j & 1)
+        asm("{\n.reg .b16 vl, vh, xl, xh;\nmov.b32 {vl, vh}, %2;\nmov.b32 {xl, xh}, %3;\n"
+            "fma.rn.f32.bf16 %0, vl, xl, %0;\nfma.rn.f32.bf16 %1, vh, xh, %1;\n}"
+            : "+f"(a0), "+f"(a1)
+            : "r"(v), "r"(g.xp[4 * m + j]));
+      else
+        asm("{\n.reg .b16 vl, vh, xl, xh;\nmov.b32 {vl, vh}, %2;\nmov.b32 {xl, xh}, %3;\n"
+            "fma.rn.f32.bf16 %0, vl, xl, %0;\nfma.rn.f32.bf16 %1, vh, xh, %1;\n}"
+            : "+f"(a2), "+f"(a3)
+            : "r"(v), "r"(g.xp[4 * m + j]));
+    }
+  }
+  return (a0 + a2) + (a1 + a3);
+}
+
+// s*(sum q x) + b*(sum x) for bf16 x.
+__device__ __forceinline__ float q4_group_dot_b(const uint4 w0, const uint4 w1, const XGroupB &g,
+                                                float s, float b) {
+  return fmaf(s, q4_group_raw_b(w0, w1, g) - g.X128, b * g.X);
+}
+
 // Dot product of one dequantised 64-group with the prepared x: s*(sum q x) + b*(sum x).
 __device__ __forceinline__ float q4_group_dot(const uint4 w0, const uint4 w1, const XGroup &g,
                                               float s, float b) {
