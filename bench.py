@@ -31,6 +31,10 @@ sys.path.insert(0, ROOT)
 METRIC = "Q4 MoE decode tok/s per layer & HBM GB/s vs peak; prefill chunk TFLOP/s"
 UNIT = "tok/s per layer"
 EXPERT_BYTES = 1769472  # gate + up + down of one expert at H=2048, I=512 (codes + s + b)
+# DRAM bytes (read + write) of one single-launch decode-layer kernel at batch 1, from the ncu
+# capture summarised in profiles/moe_decode_fused_decode-layer_H2048_E256_k8.md.  Set to None
+# whenever that kernel changes until it is captured again.
+DECODE_TRAFFIC_BYTES = 17073664
 
 
 def peaks():
@@ -321,7 +325,7 @@ def run_gb300(args):
         "roofline": {"bound": "hbm", "kernel": "lily_q4_moe_decode (router+top-k, gate/up, down)",
                      "achieved": round(dec_gbs, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
                      "frac": round(dec_gbs / pk["hbm_gbs"], 4), "peak_source": pk["source"],
-                     "traffic": None},
+                     "traffic": DECODE_TRAFFIC_BYTES if T == 1 else None},
         "e2e": {"value": e2e_val, "unit": UNIT,
                 "h2d_bytes_per_step": nl * T * wl.H * 2, "d2h_bytes_per_step": nl * T * wl.H * 2,
                 "scope": "decode layers through lily_q4_moe_decode with pinned host x/y copies"},
