@@ -18,7 +18,7 @@ namespace lq4 {
 
 constexpr int kLmThreads = 256;
 constexpr int kLmWarps = kLmThreads / 32;
-constexpr int kLmBlocksPerSm = 1;
+constexpr int kLmBlocksPerSm = 2;
 
 LmWsLayout lm_ws_layout(int N, int K) {
   (void)K;
@@ -62,7 +62,7 @@ __global__ void __launch_bounds__(kLmThreads, kLmBlocksPerSm)
     xgroupb_from_bf16(xg, c);
   }
 
-  float best_v = -FLT_MAX;
+  float best_v = -INFINITY;
   int best_i = INT_MAX;
   const int gwarp = blockIdx.x * kLmWarps + warp;
   const int nwarps = gridDim.x * kLmWarps;
@@ -88,27 +88,20 @@ __global__ void __launch_bounds__(kLmThreads, kLmBlocksPerSm)
     }
 #pragma unroll
     for (int u = 0; u < U; ++u) {
-      float d = seg_sum<G>(q4_group_dot_b(wa[u], wb[u], xg, sv[u], bv[u]));
+      const float d = seg_sum<G>(q4_group_dot_b(wa[u], wb[u], xg, sv[u], bv[u]));
+      const float dc = cand(d);
       const int row = r0 + u * RPS + rsub;
       if (g == 0 && row < N) {
         if (logits) logits[row] = d;
-        if (better(d, row, best_v, best_i)) {
-          best_v = d;
+        if (better(dc, row, best_v, best_i)) {
+          best_v = dc;
           best_i = row;
         }
       }
     }
   }
   // warp argmax
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    float ov = __shfl_xor_sync(0xffffffffu, best_v, o);
-    int oi = __shfl_xor_sync(0xffffffffu, best_i, o);
-    if (better(ov, oi, best_v, best_i)) {
-      best_v = ov;
-      best_i = oi;
-    }
-  }
+  warp_argmax(best_v, best_i);
   __shared__ float sv_[kLmWarps];
   __shared__ int si_[kLmWarps];
   __shared__ int is_last;
@@ -135,7 +128,7 @@ __global__ void __launch_bounds__(kLmThreads, kLmBlocksPerSm)
   if (!is_last) return;
   __threadfence();
   // last block: reduce the per-block pairs
-  float v = -FLT_MAX;
+  float v = -INFINITY;
   int i = INT_MAX;
   for (int j = threadIdx.x; j < (int)gridDim.x; j += kLmThreads) {
     const float pv = __ldcg(part_v + j);
@@ -145,15 +138,7 @@ __global__ void __launch_bounds__(kLmThreads, kLmBlocksPerSm)
       i = pi;
     }
   }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    float ov = __shfl_xor_sync(0xffffffffu, v, o);
-    int oi = __shfl_xor_sync(0xffffffffu, i, o);
-    if (better(ov, oi, v, i)) {
-      v = ov;
-      i = oi;
-    }
-  }
+  warp_argmax(v, i);
   if (lane == 0) {
     sv_[warp] = v;
     si_[warp] = i;

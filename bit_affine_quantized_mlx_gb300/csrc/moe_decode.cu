@@ -135,12 +135,12 @@ __device__ void route_block(const float *logits, const float *sigma, int T, int 
     const float *lg = logits + (size_t)t * E;
     float lv[EC];
 #pragma unroll
-    for (int j = 0; j < EC; ++j) lv[j] = (lane + 32 * j < E) ? __ldcg(lg + lane + 32 * j) : -FLT_MAX;
+    for (int j = 0; j < EC; ++j) lv[j] = (lane + 32 * j < E) ? cand(__ldcg(lg + lane + 32 * j)) : -INFINITY;
     uint32_t taken = 0;  // bit j: expert lane + 32 j already selected
     float sel_v[kMaxK];
     int sel_e[kMaxK];
     for (int i = 0; i < k; ++i) {
-      float bv = -FLT_MAX;
+      float bv = -INFINITY;
       int be = INT_MAX;
 #pragma unroll
       for (int j = 0; j < EC; ++j) {
@@ -150,15 +150,7 @@ __device__ void route_block(const float *logits, const float *sigma, int T, int 
           be = e;
         }
       }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-        const int oe = __shfl_xor_sync(0xffffffffu, be, o);
-        if (better(ov, oe, bv, be)) {
-          bv = ov;
-          be = oe;
-        }
-      }
+      warp_argmax(bv, be);
       if ((be & 31) == lane) taken |= 1u << (be >> 5);
       sel_v[i] = bv;
       sel_e[i] = be;
@@ -470,7 +462,7 @@ __global__ void __launch_bounds__(kDownThreads)
 //            for all of the block's row-steps at once; partials meet in shared memory and
 //            are summed per token in a fixed order (deterministic)
 // ---------------------------------------------------------------------------------------
-constexpr int kFusedThreads = 384;
+constexpr int kFusedThreads = 448;
 constexpr int kFusedWarps = kFusedThreads / 32;
 constexpr size_t kFusedSmemMax = 100 * 1024;
 constexpr int kFusedMaxT = 4;
@@ -573,12 +565,12 @@ __device__ void route_small(const float *logits, const float *sigma, int T, int 
     const float *lg = logits + (size_t)t * E;
     float lv[EC];
 #pragma unroll
-    for (int j = 0; j < EC; ++j) lv[j] = (lane + 32 * j < E) ? __ldcg(lg + lane + 32 * j) : -FLT_MAX;
+    for (int j = 0; j < EC; ++j) lv[j] = (lane + 32 * j < E) ? cand(__ldcg(lg + lane + 32 * j)) : -INFINITY;
     uint32_t taken = 0;
     float v0 = 0.f, denom = 0.f, myv = 0.f;
     int mye = 0;
     for (int i = 0; i < k; ++i) {
-      float bv = -FLT_MAX;
+      float bv = -INFINITY;
       int be = INT_MAX;
 #pragma unroll
       for (int j = 0; j < EC; ++j) {
@@ -588,15 +580,7 @@ __device__ void route_small(const float *logits, const float *sigma, int T, int 
           be = e;
         }
       }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-        const int oe = __shfl_xor_sync(0xffffffffu, be, o);
-        if (better(ov, oe, bv, be)) {
-          bv = ov;
-          be = oe;
-        }
-      }
+      warp_argmax(bv, be);
       if ((be & 31) == lane) taken |= 1u << (be >> 5);
       if (i == 0) v0 = bv;
       denom += expf(bv - v0);
@@ -729,7 +713,7 @@ __device__ __forceinline__ void load_down_mat(const lily_q4_mat &m, int e, int r
 template <int GH, int GI, int EC>
 __global__ void __launch_bounds__(kFusedThreads, 1)
     moe_decode_fused_kernel(FusedArgs a, DecodePtrs w) {
-  extern __shared__ float s_h[];  // [P][I] (phase C) / [T][I] shared h (phase B)
+  extern __shared__ __align__(16) uint16_t s_h[];  // bf16 h of every pair [P][I] (phase C)
   __shared__ int32_t s_U;
   __shared__ int32_t s_uexp[kMaxT * kMaxK + 1];
   __shared__ int32_t s_ubase[kMaxT * kMaxK + 2];
@@ -754,6 +738,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
   }
   __syncthreads();
   const unsigned long long bbase = s_bbase;
+  uint16_t *h16 = reinterpret_cast<uint16_t *>(w.h);  // this path keeps h as bf16
 
   // ------------------------------------------------------------------ phase A
   const int nshared_tasks = a.has_shared ? I / RPS_H : 0;
@@ -812,7 +797,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
         const float gd = seg_sum<GH>(q4_group_dot_b(g0, g1, xg, gs, gb));
         const float ud = seg_sum<GH>(q4_group_dot_b(u0, u1, xg, us, ub));
         // shared pairs sit after the T*k routed pairs
-        if (gh == 0) __stcg(w.h + (size_t)(T * k + t) * I + row, silu_mul(gd, ud));
+        if (gh == 0) h16[(size_t)(T * k + t) * I + row] = f2bf16_rne(silu_mul(gd, ud));
       }
     }
   }
@@ -865,7 +850,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
           }
           const float gd = seg_sum<GH>(q4_group_dot_b(rp[i].a0, rp[i].a1, xg, rp[i].as, rp[i].ab));
           const float ud = seg_sum<GH>(q4_group_dot_b(rp[i].b0, rp[i].b1, xg, rp[i].bs, rp[i].bb));
-          if (gh == 0) __stcg(w.h + (size_t)pr * I + row, silu_mul(gd, ud));
+          if (gh == 0) h16[(size_t)pr * I + row] = f2bf16_rne(silu_mul(gd, ud));
         }
       }
     }
@@ -882,7 +867,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
 
   // ------------------------------------------------------------------ phase C
   const int P = s_ubase[U];  // routed pairs, then the shared expert's T pairs
-  stage_rows(s_h, w.h, P * I);
+  stage_rows(reinterpret_cast<float *>(s_h), reinterpret_cast<const float *>(h16), P * I / 2);
   __syncthreads();
   constexpr int ROWS = kFusedMaxQ * RPS_I;  // rows of this block, at most
   __shared__ float s_part[kFusedMaxT * (kMaxK + 1)][ROWS];
@@ -900,13 +885,19 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
           load_down_mat<GI>(a.down, e, row, H, gi, dr[qi]);
       }
     }
-    XGroup xg;
-    xgroup_from(xg, s_h + (size_t)pr * I + kGroup * gi);
+    XGroupB xg;
+    {
+      uint4 c[8];
+      const uint4 *hp = reinterpret_cast<const uint4 *>(s_h + (size_t)pr * I + kGroup * gi);
+#pragma unroll
+      for (int q = 0; q < 8; ++q) c[q] = hp[q];
+      xgroupb_from_bf16(xg, c);
+    }
     const float pw = s_pair_w[pr];
 #pragma unroll
     for (int qi = 0; qi < kFusedMaxQ; ++qi) {
       if (qi < nq_cta) {
-        const float dd = seg_sum<GI>(q4_group_dot(dr[qi].w0, dr[qi].w1, xg, dr[qi].s, dr[qi].b));
+        const float dd = seg_sum<GI>(q4_group_dot_b(dr[qi].w0, dr[qi].w1, xg, dr[qi].s, dr[qi].b));
         if (gi == 0) s_part[pr][qi * RPS_I + ri] = pw * dd;
       }
     }
@@ -925,7 +916,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
 
 static bool fused_ok(const lily_q4_moe_layer &L, int T) {
   const int P = T * L.top_k + (L.has_shared ? T : 0);
-  if ((size_t)P * L.inter * sizeof(float) > kFusedSmemMax) return false;
+  if ((size_t)P * L.inter * sizeof(uint16_t) > kFusedSmemMax) return false;
   if (T > kFusedMaxT) return false;
   const int GH = L.hidden / kGroup, GI = L.inter / kGroup;
   // each block owns at most kFusedMaxQ down row-steps
@@ -1001,7 +992,7 @@ int launch_moe_decode(const lily_q4_moe_layer &L, const uint16_t *x, int T, uint
     FusedArgs fa{L.gate, L.up, L.down, L.sh_gate, L.sh_up, L.sh_down, L.router, L.router_bias,
                  L.shared_gate, x, y, T, L.n_experts, L.hidden, L.inter, L.top_k, L.has_shared,
                  topk_idx, topk_w};
-    const size_t smem = (size_t)l.P * L.inter * sizeof(float);
+    const size_t smem = (size_t)l.P * L.inter * sizeof(uint16_t);
     if (L.hidden / kGroup == 32) {
       if (L.n_experts <= 256) return launch_fused<32, 8, 8>(fa, p, smem, st);
       if (L.n_experts <= 512) return launch_fused<32, 8, 16>(fa, p, smem, st);

@@ -41,10 +41,9 @@ namespace lq4 {
 
 constexpr int kBM = 128;  // weight rows per tile (MMA M)
 constexpr int kBN = 128;  // tokens per tile (MMA N, padded to a multiple of 16)
-constexpr int kGemmThreads = 512;
 constexpr int kMmaWarp = 4;
 constexpr int kBWarp0 = 5, kBThreads = 96;
-constexpr int kAWarp0 = 8, kAThreads = 256;
+constexpr int kAWarp0 = 8;  // weight producers: warps 8.. (256 threads per A matrix)
 constexpr long long kWaitCycles = 4000000000LL;  // ~2 s at GB300 clocks
 constexpr int kHdrItemsGU = 8, kHdrItemsDN = 9;
 
@@ -59,6 +58,8 @@ struct Cfg {
   static constexpr int NA = MODE == kGateUp ? 2 : 1;  // A tiles per k-block
   static constexpr int SA = MODE == kGateUp ? 3 : 4;  // A (weight) stages
   static constexpr int SB = 6;                        // B (token) stages
+  static constexpr int AT = NA * 256;                 // weight-producer threads (4 words each)
+  static constexpr int THREADS = kAWarp0 * 32 + AT;
   static constexpr int A_BYTES = kBM * 128;
   static constexpr int B_BYTES = kBN * 128;
   static constexpr int A_STAGE = NA * A_BYTES;
@@ -170,7 +171,7 @@ struct ScaleVec {
 };
 
 template <int MODE, int KG>
-__global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const GemmArgs a) {
+__global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) grouped_gemm_kernel(const GemmArgs a) {
   using C = Cfg<MODE>;
   extern __shared__ uint8_t smem_dyn[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(((uintptr_t)smem_dyn + 1023) & ~(uintptr_t)1023);
@@ -190,7 +191,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const Gem
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n_items = MODE == kRouter ? a.n_items_static : *(volatile const int32_t *)a.n_items_ptr;
   if (MODE != kRouter) {
-    for (int i = threadIdx.x; i < kSmemItems; i += kGemmThreads) {
+    for (int i = threadIdx.x; i < kSmemItems; i += C::THREADS) {
       const int it = (int)blockIdx.x + i * (int)gridDim.x;
       if (it < n_items) s_items[i] = a.items[it];
     }
@@ -201,7 +202,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const Gem
   if (threadIdx.x == 0) {
     s_abort = 0;
     for (int s = 0; s < C::SA; ++s) {
-      tc::mbar_init(afull(s), kAThreads);
+      tc::mbar_init(afull(s), C::AT);
       tc::mbar_init(aempty(s), 1);
     }
     for (int s = 0; s < C::SB; ++s) {
@@ -359,10 +360,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const Gem
     tc::cp_async_wait_all();
   } else {
     // ------------------------------------------------------------------ weight producers
-    const int ta = threadIdx.x - kAWarp0 * 32;  // 0..255
+    const int ta = threadIdx.x - kAWarp0 * 32;  // 0 .. C::AT-1
     const int row = ta & (kBM - 1);
-    const int half = ta >> 7;                   // GateUp: matrix; Down/Router: half of the row
-    const int mat = C::NA == 2 ? half : 0;
+    const int sub = ta >> 7;
+    const int mat = C::NA == 2 ? sub >> 1 : 0;  // GateUp: gate or up
+    const int half = sub & 1;                   // which half of the row's k-block
     int sa = 0;
     uint32_t pa = 0;
     bool ok = true;
@@ -393,8 +395,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const Gem
       // Codes of the next group of KG k-blocks are loaded into registers while the current
       // group is dequantised (prefetch distance KG k-blocks); per-item addressing is done
       // once per item.
-      constexpr int NV = C::NA == 2 ? 2 : 1;  // 16-byte code vectors per thread per k-block
-      const int woff = C::NA == 2 ? 0 : 4 * half;
+      constexpr int NV = 1;  // one 16-byte code vector (4 words) per thread per k-block
+      const int woff = 4 * half;
       const uint32_t a_row_off = (uint32_t)(mat * C::A_BYTES + row * 128);
       const uint32_t rsw = (uint32_t)(row & 7);
       const int ngrp = nkb / KG;
@@ -545,11 +547,12 @@ __global__ void __launch_bounds__(256) topk_prefill_kernel(TopkArgs a) {
 #pragma unroll
   for (int j = 0; j < EC; ++j) {
     const int e = lane + 32 * j;
-    float v = -FLT_MAX;
+    float v = -INFINITY;
     if (e < a.E) {
       v = 0.f;
       for (int sp = 0; sp < a.nsplit; ++sp) v += a.logits[((size_t)sp * a.T + t) * a.E + e];
       if (a.bias) v += a.bias[e];
+      v = cand(v);
     }
     lv[j] = v;
   }
@@ -557,7 +560,7 @@ __global__ void __launch_bounds__(256) topk_prefill_kernel(TopkArgs a) {
   float sel_v[16];
   int sel_e[16];
   for (int i = 0; i < a.k; ++i) {
-    float bv = -FLT_MAX;
+    float bv = -INFINITY;
     int be = INT_MAX;
 #pragma unroll
     for (int j = 0; j < EC; ++j) {
@@ -567,15 +570,7 @@ __global__ void __launch_bounds__(256) topk_prefill_kernel(TopkArgs a) {
         be = e;
       }
     }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-      const int oe = __shfl_xor_sync(0xffffffffu, be, o);
-      if (better(ov, oe, bv, be)) {
-        bv = ov;
-        be = oe;
-      }
-    }
+    warp_argmax(bv, be);
     if ((be & 31) == lane) taken |= 1u << (be >> 5);
     sel_v[i] = bv;
     sel_e[i] = be;
@@ -812,7 +807,7 @@ static int launch_gemm_kg(const GemmArgs &a, int grid, cudaStream_t st) {
       return LILY_Q4_ERR_CUDA;
     attr_set = true;
   }
-  grouped_gemm_kernel<MODE, KG><<<grid, kGemmThreads, bytes, st>>>(a);
+  grouped_gemm_kernel<MODE, KG><<<grid, Cfg<MODE>::THREADS, bytes, st>>>(a);
   return check_launch();
 }
 

@@ -218,6 +218,30 @@ __device__ __forceinline__ int warp_excl_scan(int v, int *total) {
 
 __device__ __forceinline__ float silu_mul(float g, float u) { return g / (1.0f + __expf(-g)) * u; }
 
+// Candidate value for an argmax / top-k: NaN counts as -inf, so every candidate can win a
+// round (candidates start at -inf and ties go to the lower index) and a selected index is
+// always a real one, whatever the inputs.
+__device__ __forceinline__ float cand(float v) { return v != v ? -INFINITY : v; }
+
+// Order-preserving map of a float to uint32 (-0 is folded onto +0 first, so the two compare
+// equal as floats do); and back.
+__device__ __forceinline__ uint32_t f2key(float v) {
+  const uint32_t b = __float_as_uint(v + 0.0f);
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+__device__ __forceinline__ float key2f(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
+
+// Warp-wide argmax of (v, i): larger value first, ties to the lower index (NaN-free input);
+// every lane gets the result.  Two single-instruction warp reductions.
+__device__ __forceinline__ void warp_argmax(float &v, int &i) {
+  const uint32_t key = f2key(v);
+  const uint32_t kmax = __reduce_max_sync(0xffffffffu, key);
+  i = (int)__reduce_min_sync(0xffffffffu, key == kmax ? (uint32_t)i : 0xffffffffu);
+  v = key2f(kmax);
+}
+
 // (value, index) ordering used by every argmax / top-k: larger value first, then lower index.
 __device__ __forceinline__ bool better(float va, int ia, float vb, int ib) {
   return va > vb || (va == vb && ia < ib);

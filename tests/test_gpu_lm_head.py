@@ -88,3 +88,15 @@ def test_deterministic(torch_dev):
     a = _run(torch, dev, W, x)
     b = _run(torch, dev, W, x)
     assert a[0] == b[0] and np.array_equal(a[1], b[1])
+
+
+def test_all_nan_logits_give_a_real_token(torch_dev):
+    """NaN scales make every logit NaN: the token is still a real id (0, as ties and NaN
+    candidates resolve to the lowest id) and nothing faults."""
+    torch, dev = torch_dev
+    N, K = 3000, 256
+    W = synth.draw_q4(N, K, 63, 0)
+    W = Q4Matrix(W.w, np.full_like(W.s, 0x7FC0), W.b)   # bf16 NaN scales
+    x = synth.draw_x(K, (63, 0), 0, 0)
+    got_tok, _ = _run(torch, dev, W, x)
+    assert got_tok == 0

@@ -113,3 +113,20 @@ def test_deterministic_and_workspace_reuse(torch_dev):
     c = run_decode(torch, dev, dl, x4, ws)
     assert np.array_equal(a[0], c[0]) and np.array_equal(a[1], c[1])
     assert np.array_equal(a[0][0], b[0][0])
+
+
+@pytest.mark.parametrize("T", [1, 3, 6])
+def test_non_finite_logits_select_lowest_experts(torch_dev, T):
+    """Router offsets of -inf (and NaN, which counts as -inf) make every logit non-finite: the
+    selection still names real experts -- the lowest ids, as the (value desc, index asc) order
+    gives for equal logits -- and the call completes."""
+    torch, dev = torch_dev
+    key = (72, T)
+    L = synth.draw_layer(256, 16, 4, 128, shared=True, router_std=0.05, router_bias=True, key=key)
+    L.router_bias = np.full(16, -np.inf, dtype=np.float32)
+    L.router_bias[[3, 9]] = np.nan
+    x = synth.draw_tokens(256, T, key)
+    dl = q4.DeviceLayer.upload(L, dev)
+    _, idx, _ = run_decode(torch, dev, dl, x)
+    for t in range(T):
+        assert sorted(idx[t].tolist()) == [0, 1, 2, 3]

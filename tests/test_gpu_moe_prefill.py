@@ -113,3 +113,18 @@ def test_deterministic(torch_dev):
     c = run_prefill(torch, dev, dl, x, ws)
     assert np.array_equal(a[0], c[0]) and np.array_equal(a[1], c[1])
     assert b[0].shape == (100, 1024)
+
+
+def test_non_finite_logits_select_lowest_experts(torch_dev):
+    """All logits -inf or NaN (NaN counts as -inf): every token still routes to real experts,
+    the lowest ids, nothing is written out of bounds, and the call completes."""
+    torch, dev = torch_dev
+    key = (83, 0)
+    L = synth.draw_layer(256, 16, 4, 128, shared=True, router_std=0.05, router_bias=True, key=key)
+    L.router_bias = np.full(16, -np.inf, dtype=np.float32)
+    L.router_bias[[3, 9]] = np.nan
+    x = synth.draw_tokens(256, 40, key)
+    dl = q4.DeviceLayer.upload(L, dev)
+    _, idx, _ = run_prefill(torch, dev, dl, x)
+    for t in range(40):
+        assert sorted(idx[t].tolist()) == [0, 1, 2, 3]
