@@ -25,6 +25,7 @@ enum HeaderWord : int {
 struct LmWsLayout {
   size_t off_partial_v, off_partial_i, total;
   int grid;
+  int rows_per_block;  // streaming kernel (K >= 512): contiguous rows per block
 };
 LmWsLayout lm_ws_layout(int N, int K);
 int launch_gemv_argmax(const lily_q4_mat &W, int N, int K, const uint16_t *x, int32_t *token,

@@ -13,6 +13,7 @@
 
 #include "internal.h"
 #include "q4_device.cuh"
+#include "tc_sm100.cuh"
 
 namespace lq4 {
 
@@ -20,15 +21,32 @@ constexpr int kLmThreads = 256;
 constexpr int kLmWarps = kLmThreads / 32;
 constexpr int kLmBlocksPerSm = 2;
 
+// streaming kernel (rows of >= 8 groups)
+constexpr int kLsWarps = 16;                     // compute warps
+constexpr int kLsThreads = (kLsWarps + 1) * 32;  // + the copy warp
+constexpr int kLsStages = 5;
+constexpr int kLsStageCodes = 32768;             // code bytes per stage
+__host__ __device__ constexpr int ls_rows_per_stage(int G) { return kLsStageCodes / (32 * G); }
+
 LmWsLayout lm_ws_layout(int N, int K) {
-  (void)K;
   LmWsLayout l{};
   int sms = sm_count();
   if (sms <= 0) sms = 152;
-  // at most one block per 32 rows, at most kLmBlocksPerSm per SM
-  int want = (N + 31) / 32;
-  l.grid = want < sms * kLmBlocksPerSm ? want : sms * kLmBlocksPerSm;
-  if (l.grid < 1) l.grid = 1;
+  if (K / kGroup >= 8) {
+    // streaming kernel: one block per SM, at most one block per stage of rows, each block a
+    // contiguous range of rows
+    const int sr = ls_rows_per_stage(K / kGroup);
+    const int want = (N + sr - 1) / sr;
+    l.grid = want < sms ? want : sms;
+    if (l.grid < 1) l.grid = 1;
+    l.rows_per_block = (N + l.grid - 1) / l.grid;
+  } else {
+    // at most one block per 32 rows, at most kLmBlocksPerSm per SM
+    int want = (N + 31) / 32;
+    l.grid = want < sms * kLmBlocksPerSm ? want : sms * kLmBlocksPerSm;
+    if (l.grid < 1) l.grid = 1;
+    l.rows_per_block = 0;
+  }
   size_t off = kHdrWords * sizeof(int32_t);
   off = align_up(off);
   l.off_partial_v = off;
@@ -37,6 +55,69 @@ LmWsLayout lm_ws_layout(int N, int K) {
   off = align_up(off + sizeof(int32_t) * (size_t)sms * kLmBlocksPerSm);
   l.total = off;
   return l;
+}
+
+// Block-wide then grid-wide argmax of the threads' (value, row) pairs: every block publishes
+// its best pair, and the last block to finish (ticket on header counter A) reduces the pairs
+// into *token and re-arms the counter for the next call.
+template <int NW>
+__device__ __forceinline__ void block_argmax_finish(float best_v, int best_i, int32_t *token,
+                                                    int32_t *hdr, float *part_v, int32_t *part_i) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  warp_argmax(best_v, best_i);
+  __shared__ float sv_[NW];
+  __shared__ int si_[NW];
+  __shared__ int is_last;
+  if (lane == 0) {
+    sv_[warp] = best_v;
+    si_[warp] = best_i;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float bv_ = sv_[0];
+    int bi_ = si_[0];
+    for (int i = 1; i < NW; ++i)
+      if (better(sv_[i], si_[i], bv_, bi_)) {
+        bv_ = sv_[i];
+        bi_ = si_[i];
+      }
+    part_v[blockIdx.x] = bv_;
+    part_i[blockIdx.x] = bi_;
+    __threadfence();
+    const int ticket = atomicAdd(hdr + kHdrCounterA, 1);
+    is_last = (ticket == (int)gridDim.x - 1);
+  }
+  __syncthreads();
+  if (!is_last) return;
+  __threadfence();
+  float v = -INFINITY;
+  int i = INT_MAX;
+  for (int j = threadIdx.x; j < (int)gridDim.x; j += NW * 32) {
+    const float pv = __ldcg(part_v + j);
+    const int pi = __ldcg(part_i + j);
+    if (better(pv, pi, v, i)) {
+      v = pv;
+      i = pi;
+    }
+  }
+  warp_argmax(v, i);
+  __syncthreads();
+  if (lane == 0) {
+    sv_[warp] = v;
+    si_[warp] = i;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float bv_ = sv_[0];
+    int bi_ = si_[0];
+    for (int j = 1; j < NW; ++j)
+      if (better(sv_[j], si_[j], bv_, bi_)) {
+        bv_ = sv_[j];
+        bi_ = si_[j];
+      }
+    *token = bi_;
+    hdr[kHdrCounterA] = 0;  // leave the counter ready for the next call
+  }
 }
 
 // G = groups per row (K/64), U = row-steps per iteration: a warp issues the loads of U
@@ -100,71 +181,165 @@ __global__ void __launch_bounds__(kLmThreads, kLmBlocksPerSm)
       }
     }
   }
-  // warp argmax
-  warp_argmax(best_v, best_i);
-  __shared__ float sv_[kLmWarps];
-  __shared__ int si_[kLmWarps];
-  __shared__ int is_last;
-  if (lane == 0) {
-    sv_[warp] = best_v;
-    si_[warp] = best_i;
-  }
-  __syncthreads();
+  block_argmax_finish<kLmWarps>(best_v, best_i, token, hdr, part_v, part_i);
+}
+
+// ---------------------------------------------------------------------------------------
+// Streaming variant for rows of at least 8 groups (K >= 512), the LM-head shapes.
+//
+// Each block owns a contiguous range of rows -- one contiguous range of codes, of scales and
+// of biases -- and streams it through a ring of shared-memory stages with untiled bulk
+// copies (one copy thread; completion counted in bytes on the stage's mbarrier), so the
+// loads of later stages are in flight while 16 warps dequantise and reduce the current one.
+// A warp copies its rows of a stage into registers and hands the stage back at once.
+// ---------------------------------------------------------------------------------------
+template <int G>
+struct LsCfg {
+  static constexpr int RPS = 32 / G;                      // rows per warp-step
+  static constexpr int SR = kLsStageCodes / (32 * G);     // rows per stage (32*G code bytes a row)
+  static constexpr int WR = SR / (kLsWarps * RPS);        // warp-steps per warp per stage
+  static constexpr int SC = SR * 2 * G;                   // bytes of scales (and of biases)
+  static constexpr int STAGE = kLsStageCodes + 2 * SC;
+  static constexpr int OFF_BAR = kLsStages * STAGE;
+  static constexpr int BYTES = OFF_BAR + 2 * kLsStages * 8;
+  static_assert(G >= 8 && WR * kLsWarps * RPS == SR && STAGE % 128 == 0, "stage shape");
+};
+
+template <int G>
+__global__ void __launch_bounds__(kLsThreads, 1)
+    gemv_argmax_stream_kernel(const uint32_t *__restrict__ w, const uint16_t *__restrict__ s,
+                              const uint16_t *__restrict__ b, int N, int rows_per_block,
+                              const uint16_t *__restrict__ x, float *__restrict__ logits,
+                              int32_t *__restrict__ token, int32_t *__restrict__ hdr,
+                              float *__restrict__ part_v, int32_t *__restrict__ part_i) {
+  using C = LsCfg<G>;
+  extern __shared__ __align__(128) uint8_t ls_smem[];
+  __shared__ volatile int s_abort;
+  const uint32_t sbase = tc::smem_u32(ls_smem);
+  const uint32_t bar0 = sbase + C::OFF_BAR;
+  auto full = [&](int i) { return bar0 + 8u * i; };
+  auto empty = [&](int i) { return bar0 + 8u * (kLsStages + i); };
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int32_t *err = hdr + kHdrError;
+  const int r_begin = min(N, (int)blockIdx.x * rows_per_block);
+  const int r_end = min(N, r_begin + rows_per_block);
+  const int nst = (r_end - r_begin + C::SR - 1) / C::SR;
   if (threadIdx.x == 0) {
-    float bv_ = sv_[0];
-    int bi_ = si_[0];
-    for (int i = 1; i < kLmWarps; ++i)
-      if (better(sv_[i], si_[i], bv_, bi_)) {
-        bv_ = sv_[i];
-        bi_ = si_[i];
-      }
-    part_v[blockIdx.x] = bv_;
-    part_i[blockIdx.x] = bi_;
-    __threadfence();
-    const int ticket = atomicAdd(hdr + kHdrCounterA, 1);
-    is_last = (ticket == (int)gridDim.x - 1);
+    s_abort = 0;
+    for (int i = 0; i < kLsStages; ++i) {
+      tc::mbar_init(full(i), 1);
+      tc::mbar_init(empty(i), kLsWarps);
+    }
+    tc::mbar_init_fence();
   }
   __syncthreads();
-  if (!is_last) return;
-  __threadfence();
-  // last block: reduce the per-block pairs
-  float v = -INFINITY;
-  int i = INT_MAX;
-  for (int j = threadIdx.x; j < (int)gridDim.x; j += kLmThreads) {
-    const float pv = __ldcg(part_v + j);
-    const int pi = __ldcg(part_i + j);
-    if (better(pv, pi, v, i)) {
-      v = pv;
-      i = pi;
+
+  float best_v = -INFINITY;
+  int best_i = INT_MAX;
+  if (warp == kLsWarps) {
+    // ---------------------------------------------------------------- copy thread
+    if (lane == 0) {
+      int st = 0;
+      for (; st < nst; ++st) {
+        const int slot = st % kLsStages;
+        if (!tc::wait_bar(empty(slot), ((st / kLsStages) & 1) ^ 1, &s_abort, err)) break;
+        const int r0 = r_begin + st * C::SR;
+        const int rows = min(C::SR, r_end - r0);
+        const uint32_t cb = (uint32_t)rows * 32u * G, sb = (uint32_t)rows * 2u * G;
+        const uint32_t dst = sbase + (uint32_t)(slot * C::STAGE);
+        tc::mbar_arrive_expect_tx(full(slot), cb + 2u * sb);
+        tc::bulk_g2s(dst, w + (size_t)r0 * 8 * G, cb, full(slot));
+        tc::bulk_g2s(dst + kLsStageCodes, s + (size_t)r0 * G, sb, full(slot));
+        tc::bulk_g2s(dst + kLsStageCodes + C::SC, b + (size_t)r0 * G, sb, full(slot));
+      }
+      if (s_abort) {
+        // after a time-out: let the copies still in flight land before the block exits
+        for (int j = st > kLsStages ? st - kLsStages : 0; j < st; ++j) {
+          const long long t0 = clock64();
+          while (!tc::mbar_try_wait(full(j % kLsStages), (j / kLsStages) & 1) &&
+                 clock64() - t0 < tc::kWaitCycles) {
+          }
+        }
+      }
+    }
+  } else {
+    // ---------------------------------------------------------------- compute warps
+    const int g = lane % G, rsub = lane / G;
+    XGroupB xg;
+    {
+      uint4 c[8];
+      const uint4 *xp = reinterpret_cast<const uint4 *>(x + kGroup * g);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) c[i] = __ldg(xp + i);
+      xgroupb_from_bf16(xg, c);
+    }
+#pragma unroll 1
+    for (int st = 0; st < nst; ++st) {
+      const int slot = st % kLsStages;
+      if (!__all_sync(0xffffffffu,
+                      tc::wait_bar(full(slot), (st / kLsStages) & 1, &s_abort, err)))
+        break;
+      const int r0 = r_begin + st * C::SR;
+      const int rows = min(C::SR, r_end - r0);
+      const uint8_t *cs = ls_smem + slot * C::STAGE;
+      const uint16_t *ss = reinterpret_cast<const uint16_t *>(cs + kLsStageCodes);
+      const uint16_t *bs = reinterpret_cast<const uint16_t *>(cs + kLsStageCodes + C::SC);
+      uint4 wa[C::WR], wb[C::WR];
+      float sv[C::WR], bv[C::WR];
+#pragma unroll
+      for (int u = 0; u < C::WR; ++u) {
+        const int lr = (warp * C::WR + u) * C::RPS + rsub;
+        if (lr < rows) {
+          const uint4 *p = reinterpret_cast<const uint4 *>(cs + lr * 32 * G + 32 * g);
+          wa[u] = p[0];
+          wb[u] = p[1];
+          sv[u] = bf16f(ss[lr * G + g]);
+          bv[u] = bf16f(bs[lr * G + g]);
+        } else {
+          wa[u] = wb[u] = make_uint4(0, 0, 0, 0);
+          sv[u] = bv[u] = 0.f;
+        }
+      }
+      // the warp's rows are in registers: hand the stage back before computing
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(empty(slot));
+#pragma unroll
+      for (int u = 0; u < C::WR; ++u) {
+        const float d = seg_sum<G>(q4_group_dot_b(wa[u], wb[u], xg, sv[u], bv[u]));
+        const int lr = (warp * C::WR + u) * C::RPS + rsub;
+        if (g == 0 && lr < rows) {
+          const int row = r0 + lr;
+          if (logits) logits[row] = d;
+          const float dc = cand(d);
+          if (better(dc, row, best_v, best_i)) {
+            best_v = dc;
+            best_i = row;
+          }
+        }
+      }
     }
   }
-  warp_argmax(v, i);
-  if (lane == 0) {
-    sv_[warp] = v;
-    si_[warp] = i;
-  }
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    float bv_ = sv_[0];
-    int bi_ = si_[0];
-    for (int j = 1; j < kLmWarps; ++j)
-      if (better(sv_[j], si_[j], bv_, bi_)) {
-        bv_ = sv_[j];
-        bi_ = si_[j];
-      }
-    *token = bi_;
-    hdr[kHdrCounterA] = 0;  // leave the counter ready for the next call
-  }
+  block_argmax_finish<kLsWarps + 1>(best_v, best_i, token, hdr, part_v, part_i);
 }
 
 template <int G>
 static void launch_g(const lily_q4_mat &W, int N, const uint16_t *x, int32_t *token,
                      float *logits, void *ws, const LmWsLayout &l, cudaStream_t st) {
   char *base = static_cast<char *>(ws);
-  gemv_argmax_kernel<G, (G >= 16 ? 8 : 4)><<<l.grid, kLmThreads, 0, st>>>(
-      W.w, W.s, W.b, N, x, logits, token, reinterpret_cast<int32_t *>(base),
-      reinterpret_cast<float *>(base + l.off_partial_v),
-      reinterpret_cast<int32_t *>(base + l.off_partial_i));
+  int32_t *hdr = reinterpret_cast<int32_t *>(base);
+  float *pv = reinterpret_cast<float *>(base + l.off_partial_v);
+  int32_t *pi = reinterpret_cast<int32_t *>(base + l.off_partial_i);
+  if constexpr (G >= 8) {
+    using C = LsCfg<G>;
+    // set on every call: cheap, and correct for whichever device is current
+    cudaFuncSetAttribute(gemv_argmax_stream_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         C::BYTES);
+    gemv_argmax_stream_kernel<G><<<l.grid, kLsThreads, C::BYTES, st>>>(
+        W.w, W.s, W.b, N, l.rows_per_block, x, logits, token, hdr, pv, pi);
+  } else {
+    gemv_argmax_kernel<G, (G >= 16 ? 8 : 4)><<<l.grid, kLmThreads, 0, st>>>(
+        W.w, W.s, W.b, N, x, logits, token, hdr, pv, pi);
+  }
 }
 
 int launch_gemv_argmax(const lily_q4_mat &W, int N, int K, const uint16_t *x, int32_t *token,

@@ -44,7 +44,6 @@ constexpr int kBN = 128;  // tokens per tile (MMA N, padded to a multiple of 16)
 constexpr int kMmaWarp = 4;
 constexpr int kBWarp0 = 5, kBThreads = 96;
 constexpr int kAWarp0 = 8;  // weight producers: warps 8.. (256 threads per A matrix)
-constexpr long long kWaitCycles = 4000000000LL;  // ~2 s at GB300 clocks
 constexpr int kHdrItemsGU = 8, kHdrItemsDN = 9;
 
 // The router GEMM splits K so that more SMs share its few tiles; the partial logits are
@@ -91,24 +90,6 @@ struct GemmArgs {
   const float *bias;
   int32_t *hdr;
 };
-
-// Bounded wait on an mbarrier phase.  sleep_ns > 0 lets a waiting thread off the critical
-// path be suspended instead of spinning (its issue slots go to the producers).
-__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int *abort_flag,
-                                         int32_t *err, uint32_t sleep_ns = 0) {
-  if (tc::mbar_try_wait(bar, parity)) return true;
-  const long long t0 = clock64();
-  while (true) {
-    if (sleep_ns ? tc::mbar_try_wait_sleep(bar, parity, sleep_ns) : tc::mbar_try_wait(bar, parity))
-      return true;
-    if (*abort_flag) return false;
-    if (clock64() - t0 > kWaitCycles) {
-      *abort_flag = 1;
-      atomicExch(err, 1);
-      return false;
-    }
-  }
-}
 
 constexpr int kSmemItems = 256;  // work items of one block staged in shared memory
 
@@ -202,7 +183,7 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) grouped_gemm_kernel(con
   if (threadIdx.x == 0) {
     s_abort = 0;
     for (int s = 0; s < C::SA; ++s) {
-      tc::mbar_init(afull(s), C::AT);
+      tc::mbar_init(afull(s), MODE == kRouter ? C::AT : C::AT / 32);
       tc::mbar_init(aempty(s), 1);
     }
     for (int s = 0; s < C::SB; ++s) {
@@ -233,7 +214,7 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) grouped_gemm_kernel(con
     for (int it = blockIdx.x; it < n_items; it += gridDim.x, ++j) {
       const int4 item = get_item<MODE>(a, it, s_items);
       const int b = j & 1;
-      if (!wait_bar(accf_bar(b), (j >> 1) & 1, &s_abort, err)) break;
+      if (!tc::wait_bar(accf_bar(b), (j >> 1) & 1, &s_abort, err)) break;
       tc::tc_fence_after();
       const int ntok = item.z, npad = (ntok + 15) & ~15;
       const int m = item.w * kBM + r;
@@ -281,13 +262,14 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) grouped_gemm_kernel(con
       for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x, ++j) {
         const int4 item = get_item<MODE>(a, it, s_items);
         const int b = j & 1;
-        if (!wait_bar(acce_bar(b), ((j >> 1) & 1) ^ 1, &s_abort, err)) break;
+        if (!tc::wait_bar(acce_bar(b), ((j >> 1) & 1) ^ 1, &s_abort, err)) break;
         tc::tc_fence_after();
         const int npad = (item.z + 15) & ~15;
         const uint32_t idesc = tc::idesc_bf16_f32(kBM, npad);
         const uint32_t d0 = taddr + (uint32_t)(b * C::ACC_COLS);
         for (int kb = 0; kb < nkb; ++kb) {
-          if (!wait_bar(afull(sa), pa, &s_abort, err) || !wait_bar(bfull(sb), pb, &s_abort, err)) {
+          if (!tc::wait_bar(afull(sa), pa, &s_abort, err) ||
+              !tc::wait_bar(bfull(sb), pb, &s_abort, err)) {
             ok = false;
             break;
           }
@@ -314,7 +296,7 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) grouped_gemm_kernel(con
       }
       // drain: all issued MMAs complete before TMEM is released
       tc::mma_commit(done_bar);
-      wait_bar(done_bar, 0, &s_abort, err);
+      tc::wait_bar(done_bar, 0, &s_abort, err);
     }
     __syncwarp();
   } else if (warp >= kBWarp0 && warp < kAWarp0) {
@@ -344,7 +326,7 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) grouped_gemm_kernel(con
         dsto[i] = tc::sw128((uint32_t)n, (uint32_t)c);
       }
       for (int kb = 0; kb < nkb; ++kb) {
-        if (!wait_bar(bempty(sb), pb ^ 1, &s_abort, err)) {
+        if (!tc::wait_bar(bempty(sb), pb ^ 1, &s_abort, err)) {
           ok = false;
           break;
         }
@@ -374,7 +356,7 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) grouped_gemm_kernel(con
         const int m = item.w * kBM + row;
         const bool valid = m < a.a_rows;
         for (int kb = 0; kb < nkb; ++kb) {
-          if (!wait_bar(aempty(sa), pa ^ 1, &s_abort, err)) {
+          if (!tc::wait_bar(aempty(sa), pa ^ 1, &s_abort, err)) {
             ok = false;
             break;
           }
@@ -470,7 +452,9 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) grouped_gemm_kernel(con
             for (int v = 0; v < NV; ++v)
               raw[i][v] = ld_stream(nxt.w + (n_grp * KG + i) * 8 + 4 * v);
           }
-          if (!wait_bar(aempty(sa), pa ^ 1, &s_abort, err)) {
+          // The decision to go on is warp-uniform, so the warp-wide hand-over below never
+          // waits for a lane that left.
+          if (!__all_sync(0xffffffffu, tc::wait_bar(aempty(sa), pa ^ 1, &s_abort, err))) {
             ok = false;
             break;
           }
@@ -478,8 +462,11 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) grouped_gemm_kernel(con
 #pragma unroll
           for (int q = 0; q < NV * 4; ++q)
             *reinterpret_cast<uint4 *>(sA + ((((uint32_t)(woff + q)) ^ rsw) << 4)) = outv[q];
+          // Each lane orders its tile stores before the tensor core's reads; one arrival per
+          // warp (the barrier expects one per producer warp) after the warp has converged.
           tc::fence_proxy_async();
-          tc::mbar_arrive(afull(sa));
+          __syncwarp();
+          if (lane == 0) tc::mbar_arrive(afull(sa));
           if (++sa == C::SA) { sa = 0; pa ^= 1; }
         }
         c_it = n_it;
@@ -800,13 +787,10 @@ PrefillWsLayout prefill_ws_layout(const lily_q4_moe_layer &L, int T) {
 template <int MODE, int KG>
 static int launch_gemm_kg(const GemmArgs &a, int grid, cudaStream_t st) {
   const int bytes = Cfg<MODE>::BYTES;
-  static bool attr_set = false;  // per instantiation
-  if (!attr_set) {
-    if (cudaFuncSetAttribute(grouped_gemm_kernel<MODE, KG>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess)
-      return LILY_Q4_ERR_CUDA;
-    attr_set = true;
-  }
+  // set on every call: cheap, and correct for whichever device is current
+  if (cudaFuncSetAttribute(grouped_gemm_kernel<MODE, KG>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess)
+    return LILY_Q4_ERR_CUDA;
   grouped_gemm_kernel<MODE, KG><<<grid, Cfg<MODE>::THREADS, bytes, st>>>(a);
   return check_launch();
 }
