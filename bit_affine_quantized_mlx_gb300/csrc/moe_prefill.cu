@@ -23,12 +23,15 @@
 //   warps 0-3  epilogue: tcgen05.ld of the fp32 accumulator (TMEM lanes 0..127)
 //   warp  4    TMEM allocation and the single-thread tcgen05.mma issue loop
 //   warps 5-7  token-row gather: cp.async into a 128-byte-swizzled K-major tile
-//   warps 8-15 weight producers: Q4 codes and scales cp.async'd into a 4-deep raw ring,
-//              dequantised in registers (bf16x2 FMA: s*q + b, one rounding) and stored
-//              as a 128-byte-swizzled K-major bf16 tile
-// Stages are handed over with mbarriers; accumulators are double-buffered in TMEM so the
-// epilogue of one tile overlaps the main loop of the next.  Every wait is bounded: on
-// time-out the kernel records an error word in the workspace, drains and returns.
+//   warps 8-   weight producers: Q4 codes prefetched into registers a group of k-blocks
+//              ahead, dequantised (bf16x2 FMA: s*q + b, one rounding) and written with
+//              tcgen05.st straight into tensor memory as the MMA's A operand (row i of the
+//              tile in lane i); the router GEMM's bf16 A tile is cp.async'd to shared memory
+// Stages are handed over with mbarriers; the down and router accumulators are
+// double-buffered in TMEM so the epilogue of one tile overlaps the main loop of the next
+// (gate/up keeps one accumulator pair: its A stages take the other half of TMEM).  Every
+// wait is bounded: on time-out the kernel records an error word in the workspace, drains
+// and returns.
 #include <cfloat>
 #include <climits>
 #include <cuda_bf16.h>
@@ -52,22 +55,31 @@ __host__ __device__ constexpr int kRouterSplit(int H) { return H >= 1024 ? 4 : 1
 
 enum { kRouter = 0, kGateUp = 1, kDown = 2 };
 
+// Tile memory.  The router's A operand (bf16 weights) is copied into shared memory; the
+// dequantised Q4 tiles of the expert GEMMs are written by the producer threads straight into
+// tensor memory (row i in lane i), so shared-memory bandwidth is left to the token tiles.
+// TMEM columns: accumulators first (NACC buffers of ACC_COLS), then SA A stages of 32*NA.
 template <int MODE>
 struct Cfg {
+  static constexpr bool TMEM_A = MODE != kRouter;
   static constexpr int NA = MODE == kGateUp ? 2 : 1;  // A tiles per k-block
-  static constexpr int SA = MODE == kGateUp ? 3 : 4;  // A (weight) stages
-  static constexpr int SB = 6;                        // B (token) stages
+  static constexpr int SA = MODE == kGateUp ? 4 : (MODE == kDown ? 8 : 4);  // A stages
+  static constexpr int SB = TMEM_A ? 8 : 6;                                 // B (token) stages
   static constexpr int AT = NA * 256;                 // weight-producer threads (4 words each)
   static constexpr int THREADS = kAWarp0 * 32 + AT;
   static constexpr int A_BYTES = kBM * 128;
   static constexpr int B_BYTES = kBN * 128;
-  static constexpr int A_STAGE = NA * A_BYTES;
+  static constexpr int A_STAGE = NA * A_BYTES;        // shared-memory A stage (router)
   static constexpr int ACC_COLS = NA * kBN;
-  static constexpr int TMEM_COLS = 2 * ACC_COLS;  // double buffer
-  static constexpr int OFF_B = SA * A_STAGE;
+  static constexpr int NACC = MODE == kGateUp ? 1 : 2;  // accumulator buffers
+  static constexpr int A_COL0 = NACC * ACC_COLS;        // first TMEM column of the A stages
+  static constexpr int A_COLS = 32 * NA;                // TMEM columns of one A stage
+  static constexpr int TMEM_COLS = TMEM_A ? A_COL0 + SA * A_COLS : NACC * ACC_COLS;
+  static constexpr int OFF_B = TMEM_A ? 0 : SA * A_STAGE;
   static constexpr int OFF_BAR = OFF_B + SB * B_BYTES;
   static constexpr int NBARS = 2 * SA + 2 * SB + 5;
   static constexpr int BYTES = OFF_BAR + NBARS * 8 + 1024;
+  static_assert(TMEM_COLS == 256 || TMEM_COLS == 512, "TMEM allocation is a power of two");
 };
 
 struct GemmArgs {
@@ -213,8 +225,8 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) grouped_gemm_kernel(con
     int j = 0;
     for (int it = blockIdx.x; it < n_items; it += gridDim.x, ++j) {
       const int4 item = get_item<MODE>(a, it, s_items);
-      const int b = j & 1;
-      if (!tc::wait_bar(accf_bar(b), (j >> 1) & 1, &s_abort, err)) break;
+      const int b = j % C::NACC;
+      if (!tc::wait_bar(accf_bar(b), (j / C::NACC) & 1, &s_abort, err)) break;
       tc::tc_fence_after();
       const int ntok = item.z, npad = (ntok + 15) & ~15;
       const int m = item.w * kBM + r;
@@ -261,8 +273,8 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) grouped_gemm_kernel(con
       bool ok = true;
       for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x, ++j) {
         const int4 item = get_item<MODE>(a, it, s_items);
-        const int b = j & 1;
-        if (!tc::wait_bar(acce_bar(b), ((j >> 1) & 1) ^ 1, &s_abort, err)) break;
+        const int b = j % C::NACC;
+        if (!tc::wait_bar(acce_bar(b), ((j / C::NACC) & 1) ^ 1, &s_abort, err)) break;
         tc::tc_fence_after();
         const int npad = (item.z + 15) & ~15;
         const uint32_t idesc = tc::idesc_bf16_f32(kBM, npad);
@@ -275,16 +287,25 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) grouped_gemm_kernel(con
           }
           tc::fence_proxy_async();
           tc::tc_fence_after();
-          const uint32_t sA = sbase + sa * C::A_STAGE;
           const uint32_t sB = sbase + C::OFF_B + sb * C::B_BYTES;
+          if constexpr (C::TMEM_A) {
+            // A stage in TMEM: 8 columns (16 bf16 of K) per MMA
+            const uint32_t tA = taddr + (uint32_t)(C::A_COL0 + sa * C::A_COLS);
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            const uint64_t bd = tc::desc_k128_sw128(sB + 32 * kk);
-            const uint32_t acc = (kb | kk) ? 1u : 0u;
-            tc::mma_bf16(d0, tc::desc_k128_sw128(sA + 32 * kk), bd, idesc, acc);
-            if (MODE == kGateUp)
-              tc::mma_bf16(d0 + kBN, tc::desc_k128_sw128(sA + C::A_BYTES + 32 * kk), bd, idesc,
-                           acc);
+            for (int kk = 0; kk < 4; ++kk) {
+              const uint64_t bd = tc::desc_k128_sw128(sB + 32 * kk);
+              const uint32_t acc = (kb | kk) ? 1u : 0u;
+              tc::mma_bf16_ts(d0, tA + 8 * kk, bd, idesc, acc);
+              if (MODE == kGateUp) tc::mma_bf16_ts(d0 + kBN, tA + 32 + 8 * kk, bd, idesc, acc);
+            }
+          } else {
+            const uint32_t sA = sbase + sa * C::A_STAGE;
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+              const uint64_t bd = tc::desc_k128_sw128(sB + 32 * kk);
+              const uint32_t acc = (kb | kk) ? 1u : 0u;
+              tc::mma_bf16(d0, tc::desc_k128_sw128(sA + 32 * kk), bd, idesc, acc);
+            }
           }
           tc::mma_commit(aempty(sa));
           tc::mma_commit(bempty(sb));
@@ -379,8 +400,9 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) grouped_gemm_kernel(con
       // once per item.
       constexpr int NV = 1;  // one 16-byte code vector (4 words) per thread per k-block
       const int woff = 4 * half;
-      const uint32_t a_row_off = (uint32_t)(mat * C::A_BYTES + row * 128);
-      const uint32_t rsw = (uint32_t)(row & 7);
+      // this thread's 16 TMEM columns of an A stage: lane = row (warp w writes lanes
+      // 32*(w%4) .. +31, which is where its rows fall), columns mat*32 + half*16 ..
+      const uint32_t t_off = ((uint32_t)(warp & 3) << 21) + (uint32_t)(C::A_COL0 + mat * 32 + half * 16);
       const int ngrp = nkb / KG;
       struct Src {
         const uint32_t *w;
@@ -458,13 +480,21 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) grouped_gemm_kernel(con
             ok = false;
             break;
           }
-          uint8_t *sA = smem + sa * C::A_STAGE + a_row_off;
+          tc::tc_fence_after();
+          {
+            uint32_t r[16];
 #pragma unroll
-          for (int q = 0; q < NV * 4; ++q)
-            *reinterpret_cast<uint4 *>(sA + ((((uint32_t)(woff + q)) ^ rsw) << 4)) = outv[q];
-          // Each lane orders its tile stores before the tensor core's reads; one arrival per
-          // warp (the barrier expects one per producer warp) after the warp has converged.
-          tc::fence_proxy_async();
+            for (int q = 0; q < 4; ++q) {
+              r[4 * q + 0] = outv[q].x;
+              r[4 * q + 1] = outv[q].y;
+              r[4 * q + 2] = outv[q].z;
+              r[4 * q + 3] = outv[q].w;
+            }
+            tc::tmem_st16(taddr + t_off + (uint32_t)(sa * C::A_COLS), r);
+          }
+          // The stores are complete (tcgen05.wait::st); one arrival per warp (the barrier
+          // expects one per producer warp) after the warp has converged.
+          tc::tc_fence_before();
           __syncwarp();
           if (lane == 0) tc::mbar_arrive(afull(sa));
           if (++sa == C::SA) { sa = 0; pa ^= 1; }
