@@ -710,6 +710,25 @@ __device__ __forceinline__ void load_down_mat(const lily_q4_mat &m, int e, int r
   r.b = bf16f(ld_u16(m.b + so));
 }
 
+// This block's down rows (row-steps blockIdx.x + qi * gridDim.x, qi < nq) of expert e
+// (e == E: the shared expert).
+template <int GI>
+__device__ __forceinline__ void load_down_rows(const FusedArgs &a, int e, int nq, int ri, int gi,
+                                               DownRow (&dr)[kFusedMaxQ]) {
+  constexpr int RPS_I = 32 / GI;
+  const bool sh = (e == a.E);
+#pragma unroll
+  for (int qi = 0; qi < kFusedMaxQ; ++qi) {
+    if (qi < nq) {
+      const int row = (blockIdx.x + qi * gridDim.x) * RPS_I + ri;
+      if (sh)
+        load_down_mat<GI>(a.sh_down, 0, row, a.H, gi, dr[qi]);
+      else
+        load_down_mat<GI>(a.down, e, row, a.H, gi, dr[qi]);
+    }
+  }
+}
+
 template <int GH, int GI, int EC>
 __global__ void __launch_bounds__(kFusedThreads, 1)
     moe_decode_fused_kernel(FusedArgs a, DecodePtrs w) {
@@ -801,15 +820,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
       }
     }
   }
-  // the shared expert's down rows of this block's row-steps, into L2
   const int nq_cta = (nquads - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x;
-  const uint32_t sb_bytes = RPS_I * GI * 2 < 16 ? 16 : RPS_I * GI * 2;
-  if (a.has_shared && threadIdx.x < nq_cta) {
-    const size_t r0 = (size_t)(blockIdx.x + threadIdx.x * gridDim.x) * RPS_I;
-    prefetch_l2(a.sh_down.w + r0 * (GI * 8), RPS_I * GI * 32);
-    prefetch_l2(a.sh_down.s + r0 * GI, sb_bytes);
-    prefetch_l2(a.sh_down.b + r0 * GI, sb_bytes);
-  }
   if (!grid_barrier(w.hdr, bbase + gridDim.x, &s_abort)) return;
 
   // ------------------------------------------------------------------ phase B
@@ -855,35 +866,27 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
       }
     }
   }
-  // this block's routed down rows, into L2
-  for (int j = threadIdx.x; j < nq_cta * Ur; j += kFusedThreads) {
-    const size_t e = (size_t)s_uexp[j % Ur];
-    const size_t r0 = (size_t)(blockIdx.x + (j / Ur) * gridDim.x) * RPS_I;
-    prefetch_l2(a.down.w + (e * H + r0) * (GI * 8), RPS_I * GI * 32);
-    prefetch_l2(a.down.s + (e * H + r0) * GI, sb_bytes);
-    prefetch_l2(a.down.b + (e * H + r0) * GI, sb_bytes);
-  }
+  // The down rows of each down warp's first pair do not depend on h: their loads are issued
+  // now and stay in flight across the barrier.  Warp 0, whose thread 0 arrives at the grid
+  // barrier, takes no pair, so that arrival never waits on these loads.
+  const int P = s_ubase[U];  // routed pairs, then the shared expert's T pairs
+  constexpr int kDownWarps = kFusedWarps - 1;
+  DownRow dr0[kFusedMaxQ];
+  if (warp >= 1 && warp - 1 < P) load_down_rows<GI>(a, s_pair_e[warp - 1], nq_cta, ri, gi, dr0);
   if (!grid_barrier(w.hdr, bbase + 2ull * gridDim.x, &s_abort)) return;
 
   // ------------------------------------------------------------------ phase C
-  const int P = s_ubase[U];  // routed pairs, then the shared expert's T pairs
   stage_rows(reinterpret_cast<float *>(s_h), reinterpret_cast<const float *>(h16), P * I / 2);
   __syncthreads();
   constexpr int ROWS = kFusedMaxQ * RPS_I;  // rows of this block, at most
   __shared__ float s_part[kFusedMaxT * (kMaxK + 1)][ROWS];
-  for (int pr = warp; pr < P; pr += kFusedWarps) {
-    const int e = s_pair_e[pr];
-    const bool sh = (e == E);
+  for (int pr = warp - 1; warp >= 1 && pr < P; pr += kDownWarps) {
     DownRow dr[kFusedMaxQ];
+    if (pr == warp - 1) {
 #pragma unroll
-    for (int qi = 0; qi < kFusedMaxQ; ++qi) {
-      if (qi < nq_cta) {
-        const int row = (blockIdx.x + qi * gridDim.x) * RPS_I + ri;
-        if (sh)
-          load_down_mat<GI>(a.sh_down, 0, row, H, gi, dr[qi]);
-        else
-          load_down_mat<GI>(a.down, e, row, H, gi, dr[qi]);
-      }
+      for (int qi = 0; qi < kFusedMaxQ; ++qi) dr[qi] = dr0[qi];
+    } else {
+      load_down_rows<GI>(a, s_pair_e[pr], nq_cta, ri, gi, dr);
     }
     XGroupB xg;
     {

@@ -226,6 +226,14 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) grouped_gemm_kernel(con
     for (int it = blockIdx.x; it < n_items; it += gridDim.x, ++j) {
       const int4 item = get_item<MODE>(a, it, s_items);
       const int b = j % C::NACC;
+      // down: the pairs' gate weights of this tile (token n in lane n % 32 of pwv[n / 32]),
+      // fetched before the accumulator is ready
+      float pwv[kBN / 32] = {};
+      if (MODE == kDown) {
+#pragma unroll
+        for (int q = 0; q < kBN / 32; ++q)
+          if (lane + 32 * q < item.z) pwv[q] = __ldg(a.pw + item.y + lane + 32 * q);
+      }
       if (!tc::wait_bar(accf_bar(b), (j / C::NACC) & 1, &s_abort, err)) break;
       tc::tc_fence_after();
       const int ntok = item.z, npad = (ntok + 15) & ~15;
@@ -234,10 +242,9 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) grouped_gemm_kernel(con
       const uint32_t tcol = taddr + ((uint32_t)(warp * 32) << 16) + (uint32_t)(b * C::ACC_COLS);
       for (int c0 = 0; c0 < npad; c0 += 16) {
         float d[16];
-        tc::tmem_ld16(tcol + c0, d);
         if (MODE == kGateUp) {
           float u[16];
-          tc::tmem_ld16(tcol + kBN + c0, u);
+          tc::tmem_ld16x2(tcol + c0, d, tcol + kBN + c0, u);
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
             const int n = c0 + i;
@@ -245,15 +252,17 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) grouped_gemm_kernel(con
               a.h_out[(size_t)(item.y + n) * a.a_rows + kpos(m)] = f2bf16_rne(silu_mul(d[i], u[i]));
           }
         } else if (MODE == kDown) {
+          tc::tmem_ld16(tcol + c0, d);
+          const float pwc = c0 < 32 ? pwv[0] : c0 < 64 ? pwv[1] : c0 < 96 ? pwv[2] : pwv[3];
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
             const int n = c0 + i;
-            if (row_ok && n < ntok) {
-              const float w = a.pw[item.y + n];
+            const float w = __shfl_sync(0xffffffffu, pwc, (c0 & 31) + i);
+            if (row_ok && n < ntok)
               a.o_out[(size_t)(item.y + n) * a.o_ld + m] = f2bf16_rne(w * d[i]);
-            }
           }
         } else {
+          tc::tmem_ld16(tcol + c0, d);
           float *part = a.logits + (size_t)item.x * a.T * a.E;  // partial of k split item.x
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
