@@ -30,9 +30,9 @@ constexpr float kLoOffset = 128.0f;
 __device__ __forceinline__ float bf16f(uint32_t bits16) { return __uint_as_float(bits16 << 16); }
 
 __device__ __forceinline__ uint16_t f2bf16_rne(float f) {
-  uint32_t u = __float_as_uint(f);
-  u += 0x7FFFu + ((u >> 16) & 1u);
-  return (uint16_t)(u >> 16);
+  uint16_t r;  // round to nearest even (one conversion instruction)
+  asm("cvt.rn.bf16.f32 %0, %1;" : "=h"(r) : "f"(f));
+  return r;
 }
 
 // Streaming 16-byte load: read-only, no L1 allocation (weights are read once).
@@ -121,6 +121,44 @@ __device__ __forceinline__ float q4_group_raw(const uint4 w0, const uint4 w1, co
     }
   }
   return (a0 + a2) + (a1 + a3);
+}
+
+// q4_group_raw with the two FMAs of a pair issued as one packed fp32x2 FMA: the pair
+// (v as fp32, low half moved up) against the matching x pair.
+__device__ __forceinline__ float q4_group_raw_x2(const uint4 w0, const uint4 w1, const XGroup &g) {
+  const uint32_t w[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+  float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+#pragma unroll
+  for (int m = 0; m < 8; ++m) {
+    uint32_t ws[4];
+    ws[0] = w[m];
+    asm("shr.b32 %0, %1, 4;" : "=r"(ws[1]) : "r"(w[m]));
+    asm("shr.b32 %0, %1, 8;" : "=r"(ws[2]) : "r"(w[m]));
+    asm("shr.b32 %0, %1, 12;" : "=r"(ws[3]) : "r"(w[m]));
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      uint32_t v, lo;
+      asm("lop3.b32 %0, %1, 0x000F000F, 0x43004300, 0xEA;" : "=r"(v) : "r"(ws[j]));
+      asm("mul.lo.u32 %0, %1, 65536;" : "=r"(lo) : "r"(v));
+      const float2 xv = g.xv[4 * m + j];
+      if (j & 1)
+        asm("{\n.reg .b64 va, xa, acc;\nmov.b64 va, {%2, %3};\nmov.b64 xa, {%4, %5};\n"
+            "mov.b64 acc, {%0, %1};\nfma.rn.f32x2 acc, va, xa, acc;\nmov.b64 {%0, %1}, acc;\n}"
+            : "+f"(a0), "+f"(a1)
+            : "r"(v), "r"(lo), "f"(xv.x), "f"(xv.y));
+      else
+        asm("{\n.reg .b64 va, xa, acc;\nmov.b64 va, {%2, %3};\nmov.b64 xa, {%4, %5};\n"
+            "mov.b64 acc, {%0, %1};\nfma.rn.f32x2 acc, va, xa, acc;\nmov.b64 {%0, %1}, acc;\n}"
+            : "+f"(a2), "+f"(a3)
+            : "r"(v), "r"(lo), "f"(xv.x), "f"(xv.y));
+    }
+  }
+  return (a0 + a2) + (a1 + a3);
+}
+
+__device__ __forceinline__ float q4_group_dot_x2(const uint4 w0, const uint4 w1, const XGroup &g,
+                                                 float s, float b) {
+  return fmaf(s, q4_group_raw_x2(w0, w1, g) - g.C, b * g.X);
 }
 
 // bf16 activations: one lane's 64 x values kept as the bf16 pairs (x_j, x_j+4) matching the
@@ -216,7 +254,11 @@ __device__ __forceinline__ int warp_excl_scan(int v, int *total) {
   return incl - v;
 }
 
-__device__ __forceinline__ float silu_mul(float g, float u) { return g / (1.0f + __expf(-g)) * u; }
+// SiLU(g) * u.  The fast divide is within 2 ulp for denominators below 2^126 and gives 0 above
+// (SiLU of a large negative g is 0 to fp32 precision anyway).
+__device__ __forceinline__ float silu_mul(float g, float u) {
+  return __fdividef(g, 1.0f + __expf(-g)) * u;
+}
 
 // Candidate value for an argmax / top-k: NaN counts as -inf, so every candidate can win a
 // round (candidates start at -inf and ties go to the lower index) and a selected index is
