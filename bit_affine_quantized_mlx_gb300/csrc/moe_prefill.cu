@@ -276,58 +276,60 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) grouped_gemm_kernel(con
     }
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------------ MMA issue
-    if (lane == 0) {
-      int sa = 0, sb = 0, j = 0;
-      uint32_t pa = 0, pb = 0;
-      bool ok = true;
-      for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x, ++j) {
-        const int4 item = get_item<MODE>(a, it, s_items);
-        const int b = j % C::NACC;
-        if (!tc::wait_bar(acce_bar(b), ((j / C::NACC) & 1) ^ 1, &s_abort, err)) break;
-        tc::tc_fence_after();
-        const int npad = (item.z + 15) & ~15;
-        const uint32_t idesc = tc::idesc_bf16_f32(kBM, npad);
-        const uint32_t d0 = taddr + (uint32_t)(b * C::ACC_COLS);
-        for (int kb = 0; kb < nkb; ++kb) {
-          if (!tc::wait_bar(afull(sa), pa, &s_abort, err) ||
-              !tc::wait_bar(bfull(sb), pb, &s_abort, err)) {
-            ok = false;
-            break;
-          }
-          tc::fence_proxy_async();
-          tc::tc_fence_after();
-          const uint32_t sB = sbase + C::OFF_B + sb * C::B_BYTES;
-          if constexpr (C::TMEM_A) {
-            // A stage in TMEM: 8 columns (16 bf16 of K) per MMA
-            const uint32_t tA = taddr + (uint32_t)(C::A_COL0 + sa * C::A_COLS);
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-              const uint64_t bd = tc::desc_k128_sw128(sB + 32 * kk);
-              const uint32_t acc = (kb | kk) ? 1u : 0u;
-              tc::mma_bf16_ts(d0, tA + 8 * kk, bd, idesc, acc);
-              if (MODE == kGateUp) tc::mma_bf16_ts(d0 + kBN, tA + 32 + 8 * kk, bd, idesc, acc);
-            }
-          } else {
-            const uint32_t sA = sbase + sa * C::A_STAGE;
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-              const uint64_t bd = tc::desc_k128_sw128(sB + 32 * kk);
-              const uint32_t acc = (kb | kk) ? 1u : 0u;
-              tc::mma_bf16(d0, tc::desc_k128_sw128(sA + 32 * kk), bd, idesc, acc);
-            }
-          }
-          tc::mma_commit(aempty(sa));
-          tc::mma_commit(bempty(sb));
-          if (++sa == C::SA) { sa = 0; pa ^= 1; }
-          if (++sb == C::SB) { sb = 0; pb ^= 1; }
+    // The whole warp runs the loop (descriptors stay warp-uniform); one elected lane issues
+    // the MMAs and commits.  Every wait outcome is made warp-uniform.
+    int sa = 0, sb = 0, j = 0;
+    uint32_t pa = 0, pb = 0;
+    bool ok = true;
+    for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x, ++j) {
+      const int4 item = get_item<MODE>(a, it, s_items);
+      const int b = j % C::NACC;
+      if (!__all_sync(0xffffffffu,
+                      tc::wait_bar(acce_bar(b), ((j / C::NACC) & 1) ^ 1, &s_abort, err)))
+        break;
+      tc::tc_fence_after();
+      const int npad = (item.z + 15) & ~15;
+      const uint32_t idesc = tc::idesc_bf16_f32(kBM, npad);
+      const uint32_t d0 = taddr + (uint32_t)(b * C::ACC_COLS);
+      for (int kb = 0; kb < nkb; ++kb) {
+        if (!__all_sync(0xffffffffu, tc::wait_bar(afull(sa), pa, &s_abort, err) &&
+                                         tc::wait_bar(bfull(sb), pb, &s_abort, err))) {
+          ok = false;
+          break;
         }
-        if (!ok) break;
-        tc::mma_commit(accf_bar(b));
+        tc::fence_proxy_async();
+        tc::tc_fence_after();
+        const uint32_t sB = sbase + C::OFF_B + sb * C::B_BYTES;
+        if constexpr (C::TMEM_A) {
+          // A stage in TMEM: 8 columns (16 bf16 of K) per MMA
+          const uint32_t tA = taddr + (uint32_t)(C::A_COL0 + sa * C::A_COLS);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint64_t bd = tc::desc_k128_sw128(sB + 32 * kk);
+            const uint32_t acc = (kb | kk) ? 1u : 0u;
+            tc::mma_bf16_ts_warp(d0, tA + 8 * kk, bd, idesc, acc);
+            if (MODE == kGateUp) tc::mma_bf16_ts_warp(d0 + kBN, tA + 32 + 8 * kk, bd, idesc, acc);
+          }
+        } else {
+          const uint32_t sA = sbase + sa * C::A_STAGE;
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint64_t bd = tc::desc_k128_sw128(sB + 32 * kk);
+            const uint32_t acc = (kb | kk) ? 1u : 0u;
+            tc::mma_bf16_warp(d0, tc::desc_k128_sw128(sA + 32 * kk), bd, idesc, acc);
+          }
+        }
+        tc::mma_commit_warp(aempty(sa));
+        tc::mma_commit_warp(bempty(sb));
+        if (++sa == C::SA) { sa = 0; pa ^= 1; }
+        if (++sb == C::SB) { sb = 0; pb ^= 1; }
       }
-      // drain: all issued MMAs complete before TMEM is released
-      tc::mma_commit(done_bar);
-      tc::wait_bar(done_bar, 0, &s_abort, err);
+      if (!ok) break;
+      tc::mma_commit_warp(accf_bar(b));
     }
+    // drain: all issued MMAs complete before TMEM is released
+    tc::mma_commit_warp(done_bar);
+    tc::wait_bar(done_bar, 0, &s_abort, err);
     __syncwarp();
   } else if (warp >= kBWarp0 && warp < kAWarp0) {
     // ------------------------------------------------------------------ token-row gather
