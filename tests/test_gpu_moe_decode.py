@@ -64,6 +64,10 @@ def test_tiny_workload_seed0(torch_dev):
     (1024, 64, 16, 128, True, True, 2),   # largest k
     (2048, 40, 3, 2048, True, False, 2),  # widest intermediate
     (256, 1024, 5, 128, True, False, 3),  # most experts
+    # hidden 2048 / intermediate 512: the single-launch cluster path
+    (2048, 64, 16, 512, True, True, 4),   # top-16 of 64, 4 tokens: several units per cluster
+    (2048, 8, 2, 512, False, False, 3),   # one router row per CTA, no shared expert
+    (2048, 24, 3, 512, True, False, 2),   # a partial router chunk
 ])
 def test_shapes(torch_dev, H, E, k, I, shared, bias, T):
     torch, dev = torch_dev
@@ -115,17 +119,17 @@ def test_deterministic_and_workspace_reuse(torch_dev):
     assert np.array_equal(a[0][0], b[0][0])
 
 
-@pytest.mark.parametrize("T", [1, 3, 6])
-def test_non_finite_logits_select_lowest_experts(torch_dev, T):
+@pytest.mark.parametrize("H,I,T", [(256, 128, 1), (256, 128, 3), (256, 128, 6), (2048, 512, 3)])
+def test_non_finite_logits_select_lowest_experts(torch_dev, H, I, T):
     """Router offsets of -inf (and NaN, which counts as -inf) make every logit non-finite: the
     selection still names real experts -- the lowest ids, as the (value desc, index asc) order
     gives for equal logits -- and the call completes."""
     torch, dev = torch_dev
     key = (72, T)
-    L = synth.draw_layer(256, 16, 4, 128, shared=True, router_std=0.05, router_bias=True, key=key)
+    L = synth.draw_layer(H, 16, 4, I, shared=True, router_std=0.05, router_bias=True, key=key)
     L.router_bias = np.full(16, -np.inf, dtype=np.float32)
     L.router_bias[[3, 9]] = np.nan
-    x = synth.draw_tokens(256, T, key)
+    x = synth.draw_tokens(H, T, key)
     dl = q4.DeviceLayer.upload(L, dev)
     _, idx, _ = run_decode(torch, dev, dl, x)
     for t in range(T):
