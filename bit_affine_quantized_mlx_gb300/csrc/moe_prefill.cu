@@ -76,7 +76,10 @@ struct Cfg {
   static constexpr int A_COLS = 32 * NA;                // TMEM columns of one A stage
   static constexpr int TMEM_COLS = TMEM_A ? A_COL0 + SA * A_COLS : NACC * ACC_COLS;
   static constexpr int OFF_B = TMEM_A ? 0 : SA * A_STAGE;
-  static constexpr int OFF_BAR = OFF_B + SB * B_BYTES;
+  // epilogue staging of one bf16 output tile [kBN tokens][kBM rows] (expert GEMMs)
+  static constexpr int STG_BYTES = TMEM_A ? kBN * kBM * 2 : 0;
+  static constexpr int OFF_STG = OFF_B + SB * B_BYTES;
+  static constexpr int OFF_BAR = OFF_STG + STG_BYTES;
   static constexpr int NBARS = 2 * SA + 2 * SB + 5;
   static constexpr int BYTES = OFF_BAR + NBARS * 8 + 1024;
   static_assert(TMEM_COLS == 256 || TMEM_COLS == 512, "TMEM allocation is a power of two");
@@ -102,6 +105,20 @@ struct GemmArgs {
   const float *bias;
   int32_t *hdr;
 };
+
+// Barrier among the four epilogue warps only (named barrier 1).
+__device__ __forceinline__ void epilogue_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+// The same barrier, returning whether any of the 128 epilogue threads passed `p` true.
+__device__ __forceinline__ bool epilogue_any(bool p) {
+  uint32_t r;
+  asm volatile(
+      "{\n.reg .pred pi, po;\nsetp.ne.u32 pi, %1, 0;\nbar.red.or.pred po, 1, 128, pi;\n"
+      "selp.u32 %0, 1, 0, po;\n}"
+      : "=r"(r)
+      : "r"((uint32_t)p)
+      : "memory");
+  return r != 0;
+}
 
 constexpr int kSmemItems = 256;  // work items of one block staged in shared memory
 
@@ -234,34 +251,52 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) grouped_gemm_kernel(con
         for (int q = 0; q < kBN / 32; ++q)
           if (lane + 32 * q < item.z) pwv[q] = __ldg(a.pw + item.y + lane + 32 * q);
       }
-      if (!tc::wait_bar(accf_bar(b), (j / C::NACC) & 1, &s_abort, err)) break;
+      // all four warps take the same decision, so the epilogue's own barriers never wait for
+      // a warp that left
+      if (epilogue_any(!tc::wait_bar(accf_bar(b), (j / C::NACC) & 1, &s_abort, err))) break;
       tc::tc_fence_after();
       const int ntok = item.z, npad = (ntok + 15) & ~15;
       const int m = item.w * kBM + r;
       const bool row_ok = m < a.a_rows;
       const uint32_t tcol = taddr + ((uint32_t)(warp * 32) << 16) + (uint32_t)(b * C::ACC_COLS);
-      for (int c0 = 0; c0 < npad; c0 += 16) {
-        float d[16];
-        if (MODE == kGateUp) {
-          float u[16];
-          tc::tmem_ld16x2(tcol + c0, d, tcol + kBN + c0, u);
+      if constexpr (MODE != kRouter) {
+        // The tile goes to shared memory as bf16 (row r of the tile at its output position),
+        // the accumulator is handed back, and then the staged token rows are written out with
+        // 16-byte stores.
+        uint16_t *stg = reinterpret_cast<uint16_t *>(smem + C::OFF_STG);  // [kBN][kBM]
+        const int pos = MODE == kGateUp ? kpos(r) : r;
+        for (int c0 = 0; c0 < npad; c0 += 16) {
+          float d[16];
+          if (MODE == kGateUp) {
+            float u[16];
+            tc::tmem_ld16x2(tcol + c0, d, tcol + kBN + c0, u);
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const int n = c0 + i;
-            if (row_ok && n < ntok)
-              a.h_out[(size_t)(item.y + n) * a.a_rows + kpos(m)] = f2bf16_rne(silu_mul(d[i], u[i]));
-          }
-        } else if (MODE == kDown) {
-          tc::tmem_ld16(tcol + c0, d);
-          const float pwc = c0 < 32 ? pwv[0] : c0 < 64 ? pwv[1] : c0 < 96 ? pwv[2] : pwv[3];
+            for (int i = 0; i < 16; ++i) stg[(c0 + i) * kBM + pos] = f2bf16_rne(silu_mul(d[i], u[i]));
+          } else {
+            tc::tmem_ld16(tcol + c0, d);
+            const float pwc = c0 < 32 ? pwv[0] : c0 < 64 ? pwv[1] : c0 < 96 ? pwv[2] : pwv[3];
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const int n = c0 + i;
-            const float w = __shfl_sync(0xffffffffu, pwc, (c0 & 31) + i);
-            if (row_ok && n < ntok)
-              a.o_out[(size_t)(item.y + n) * a.o_ld + m] = f2bf16_rne(w * d[i]);
+            for (int i = 0; i < 16; ++i) {
+              const float w = __shfl_sync(0xffffffffu, pwc, (c0 & 31) + i);
+              stg[(c0 + i) * kBM + pos] = f2bf16_rne(w * d[i]);
+            }
           }
-        } else {
+        }
+        tc::tc_fence_before();
+        tc::mbar_arrive(acce_bar(b));
+        epilogue_sync();  // the whole tile is staged
+        uint16_t *dst = MODE == kGateUp ? a.h_out : a.o_out;
+        const size_t ld = MODE == kGateUp ? (size_t)a.a_rows : (size_t)a.o_ld;
+        const int col0 = item.w * kBM;
+        for (int q = r; q < ntok * (kBM / 8); q += 128) {
+          const int n = q / (kBM / 8), c = q % (kBM / 8);
+          *reinterpret_cast<uint4 *>(dst + (size_t)(item.y + n) * ld + col0 + 8 * c) =
+              *reinterpret_cast<const uint4 *>(stg + n * kBM + 8 * c);
+        }
+        epilogue_sync();  // the staging buffer is free for the next tile
+      } else {
+        for (int c0 = 0; c0 < npad; c0 += 16) {
+          float d[16];
           tc::tmem_ld16(tcol + c0, d);
           float *part = a.logits + (size_t)item.x * a.T * a.E;  // partial of k split item.x
 #pragma unroll
@@ -270,9 +305,9 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) grouped_gemm_kernel(con
             if (row_ok && n < ntok) part[(size_t)(item.y + n) * a.E + m] = d[i];
           }
         }
+        tc::tc_fence_before();
+        tc::mbar_arrive(acce_bar(b));
       }
-      tc::tc_fence_before();
-      tc::mbar_arrive(acce_bar(b));
     }
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------------ MMA issue
