@@ -620,8 +620,8 @@ __global__ void __launch_bounds__(256) topk_prefill_kernel(TopkArgs a) {
     lv[j] = v;
   }
   uint32_t taken = 0;
-  float sel_v[16];
-  int sel_e[16];
+  float myv = -INFINITY;  // lane i < k keeps selection i
+  int mye = 0;
   for (int i = 0; i < a.k; ++i) {
     float bv = -INFINITY;
     int be = INT_MAX;
@@ -635,8 +635,10 @@ __global__ void __launch_bounds__(256) topk_prefill_kernel(TopkArgs a) {
     }
     warp_argmax(bv, be);
     if ((be & 31) == lane) taken |= 1u << (be >> 5);
-    sel_v[i] = bv;
-    sel_e[i] = be;
+    if (lane == i) {
+      myv = bv;
+      mye = be;
+    }
   }
   float sig = 0.f;
   if (a.has_shared) {
@@ -655,19 +657,19 @@ __global__ void __launch_bounds__(256) topk_prefill_kernel(TopkArgs a) {
     acc = seg_sum<32>(acc);
     sig = 1.0f / (1.0f + expf(-acc));
   }
-  if (lane == 0) {
-    float denom = 0.f;
-    for (int i = 0; i < a.k; ++i) denom += expf(sel_v[i] - sel_v[0]);
-    for (int i = 0; i < a.k; ++i) {
-      const float pi = expf(sel_v[i] - sel_v[0]) / denom;
-      a.idx[t * a.k + i] = sel_e[i];
-      a.p[t * a.k + i] = pi;
-      if (a.out_idx) a.out_idx[t * a.k + i] = sel_e[i];
-      if (a.out_w) a.out_w[t * a.k + i] = pi;
-      atomicAdd(a.counts + sel_e[i], 1);
-    }
-    a.sigma[t] = sig;
+  // softmax over the k selected logits, one selection per lane
+  const float v0 = __shfl_sync(0xffffffffu, myv, 0);
+  const float ex = lane < a.k ? expf(myv - v0) : 0.f;
+  const float denom = seg_sum<32>(ex);
+  if (lane < a.k) {
+    const float pi = ex / denom;
+    a.idx[t * a.k + lane] = mye;
+    a.p[t * a.k + lane] = pi;
+    if (a.out_idx) a.out_idx[t * a.k + lane] = mye;
+    if (a.out_w) a.out_w[t * a.k + lane] = pi;
+    atomicAdd(a.counts + mye, 1);
   }
+  if (lane == 0) a.sigma[t] = sig;
 }
 
 struct ScanArgs {
@@ -716,15 +718,21 @@ __global__ void __launch_bounds__(1024) scan_items_kernel(ScanArgs a) {
   }
   __syncthreads();
   const int ntiles = s_ibase[nexp];
-  for (int e = threadIdx.x; e < nexp; e += blockDim.x) {
-    a.offsets[e] = s_off[e];
-    for (int nt = 0; nt < s_nt[e]; ++nt) {
-      const int p0 = s_off[e] + nt * kBN;
-      const int n = min(kBN, s_cnt[e] - nt * kBN);
-      const int tile = s_ibase[e] + nt;
-      for (int mt = 0; mt < a.mt_gu; ++mt) a.items_gu[tile * a.mt_gu + mt] = make_int4(e, p0, n, mt);
-      for (int mt = 0; mt < a.mt_dn; ++mt) a.items_dn[tile * a.mt_dn + mt] = make_int4(e, p0, n, mt);
+  for (int e = threadIdx.x; e < nexp; e += blockDim.x) a.offsets[e] = s_off[e];
+  // one thread per work item: its tile's expert is found by binary search of the tile bases
+  const int ngu = ntiles * a.mt_gu, nitems = ngu + ntiles * a.mt_dn;
+  for (int q = threadIdx.x; q < nitems; q += blockDim.x) {
+    const bool gu = q < ngu;
+    const int mts = gu ? a.mt_gu : a.mt_dn, qi = gu ? q : q - ngu;
+    const int tile = qi / mts, mt = qi % mts;
+    int lo = 0, hi = nexp - 1;  // last e with s_ibase[e] <= tile
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (s_ibase[mid] <= tile) lo = mid; else hi = mid - 1;
     }
+    const int e = lo, nt = tile - s_ibase[e];
+    const int4 item = make_int4(e, s_off[e] + nt * kBN, min(kBN, s_cnt[e] - nt * kBN), mt);
+    if (gu) a.items_gu[qi] = item; else a.items_dn[qi] = item;
   }
   if (threadIdx.x == 0) {
     a.offsets[nexp] = s_off[nexp];
@@ -748,6 +756,7 @@ struct PermArgs {
 // 32 warps owns a contiguous slice of the (token, slot) entries: it counts its matches with
 // ballots, the warps' counts are scanned, then each warp places its matches in order.
 constexpr int kPermThreads = 1024;
+constexpr int kPermStaged = 48 * 1024;  // selections staged in shared memory, at most
 __global__ void __launch_bounds__(kPermThreads) perm_kernel(PermArgs a) {
   const int e = blockIdx.x;
   const int kk = a.k + 1;
@@ -761,14 +770,21 @@ __global__ void __launch_bounds__(kPermThreads) perm_kernel(PermArgs a) {
     return;
   }
   __shared__ int s_cnt[32];
+  extern __shared__ int s_idx[];  // the whole [T][k] selection, staged once when it fits
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int n = a.T * a.k;
+  const bool staged = n <= kPermStaged;
+  if (staged) {
+    for (int j = threadIdx.x; j < n; j += blockDim.x) s_idx[j] = __ldg(a.idx + j);
+    __syncthreads();
+  }
+  const int32_t *idx = staged ? s_idx : a.idx;
   const int slice = ((n + 31) / 32 + 31) & ~31;  // entries per warp, a multiple of 32
   const int lo = warp * slice, hi = min(n, lo + slice);
   int cnt = 0;
   for (int j0 = lo; j0 < hi; j0 += 32) {
     const int j = j0 + lane;
-    cnt += __popc(__ballot_sync(0xffffffffu, j < hi && __ldg(a.idx + j) == e));
+    cnt += __popc(__ballot_sync(0xffffffffu, j < hi && idx[j] == e));
   }
   if (lane == 0) s_cnt[warp] = cnt;
   __syncthreads();
@@ -782,7 +798,7 @@ __global__ void __launch_bounds__(kPermThreads) perm_kernel(PermArgs a) {
   int pos0 = a.offsets[e] + s_cnt[warp];
   for (int j0 = lo; j0 < hi; j0 += 32) {
     const int j = j0 + lane;
-    const bool f = j < hi && __ldg(a.idx + j) == e;
+    const bool f = j < hi && idx[j] == e;
     const unsigned bal = __ballot_sync(0xffffffffu, f);
     if (f) {
       const int pos = pos0 + __popc(bal & ((1u << lane) - 1));
@@ -940,7 +956,12 @@ int launch_moe_prefill(const lily_q4_moe_layer &L, const uint16_t *x, int T, uin
   scan_items_kernel<<<1, 1024, 0, st>>>(sa);
 
   PermArgs pa{idx, p, sigma, offsets, perm, pw, inv, T, E, k};
-  perm_kernel<<<nexp, kPermThreads, 0, st>>>(pa);
+  const int nsel = T * k;
+  const size_t perm_smem = nsel <= kPermStaged ? (size_t)nsel * sizeof(int32_t) : 0;
+  if (cudaFuncSetAttribute(perm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           kPermStaged * (int)sizeof(int32_t)) != cudaSuccess)
+    return LILY_Q4_ERR_CUDA;
+  perm_kernel<<<nexp, kPermThreads, perm_smem, st>>>(pa);
 
   GemmArgs ga{};
   ga.a0 = L.gate;
