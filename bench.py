@@ -263,20 +263,22 @@ def run_gb300(args):
     pf_tflops = pf_flops / (pf_mean / 1e3) / 1e12
     pf_bytes = 257 * EXPERT_BYTES + pfw.E * pfw.H * 2 + 2 * Tp * pfw.H * 2
 
-    # ---- end to end through the public API: host x in, host y out, every layer
-    x_host = [torch.empty((T, wl.H), dtype=torch.int16, pin_memory=True) for _ in range(nl)]
+    # ---- end to end through the public API: every step copies all layers' x from pinned host
+    # memory in one transfer, makes one lily_q4_moe_decode call per layer, and reads every
+    # layer's y back to pinned host memory in one transfer
+    x_host = torch.empty((nl, T, wl.H), dtype=torch.int16, pin_memory=True)
     for l in range(nl):
         x_host[l].copy_(xs[l].cpu())
-    y_host = [torch.empty((T, wl.H), dtype=torch.int16, pin_memory=True) for _ in range(nl)]
-    xdev = torch.empty((T, wl.H), dtype=torch.int16, device=dev)
-    ydev = torch.empty((T, wl.H), dtype=torch.int16, device=dev)
+    y_host = torch.empty((nl, T, wl.H), dtype=torch.int16, pin_memory=True)
+    xdev = torch.empty((nl, T, wl.H), dtype=torch.int16, device=dev)
+    ydev = torch.empty((nl, T, wl.H), dtype=torch.int16, device=dev)
 
     def e2e_step():
         with torch.cuda.stream(stream):
+            xdev.copy_(x_host, non_blocking=True)
             for l in range(nl):
-                xdev.copy_(x_host[l], non_blocking=True)
-                q4.lily_q4_moe_decode(layers[l], xdev, ydev, ws=dws, stream=stream)
-                y_host[l].copy_(ydev, non_blocking=True)
+                q4.lily_q4_moe_decode(layers[l], xdev[l], ydev[l], ws=dws, stream=stream)
+            y_host.copy_(ydev, non_blocking=True)
         stream.synchronize()
 
     e2e_val = None
@@ -328,7 +330,8 @@ def run_gb300(args):
                      "traffic": DECODE_TRAFFIC_BYTES if T == 1 else None},
         "e2e": {"value": e2e_val, "unit": UNIT,
                 "h2d_bytes_per_step": nl * T * wl.H * 2, "d2h_bytes_per_step": nl * T * wl.H * 2,
-                "scope": "decode layers through lily_q4_moe_decode with pinned host x/y copies"},
+                "scope": "decode layers through lily_q4_moe_decode; per step one copy of all "
+                         "layers' x from pinned host memory and one copy of all y back"},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk,
         "setup_s": round(gen_s, 1),
