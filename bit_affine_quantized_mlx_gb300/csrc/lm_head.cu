@@ -22,10 +22,10 @@ constexpr int kLmWarps = kLmThreads / 32;
 constexpr int kLmBlocksPerSm = 2;
 
 // streaming kernel (rows of >= 8 groups)
-constexpr int kLsWarps = 16;                     // compute warps
+constexpr int kLsWarps = 24;                     // compute warps
 constexpr int kLsThreads = (kLsWarps + 1) * 32;  // + the copy warp
-constexpr int kLsStages = 5;
-constexpr int kLsStageCodes = 32768;             // code bytes per stage
+constexpr int kLsStages = 4;
+constexpr int kLsStageCodes = 49152;             // code bytes per stage
 __host__ __device__ constexpr int ls_rows_per_stage(int G) { return kLsStageCodes / (32 * G); }
 
 LmWsLayout lm_ws_layout(int N, int K) {
@@ -190,7 +190,7 @@ __global__ void __launch_bounds__(kLmThreads, kLmBlocksPerSm)
 // Each block owns a contiguous range of rows -- one contiguous range of codes, of scales and
 // of biases -- and streams it through a ring of shared-memory stages with untiled bulk
 // copies (one copy thread; completion counted in bytes on the stage's mbarrier), so the
-// loads of later stages are in flight while 16 warps dequantise and reduce the current one.
+// loads of later stages are in flight while 24 warps dequantise and reduce the current one.
 // A warp copies its rows of a stage into registers and hands the stage back at once.
 // ---------------------------------------------------------------------------------------
 template <int G>
