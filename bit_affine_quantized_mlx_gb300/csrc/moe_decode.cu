@@ -20,6 +20,7 @@
 
 #include "internal.h"
 #include "q4_device.cuh"
+#include "tc_sm100.cuh"
 
 namespace lq4 {
 
@@ -469,6 +470,12 @@ constexpr int kFusedMaxT = 4;
 constexpr int kFusedMaxQ = 4;   // down row-steps per block
 constexpr int kFusedBatch = 3;  // gate/up rows whose loads a warp issues together
 constexpr long long kBarrierCycles = 2000000000LL;  // ~1 s
+// down codes of each warp's first pair, staged before the second grid barrier:
+// [warp][row-step][lane][32 bytes]
+constexpr size_t kFusedDnStage = (size_t)(kFusedThreads / 32) * kFusedMaxQ * 32 * 32;
+__host__ __device__ constexpr size_t fused_dn_offset(size_t P, size_t I) {
+  return (P * I * 2 + 15) / 16 * 16;
+}
 
 struct FusedArgs {
   lily_q4_mat gate, up, down, sh_gate, sh_up, sh_down;
@@ -535,7 +542,8 @@ __device__ bool grid_barrier(int32_t *hdr, unsigned long long target, volatile i
   __syncthreads();
   if (threadIdx.x == 0 && !*s_abort) {
     unsigned long long *cnt = reinterpret_cast<unsigned long long *>(hdr + kHdrBarrier64);
-    __threadfence();
+    // the release reduction itself orders the block's earlier writes (seen by thread 0
+    // through the block barrier) before the arrival
     asm volatile("red.release.gpu.global.add.u64 [%0], 1;" ::"l"(cnt) : "memory");
     const long long t0 = clock64();
     while (ld_acquire_u64(cnt) < target) {
@@ -866,13 +874,35 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
       }
     }
   }
-  // The down rows of each down warp's first pair do not depend on h: their loads are issued
-  // now and stay in flight across the barrier.  Warp 0, whose thread 0 arrives at the grid
-  // barrier, takes no pair, so that arrival never waits on these loads.
+  // The down rows of each down warp's first pair do not depend on h: their codes are copied
+  // into shared memory now (cp.async, nothing held in registers) and their scales loaded, so
+  // the traffic is in flight across the barrier.  Warp 0, whose thread 0 arrives at the grid
+  // barrier, takes no pair.
   const int P = s_ubase[U];  // routed pairs, then the shared expert's T pairs
   constexpr int kDownWarps = kFusedWarps - 1;
-  DownRow dr0[kFusedMaxQ];
-  if (warp >= 1 && warp - 1 < P) load_down_rows<GI>(a, s_pair_e[warp - 1], nq_cta, ri, gi, dr0);
+  uint8_t *s_dn = reinterpret_cast<uint8_t *>(s_h) + fused_dn_offset(P, I);
+  float dsv[kFusedMaxQ], dbv[kFusedMaxQ];
+  if (warp >= 1 && warp - 1 < P) {
+    const int e = s_pair_e[warp - 1];
+    const bool sh = (e == E);
+    const lily_q4_mat &m = sh ? a.sh_down : a.down;
+    const size_t ee = sh ? 0 : (size_t)e;
+#pragma unroll
+    for (int qi = 0; qi < kFusedMaxQ; ++qi) {
+      dsv[qi] = dbv[qi] = 0.f;
+      if (qi < nq_cta) {
+        const int row = (blockIdx.x + qi * gridDim.x) * RPS_I + ri;
+        const size_t wo = (ee * H + row) * (GI * 8) + 8 * gi, so = (ee * H + row) * GI + gi;
+        const uint32_t dst =
+            tc::smem_u32(s_dn + ((size_t)(warp * kFusedMaxQ + qi) * 32 + lane) * 32);
+        tc::cp_async16(dst, m.w + wo, 16);
+        tc::cp_async16(dst + 16, m.w + wo + 4, 16);
+        dsv[qi] = bf16f(ld_u16(m.s + so));
+        dbv[qi] = bf16f(ld_u16(m.b + so));
+      }
+    }
+  }
+  tc::cp_async_commit();
   if (!grid_barrier(w.hdr, bbase + 2ull * gridDim.x, &s_abort)) return;
 
   // ------------------------------------------------------------------ phase C
@@ -883,8 +913,17 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
   for (int pr = warp - 1; warp >= 1 && pr < P; pr += kDownWarps) {
     DownRow dr[kFusedMaxQ];
     if (pr == warp - 1) {
+      tc::cp_async_wait_all();
+      __syncwarp();
 #pragma unroll
-      for (int qi = 0; qi < kFusedMaxQ; ++qi) dr[qi] = dr0[qi];
+      for (int qi = 0; qi < kFusedMaxQ; ++qi) {
+        const uint4 *c =
+            reinterpret_cast<const uint4 *>(s_dn + ((size_t)(warp * kFusedMaxQ + qi) * 32 + lane) * 32);
+        dr[qi].w0 = c[0];
+        dr[qi].w1 = c[1];
+        dr[qi].s = dsv[qi];
+        dr[qi].b = dbv[qi];
+      }
     } else {
       load_down_rows<GI>(a, s_pair_e[pr], nq_cta, ri, gi, dr);
     }
@@ -919,7 +958,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
 
 static bool fused_ok(const lily_q4_moe_layer &L, int T) {
   const int P = T * L.top_k + (L.has_shared ? T : 0);
-  if ((size_t)P * L.inter * sizeof(uint16_t) > kFusedSmemMax) return false;
+  if (fused_dn_offset(P, L.inter) + kFusedDnStage > kFusedSmemMax) return false;
   if (T > kFusedMaxT) return false;
   const int GH = L.hidden / kGroup, GI = L.inter / kGroup;
   // each block owns at most kFusedMaxQ down row-steps
@@ -995,7 +1034,7 @@ int launch_moe_decode(const lily_q4_moe_layer &L, const uint16_t *x, int T, uint
     FusedArgs fa{L.gate, L.up, L.down, L.sh_gate, L.sh_up, L.sh_down, L.router, L.router_bias,
                  L.shared_gate, x, y, T, L.n_experts, L.hidden, L.inter, L.top_k, L.has_shared,
                  topk_idx, topk_w};
-    const size_t smem = (size_t)l.P * L.inter * sizeof(uint16_t);
+    const size_t smem = fused_dn_offset(l.P, L.inter) + kFusedDnStage;
     if (L.hidden / kGroup == 32) {
       if (L.n_experts <= 256) return launch_fused<32, 8, 8>(fa, p, smem, st);
       if (L.n_experts <= 512) return launch_fused<32, 8, 16>(fa, p, smem, st);
