@@ -575,7 +575,7 @@ __device__ void route_small(const float *logits, const float *sigma, int T, int 
 #pragma unroll
     for (int j = 0; j < EC; ++j) lv[j] = (lane + 32 * j < E) ? cand(__ldcg(lg + lane + 32 * j)) : -INFINITY;
     uint32_t taken = 0;
-    float v0 = 0.f, denom = 0.f, myv = 0.f;
+    float myv = 0.f;
     int mye = 0;
     for (int i = 0; i < k; ++i) {
       float bv = -INFINITY;
@@ -590,22 +590,50 @@ __device__ void route_small(const float *logits, const float *sigma, int T, int 
       }
       warp_argmax(bv, be);
       if ((be & 31) == lane) taken |= 1u << (be >> 5);
-      if (i == 0) v0 = bv;
-      denom += expf(bv - v0);
       if (lane == i) {  // lane i keeps selection i
         myv = bv;
         mye = be;
       }
     }
+    // softmax over the k selected logits (selection 0 holds the largest)
+    const float v0 = __shfl_sync(0xffffffffu, myv, 0);
+    const float ex = lane < k ? expf(myv - v0) : 0.f;
+    const float pi = ex / seg_sum<32>(ex);
     if (lane < k) {
-      const float pi = expf(myv - v0) / denom;
       s_idx[t * k + lane] = mye;
       s_p[t * k + lane] = pi;
       if (d.out_idx) d.out_idx[t * k + lane] = mye;
       if (d.out_w) d.out_w[t * k + lane] = pi;
     }
+    if (T == 1) {
+      // one token: the k selected experts are the unique experts, each with one pair;
+      // lane i places selection i at the rank of its expert id among the k
+      int rank = 0;
+      for (int j = 0; j < k; ++j) rank += __shfl_sync(0xffffffffu, mye, j) < mye;
+      if (lane < k) {
+        d.uexp[rank] = mye;
+        d.ubase[rank] = rank;
+        d.pair_tok[rank] = 0;
+        d.pair_w[rank] = pi;
+        d.pair_e[rank] = mye;
+      }
+      if (lane == 0) {
+        int U = k;
+        if (has_shared) {
+          d.uexp[U] = E;
+          d.ubase[U] = k;
+          d.pair_tok[k] = 0;
+          d.pair_w[k] = __ldcg(sigma);
+          d.pair_e[k] = E;
+          ++U;
+        }
+        d.ubase[U] = k + (has_shared ? 1 : 0);
+        *d.U = U;
+      }
+    }
   }
   __syncthreads();
+  if (T == 1) return;
   if (warp == 0) {
     const int n = T * k;  // <= 64
     uint32_t word = 0;    // lane's 32 experts: bit set if selected
