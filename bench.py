@@ -34,7 +34,7 @@ EXPERT_BYTES = 1769472  # gate + up + down of one expert at H=2048, I=512 (codes
 # DRAM bytes (read + write) of one single-launch decode-layer kernel at batch 1, from the ncu
 # capture summarised in profiles/moe_decode_fused_decode-layer_H2048_E256_k8.md.  Set to None
 # whenever that kernel changes until it is captured again.
-DECODE_TRAFFIC_BYTES = 17070336  # ncu dram__bytes_read+write of one moe_decode_fused launch
+DECODE_TRAFFIC_BYTES = 17071104  # ncu dram__bytes_read+write of one moe_decode_fused launch
 
 
 def peaks():
@@ -177,14 +177,20 @@ def run_gb300(args):
     torch.cuda.synchronize()
     gen_s = time.time() - t0
 
-    # One CUDA graph per part of the step (captured after a warm-up call of each part, so
-    # one-time library set-up happens outside capture).  Replaying graphs keeps the host
-    # (ctypes per call) off the critical path, as a serving loop would.
+    # The LM head and prefill parts run as CUDA graphs (captured after a warm-up call of each
+    # part, so one-time library set-up happens outside capture); replaying them keeps the host
+    # (ctypes per call) off the critical path, as a serving loop would.  The decode layers are
+    # launched directly on the stream: each layer's kernel is enqueued as a programmatic
+    # dependent of the previous one, which lets its blocks take SMs while that kernel drains
+    # (a graph replay serialises the kernels fully, about 1 us per layer slower).  The host
+    # enqueues a layer in a few microseconds, well ahead of the ~19 us kernels.
     stream = torch.cuda.Stream(device=dev)
+
+    idx_v = [idx_all[l] for l in range(nl)]  # views made once: slicing costs host time per call
 
     def dec_part():
         for l in range(nl):
-            q4.lily_q4_moe_decode(layers[l], xs[l], ys[l], topk_idx=idx_all[l], ws=dws,
+            q4.lily_q4_moe_decode(layers[l], xs[l], ys[l], topk_idx=idx_v[l], ws=dws,
                                   stream=stream)
 
     def lm_part():
@@ -199,19 +205,20 @@ def run_gb300(args):
             f()
     stream.synchronize()
     graphs = []
-    for f in parts:
+    for f in parts[1:]:
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=stream):
             f()
-        graphs.append(g)
+        graphs.append(g.replay)
     stream.synchronize()
+    runs = [dec_part] + graphs
 
     def step(ev=None):
         with torch.cuda.stream(stream):
-            for i, g in enumerate(graphs):
+            for i, run in enumerate(runs):
                 if ev:
                     ev[i].record(stream)
-                g.replay()
+                run()
             if ev:
                 ev[3].record(stream)
 
@@ -272,12 +279,13 @@ def run_gb300(args):
     y_host = torch.empty((nl, T, wl.H), dtype=torch.int16, pin_memory=True)
     xdev = torch.empty((nl, T, wl.H), dtype=torch.int16, device=dev)
     ydev = torch.empty((nl, T, wl.H), dtype=torch.int16, device=dev)
+    xdev_v, ydev_v = list(xdev), list(ydev)
 
     def e2e_step():
         with torch.cuda.stream(stream):
             xdev.copy_(x_host, non_blocking=True)
             for l in range(nl):
-                q4.lily_q4_moe_decode(layers[l], xdev[l], ydev[l], ws=dws, stream=stream)
+                q4.lily_q4_moe_decode(layers[l], xdev_v[l], ydev_v[l], ws=dws, stream=stream)
             y_host.copy_(ydev, non_blocking=True)
         stream.synchronize()
 

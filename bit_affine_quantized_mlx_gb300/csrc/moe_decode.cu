@@ -446,22 +446,22 @@ __global__ void __launch_bounds__(kDownThreads)
   }
 }
 
-
 // ---------------------------------------------------------------------------------------
-// Single-launch decode layer (cooperative, one block per SM, two grid barriers)
+// Single-launch decode layer (one block per SM, two grid barriers)
 //
 //   phase A: router rows (+ the shared gate row) and the shared expert's gate/up rows,
-//            none of which depends on the routing; each block prefetches the shared
-//            expert's down rows it will need into L2
+//            none of which depends on the routing
 //   barrier
 //   phase B: every block takes the routing of all tokens from the logits (identical
 //            result in every block); routed gate/up rows, each warp issuing the loads of
-//            a batch of rows before computing; each block prefetches its routed down rows
+//            a batch of rows before computing; each down warp copies the codes of its first
+//            pair's down rows into shared memory (cp.async) so they load across the barrier
 //   barrier
 //   phase C: h of every pair staged in shared memory; block b owns down row-steps
-//            b, b + grid, ...; its warps split the pairs, each warp loading its pairs' rows
-//            for all of the block's row-steps at once; partials meet in shared memory and
-//            are summed per token in a fixed order (deterministic)
+//            b, b + grid, ...; its warps split the pairs (warp 0, which arrives at the grid
+//            barriers, takes none), each warp loading its pairs' rows for all of the block's
+//            row-steps at once; partials meet in shared memory and are summed per token in a
+//            fixed order (deterministic)
 // ---------------------------------------------------------------------------------------
 constexpr int kFusedThreads = 448;
 constexpr int kFusedWarps = kFusedThreads / 32;
@@ -488,16 +488,6 @@ struct FusedArgs {
   int32_t *out_idx;
   float *out_w;
 };
-
-__device__ __forceinline__ int ld_acquire(const int32_t *p) {
-  int v;
-  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-
-__device__ __forceinline__ void prefetch_l2(const void *p, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
-}
 
 // Copy n floats (n a multiple of 4, 16-byte aligned) from L2 to shared memory, 8 float4
 // loads in flight per thread.
@@ -787,6 +777,12 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
   const int gi = lane % GI, ri = lane / GI;
   const int nquads = H / RPS_I;  // down row-steps
   __shared__ unsigned long long s_bbase;
+  // Launched as a programmatic dependent of the previous kernel on the stream: the block may
+  // start while that kernel drains, so it lets its own dependents be scheduled, then waits
+  // for the previous kernel to complete before touching anything it may have written (x,
+  // the workspace).
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   if (threadIdx.x == 0) {
     s_abort = 0;
     s_bbase = barrier_base(w.hdr);
@@ -1016,9 +1012,18 @@ static int launch_fused(const FusedArgs &fa, const DecodePtrs &p, size_t smem, c
   cfg.blockDim = dim3(kFusedThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
+  // One block per SM (the occupancy check above), so on a GPU that runs this stream alone
+  // every block is resident at once, which the grid barriers need.  The launch is a
+  // programmatic dependent of the previous kernel on the stream: blocks take SMs as that
+  // kernel's blocks leave and wait for it (griddepcontrol.wait) before reading anything,
+  // which hides the launch gap between consecutive layers.  (A cooperative launch would
+  // guarantee co-residency even with other work on the GPU, but the runtime does not accept
+  // it together with programmatic serialization.)  Should other work hold SMs so that some
+  // blocks start late, the bounded barrier waits give up and the call reports
+  // LILY_Q4_ERR_TIMEOUT through lily_q4_workspace_status instead of hanging.
   cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeCooperative;
-  attr[0].val.cooperative = 1;
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   if (cudaLaunchKernelEx(&cfg, fn, fa, p) != cudaSuccess) return LILY_Q4_ERR_CUDA;

@@ -172,8 +172,9 @@ LILY_Q4_API size_t lily_q4_gemv_argmax_workspace_bytes(int32_t N, int32_t K);
 
 /* Number of kernel launches one lily_q4_moe_decode (prefill = 0) or lily_q4_moe_prefill
  * (prefill = 1) call enqueues for this layer and T; 0 when the arguments are invalid.
- * Decode uses one cooperative launch when its single-launch kernel covers the shapes and
- * batch, three launches otherwise. */
+ * Decode uses one launch when its single-launch kernel covers the shapes and batch (one
+ * block per SM, enqueued as a programmatic dependent of the previous kernel on the
+ * stream), three launches otherwise. */
 LILY_Q4_API int lily_q4_moe_launches(const lily_q4_moe_layer *layer, int32_t T, int32_t prefill);
 
 /* Zero-fill a workspace on `stream` (asynchronous). */
