@@ -450,31 +450,60 @@ __global__ void __launch_bounds__(kDownThreads)
 // Single-launch decode layer (one block per SM, two grid barriers)
 //
 //   phase A: router rows (+ the shared gate row) and the shared expert's gate/up rows,
-//            none of which depends on the routing
+//            none of which depends on the routing; x is prepared once per block in shared
+//            memory for the Q4 dot products while the first weight loads are in flight
 //   barrier
 //   phase B: every block takes the routing of all tokens from the logits (identical
 //            result in every block); routed gate/up rows, each warp issuing the loads of
-//            a batch of rows before computing; each down warp copies the codes of its first
-//            pair's down rows into shared memory (cp.async) so they load across the barrier
+//            a batch of rows before computing; each warp copies the codes and scales of its
+//            first down tasks into shared memory (cp.async) so they load across the barrier
 //   barrier
-//   phase C: h of every pair staged in shared memory; block b owns down row-steps
-//            b, b + grid, ...; its warps split the pairs (warp 0, which arrives at the grid
-//            barriers, takes none), each warp loading its pairs' rows for all of the block's
-//            row-steps at once; partials meet in shared memory and are summed per token in a
-//            fixed order (deterministic)
+//   phase C: h of every pair prepared in shared memory; block b owns down row-steps
+//            b, b + grid, ...; the (pair, row-step) tasks are spread over all warps;
+//            partials meet in shared memory and are summed per token in a fixed order
+//            (deterministic)
 // ---------------------------------------------------------------------------------------
 constexpr int kFusedThreads = 448;
 constexpr int kFusedWarps = kFusedThreads / 32;
-constexpr size_t kFusedSmemMax = 100 * 1024;
+constexpr size_t kFusedSmemMax = 160 * 1024;
 constexpr int kFusedMaxT = 4;
 constexpr int kFusedMaxQ = 4;   // down row-steps per block
-constexpr int kFusedBatch = 3;  // gate/up rows whose loads a warp issues together
+constexpr int kFusedBatch = 2;  // gate/up rows whose loads a warp issues together
 constexpr long long kBarrierCycles = 2000000000LL;  // ~1 s
-// down codes of each warp's first pair, staged before the second grid barrier:
-// [warp][row-step][lane][32 bytes]
-constexpr size_t kFusedDnStage = (size_t)(kFusedThreads / 32) * kFusedMaxQ * 32 * 32;
-__host__ __device__ constexpr size_t fused_dn_offset(size_t P, size_t I) {
-  return (P * I * 2 + 15) / 16 * 16;
+// Down tasks (pair, row-step) of a block: warp w takes tasks w, w + kFusedWarps, ...; its
+// first kFusedStaged tasks have their codes and scales copied into shared memory before the
+// second grid barrier.
+constexpr int kFusedStaged = 4;
+constexpr int kFusedSlots = kFusedWarps * kFusedStaged;
+constexpr int kFusedMaxLoads = 6;  // 16-byte loads per thread when preparing x or h
+
+// Dynamic shared memory of the single-launch kernel (byte offsets, 16-byte aligned): x as
+// given, x prepared for the Q4 dot products (pair words + per-group sums), the staged down
+// codes ([slot][lane][32 bytes]) and scales ([slot][s 32 | b 32] bf16), then h prepared like
+// x.  h is sized for P pairs; the rest does not depend on the routing.
+struct FusedLayout {
+  size_t xr, xp, xX, dsc, dn, hp, hX, total;
+};
+__host__ __device__ constexpr size_t al16(size_t v) { return (v + 15) / 16 * 16; }
+__host__ __device__ inline FusedLayout fused_layout(int P, int T, int H, int I) {
+  FusedLayout l{};
+  size_t o = 0;
+  l.xr = o;  // x as given (bf16), for the router rows
+  o = al16(o + (size_t)T * H * 2);
+  l.xp = o;
+  o = al16(o + (size_t)T * H * 2);
+  l.xX = o;
+  o = al16(o + (size_t)T * (H / kGroup) * 4);
+  l.dsc = o;
+  o = al16(o + (size_t)kFusedSlots * 128);
+  l.dn = o;
+  o = al16(o + (size_t)kFusedSlots * 32 * 32);
+  l.hp = o;
+  o = al16(o + (size_t)P * I * 2);
+  l.hX = o;
+  o = al16(o + (size_t)P * (I / kGroup) * 4);
+  l.total = o;
+  return l;
 }
 
 struct FusedArgs {
@@ -489,25 +518,73 @@ struct FusedArgs {
   float *out_w;
 };
 
-// Copy n floats (n a multiple of 4, 16-byte aligned) from L2 to shared memory, 8 float4
-// loads in flight per thread.
-__device__ __forceinline__ void stage_rows(float *dst, const float *src, int n) {
-  const int n4 = n / 4;
-  const float4 *s4 = reinterpret_cast<const float4 *>(src);
-  float4 *d4 = reinterpret_cast<float4 *>(dst);
-  for (int base = threadIdx.x; base < n4; base += kFusedThreads * 8) {
-    float4 v[8];
+// Word offset of chunk c (8 values) of 64-value group g in a prepared vector: each group's
+// eight 4-word chunks are rotated by g so that lanes reading different groups at once hit
+// different shared-memory banks.
+__device__ __forceinline__ int xg_word(int g, int c) { return g * 32 + (((c + g) & 7) << 2); }
+
+// Prepare n8 chunks of 8 bf16 values (src 16-byte aligned, read through L2) for
+// q4_group_dot_b: each chunk becomes the four words (v[j] | v[j+4] << 16), j < 4 -- the order
+// in which the dequantised codes pair up -- and each 64-value group's sum goes to X (and the
+// chunk as given to raw[c], with RAW).  The whole
+// block takes part (the group sums are warp reductions over 8 consecutive chunks); every load
+// is issued before any is used.  n8 <= kFusedMaxLoads * kFusedThreads, a multiple of 8.
+template <bool RAW>
+__device__ __forceinline__ void xg_stage(uint32_t *dst, float *X, const uint16_t *src, int n8,
+                                         uint4 *raw) {
+  const uint4 *s4 = reinterpret_cast<const uint4 *>(src);
+  uint4 v[kFusedMaxLoads];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int j = base + i * kFusedThreads;
-      if (j < n4) v[i] = __ldcg(s4 + j);
-    }
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int j = base + i * kFusedThreads;
-      if (j < n4) d4[j] = v[i];
-    }
+  for (int i = 0; i < kFusedMaxLoads; ++i) {
+    const int c = threadIdx.x + i * kFusedThreads;
+    if (c < n8) v[i] = __ldcg(s4 + c);
   }
+#pragma unroll
+  for (int i = 0; i < kFusedMaxLoads; ++i) {
+    if (i * kFusedThreads >= n8) break;  // same for every thread of the block
+    const int c = threadIdx.x + i * kFusedThreads;
+    float sum = 0.f;
+    if (c < n8) {
+      if (RAW) raw[c] = v[i];
+      const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};  // w[q] = v[2q] | v[2q+1] << 16
+      uint32_t o[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const uint32_t lo = (j & 1) ? (w[j >> 1] >> 16) : (w[j >> 1] & 0xFFFFu);
+        const uint32_t hi = (j & 1) ? (w[2 + (j >> 1)] >> 16) : (w[2 + (j >> 1)] & 0xFFFFu);
+        o[j] = lo | (hi << 16);
+        sum += __uint_as_float(lo << 16) + __uint_as_float(hi << 16);
+      }
+      *reinterpret_cast<uint4 *>(dst + xg_word(c >> 3, c & 7)) = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+    sum = seg_sum<8>(sum);
+    if (c < n8 && (c & 7) == 0) X[c >> 3] = sum;
+  }
+}
+
+// Group g of a vector prepared by xg_stage, into the registers q4_group_dot_b takes.
+__device__ __forceinline__ void xg_load(XGroupB &g, const uint32_t *xp, const float *X, int grp) {
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    const uint4 v = *reinterpret_cast<const uint4 *>(xp + xg_word(grp, c));
+    g.xp[4 * c + 0] = v.x;
+    g.xp[4 * c + 1] = v.y;
+    g.xp[4 * c + 2] = v.z;
+    g.xp[4 * c + 3] = v.w;
+  }
+  g.X = X[grp];
+  g.X128 = 128.0f * g.X;
+}
+
+// The GI bf16 scales (or biases) of one down row, global -> shared (GI = 8: 16 bytes,
+// GI = 2: 4 bytes; both addresses aligned to the size).
+template <int GI>
+__device__ __forceinline__ void cp_async_row_scales(uint32_t dst, const uint16_t *src) {
+  static_assert(GI == 8 || GI == 2, "row scales of 16 or 4 bytes");
+  if constexpr (GI == 8)
+    tc::cp_async16(dst, src, 16);
+  else
+    tc::cp_async4(dst, src);
 }
 
 // Grid barrier on a 64-bit arrival counter that only grows: each block adds 1 per barrier
@@ -558,6 +635,8 @@ __device__ void route_small(const float *logits, const float *sigma, int T, int 
   __shared__ float s_p[4 * kMaxK];
   __shared__ int s_cnt[4 * kMaxK + 1];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  // the shared expert's gate of token `lane`, loaded together with the logits
+  const float sig = (has_shared && warp == 0 && lane < T) ? __ldcg(sigma + lane) : 0.f;
   if (warp < T) {
     const int t = warp;
     const float *lg = logits + (size_t)t * E;
@@ -613,7 +692,7 @@ __device__ void route_small(const float *logits, const float *sigma, int T, int 
           d.uexp[U] = E;
           d.ubase[U] = k;
           d.pair_tok[k] = 0;
-          d.pair_w[k] = __ldcg(sigma);
+          d.pair_w[k] = sig;
           d.pair_e[k] = E;
           ++U;
         }
@@ -690,7 +769,7 @@ __device__ void route_small(const float *logits, const float *sigma, int T, int 
     }
     if (has_shared && lane < T) {
       d.pair_tok[n + lane] = lane;
-      d.pair_w[n + lane] = __ldcg(sigma + lane);
+      d.pair_w[n + lane] = sig;
       d.pair_e[n + lane] = E;
     }
   }
@@ -736,29 +815,41 @@ __device__ __forceinline__ void load_down_mat(const lily_q4_mat &m, int e, int r
   r.b = bf16f(ld_u16(m.b + so));
 }
 
-// This block's down rows (row-steps blockIdx.x + qi * gridDim.x, qi < nq) of expert e
-// (e == E: the shared expert).
-template <int GI>
-__device__ __forceinline__ void load_down_rows(const FusedArgs &a, int e, int nq, int ri, int gi,
-                                               DownRow (&dr)[kFusedMaxQ]) {
-  constexpr int RPS_I = 32 / GI;
-  const bool sh = (e == a.E);
+// Weights of one phase-A task into registers: a router row (bf16; the lane's chunks
+// lane + 32 j) or one row-step of the shared expert's gate and up rows (codes in wv[0..3],
+// raw bf16 scales and biases in sc, converted where they are used).
+template <int GH>
+__device__ __forceinline__ void load_phase_a(const FusedArgs &a, int task, int nrouter, int lane,
+                                             uint4 (&wv)[8], uint32_t (&sc)[4]) {
+  constexpr int RPS_H = 32 / GH;
+  if (task < nrouter) {
+    const uint16_t *wr = task < a.E ? a.router + (size_t)task * a.H : a.shared_gate;
+    const int nchunk = a.H / 8;
 #pragma unroll
-  for (int qi = 0; qi < kFusedMaxQ; ++qi) {
-    if (qi < nq) {
-      const int row = (blockIdx.x + qi * gridDim.x) * RPS_I + ri;
-      if (sh)
-        load_down_mat<GI>(a.sh_down, 0, row, a.H, gi, dr[qi]);
-      else
-        load_down_mat<GI>(a.down, e, row, a.H, gi, dr[qi]);
+    for (int j = 0; j < 8; ++j) {
+      const int c = lane + 32 * j;
+      wv[j] = c < nchunk ? ld_stream(wr + 8 * c) : make_uint4(0, 0, 0, 0);
     }
+  } else {
+    const int gh = lane % GH, rh = lane / GH;
+    const int row = (task - nrouter) * RPS_H + rh;
+    const size_t wo = (size_t)row * (GH * 8) + 8 * gh, so = (size_t)row * GH + gh;
+    wv[0] = ld_stream(a.sh_gate.w + wo);
+    wv[1] = ld_stream(a.sh_gate.w + wo + 4);
+    wv[2] = ld_stream(a.sh_up.w + wo);
+    wv[3] = ld_stream(a.sh_up.w + wo + 4);
+    sc[0] = ld_u16(a.sh_gate.s + so);
+    sc[1] = ld_u16(a.sh_gate.b + so);
+    sc[2] = ld_u16(a.sh_up.s + so);
+    sc[3] = ld_u16(a.sh_up.b + so);
   }
 }
 
 template <int GH, int GI, int EC>
 __global__ void __launch_bounds__(kFusedThreads, 1)
     moe_decode_fused_kernel(FusedArgs a, DecodePtrs w) {
-  extern __shared__ __align__(16) uint16_t s_h[];  // bf16 h of every pair [P][I] (phase C)
+  static_assert(kFusedThreads % 8 == 0, "xg_stage groups 8 consecutive threads");
+  extern __shared__ __align__(16) uint8_t fsm[];
   __shared__ int32_t s_U;
   __shared__ int32_t s_uexp[kMaxT * kMaxK + 1];
   __shared__ int32_t s_ubase[kMaxT * kMaxK + 2];
@@ -766,6 +857,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
   __shared__ int32_t s_pair_e[kMaxPairs];
   __shared__ float s_pair_w[kMaxPairs];
   __shared__ volatile int s_abort;
+  __shared__ unsigned long long s_bbase;
   constexpr int RPS_H = 32 / GH;  // rows per warp-step, K = H (gate/up)
   constexpr int RPS_I = 32 / GI;  // rows per warp-step, K = I (down)
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -776,7 +868,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
   const int gh = lane % GH, rh = lane / GH;
   const int gi = lane % GI, ri = lane / GI;
   const int nquads = H / RPS_I;  // down row-steps
-  __shared__ unsigned long long s_bbase;
+  const int GXH = H / kGroup, GXI = I / kGroup;  // groups of an x row, of an h row
   // Launched as a programmatic dependent of the previous kernel on the stream: the block may
   // start while that kernel drains, so it lets its own dependents be scheduled, then waits
   // for the previous kernel to complete before touching anything it may have written (x,
@@ -787,31 +879,38 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
     s_abort = 0;
     s_bbase = barrier_base(w.hdr);
   }
-  __syncthreads();
-  const unsigned long long bbase = s_bbase;
-  uint16_t *h16 = reinterpret_cast<uint16_t *>(w.h);  // this path keeps h as bf16
+  const FusedLayout L0 = fused_layout(0, T, H, I);  // the offsets that do not depend on P
+  const uint4 *s_xr = reinterpret_cast<const uint4 *>(fsm + L0.xr);
+  uint32_t *s_xp = reinterpret_cast<uint32_t *>(fsm + L0.xp);
+  float *s_xX = reinterpret_cast<float *>(fsm + L0.xX);
+  uint16_t *s_dsc = reinterpret_cast<uint16_t *>(fsm + L0.dsc);
+  uint8_t *s_dn = fsm + L0.dn;
+  uint16_t *h16 = reinterpret_cast<uint16_t *>(w.h);  // this path keeps h as bf16 [pair][I]
 
   // ------------------------------------------------------------------ phase A
+  // Each warp issues its first task's weight loads, then the block prepares x in shared
+  // memory while they are in flight.
   const int nshared_tasks = a.has_shared ? I / RPS_H : 0;
-  for (int task = gw; task < nrouter + nshared_tasks; task += nw) {
+  const int ntasks_a = nrouter + nshared_tasks;
+  uint4 wv[8];
+  uint32_t sc[4];
+  if (gw < ntasks_a) load_phase_a<GH>(a, gw, nrouter, lane, wv, sc);
+  xg_stage<true>(s_xp, s_xX, a.x, T * H / 8, reinterpret_cast<uint4 *>(fsm + L0.xr));
+  __syncthreads();
+  const unsigned long long bbase = s_bbase;
+  for (int task = gw; task < ntasks_a; task += nw) {
+    if (task != gw) load_phase_a<GH>(a, task, nrouter, lane, wv, sc);
     if (task < nrouter) {
       const int row = task;
-      const uint16_t *wr = row < E ? a.router + (size_t)row * H : a.shared_gate;
       const int nchunk = H / 8;
-      uint4 wv[8];
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const int c = lane + 32 * j;
-        wv[j] = c < nchunk ? ld_stream(wr + 8 * c) : make_uint4(0, 0, 0, 0);
-      }
       for (int t = 0; t < T; ++t) {
-        const uint16_t *xt = a.x + (size_t)t * H;
+        const uint4 *xt = s_xr + (size_t)t * nchunk;
         float acc = 0.f;
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
           const int c = lane + 32 * j;
           if (c < nchunk) {
-            const uint4 xv = __ldg(reinterpret_cast<const uint4 *>(xt + 8 * c));
+            const uint4 xv = xt[c];
             const uint32_t ww[4] = {wv[j].x, wv[j].y, wv[j].z, wv[j].w};
             const uint32_t xx[4] = {xv.x, xv.y, xv.z, xv.w};
 #pragma unroll
@@ -833,26 +932,17 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
     } else {
       // shared expert gate/up rows (one warp-step of RPS_H rows)
       const int row = (task - nrouter) * RPS_H + rh;
-      const size_t wo = (size_t)row * (GH * 8) + 8 * gh, so = (size_t)row * GH + gh;
-      const uint4 g0 = ld_stream(a.sh_gate.w + wo), g1 = ld_stream(a.sh_gate.w + wo + 4);
-      const uint4 u0 = ld_stream(a.sh_up.w + wo), u1 = ld_stream(a.sh_up.w + wo + 4);
-      const float gs = bf16f(ld_u16(a.sh_gate.s + so)), gb = bf16f(ld_u16(a.sh_gate.b + so));
-      const float us = bf16f(ld_u16(a.sh_up.s + so)), ub = bf16f(ld_u16(a.sh_up.b + so));
+      const float gs = bf16f(sc[0]), gb = bf16f(sc[1]), us = bf16f(sc[2]), ub = bf16f(sc[3]);
       for (int t = 0; t < T; ++t) {
         XGroupB xg;
-        uint4 c[8];
-        const uint4 *xp = reinterpret_cast<const uint4 *>(a.x + (size_t)t * H + kGroup * gh);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) c[i] = __ldg(xp + i);
-        xgroupb_from_bf16(xg, c);
-        const float gd = seg_sum<GH>(q4_group_dot_b(g0, g1, xg, gs, gb));
-        const float ud = seg_sum<GH>(q4_group_dot_b(u0, u1, xg, us, ub));
+        xg_load(xg, s_xp, s_xX, t * GXH + gh);
+        const float gd = seg_sum<GH>(q4_group_dot_b(wv[0], wv[1], xg, gs, gb));
+        const float ud = seg_sum<GH>(q4_group_dot_b(wv[2], wv[3], xg, us, ub));
         // shared pairs sit after the T*k routed pairs
         if (gh == 0) h16[(size_t)(T * k + t) * I + row] = f2bf16_rne(silu_mul(gd, ud));
       }
     }
   }
-  const int nq_cta = (nquads - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x;
   if (!grid_barrier(w.hdr, bbase + gridDim.x, &s_abort)) return;
 
   // ------------------------------------------------------------------ phase B
@@ -884,11 +974,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
         for (int pr = s_ubase[u]; pr < s_ubase[u + 1]; ++pr) {
           const int t = s_pair_tok[pr];
           if (t != xg_tok) {
-            uint4 c[8];
-            const uint4 *xp = reinterpret_cast<const uint4 *>(a.x + (size_t)t * H + kGroup * gh);
-#pragma unroll
-            for (int q = 0; q < 8; ++q) c[q] = __ldg(xp + q);
-            xgroupb_from_bf16(xg, c);
+            xg_load(xg, s_xp, s_xX, t * GXH + gh);
             xg_tok = t;
           }
           const float gd = seg_sum<GH>(q4_group_dot_b(rp[i].a0, rp[i].a1, xg, rp[i].as, rp[i].ab));
@@ -898,73 +984,99 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
       }
     }
   }
-  // The down rows of each down warp's first pair do not depend on h: their codes are copied
-  // into shared memory now (cp.async, nothing held in registers) and their scales loaded, so
-  // the traffic is in flight across the barrier.  Warp 0, whose thread 0 arrives at the grid
-  // barrier, takes no pair.
+  // Down tasks (pair pr, row-step qi) -> j = pr * nq_cta + qi.  The first kFusedSlots are
+  // split into contiguous runs, one per warp (neighbouring tasks share the pair, so a warp
+  // prepares few h vectors); their codes and scales do not depend on h and are copied into
+  // shared memory now (cp.async, nothing held in registers), so the traffic is in flight
+  // across the barrier.  Warp w takes the rest, j = nstaged + w + kFusedWarps i, in phase C.
   const int P = s_ubase[U];  // routed pairs, then the shared expert's T pairs
-  constexpr int kDownWarps = kFusedWarps - 1;
-  uint8_t *s_dn = reinterpret_cast<uint8_t *>(s_h) + fused_dn_offset(P, I);
-  float dsv[kFusedMaxQ], dbv[kFusedMaxQ];
-  if (warp >= 1 && warp - 1 < P) {
-    const int e = s_pair_e[warp - 1];
-    const bool sh = (e == E);
-    const lily_q4_mat &m = sh ? a.sh_down : a.down;
-    const size_t ee = sh ? 0 : (size_t)e;
+  const int nq_cta = (nquads - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x;
+  const int ntask_c = P * nq_cta;
+  const int nstaged = min(ntask_c, kFusedSlots);
+  const int jlo = warp * nstaged / kFusedWarps, jhi = (warp + 1) * nstaged / kFusedWarps;
 #pragma unroll
-    for (int qi = 0; qi < kFusedMaxQ; ++qi) {
-      dsv[qi] = dbv[qi] = 0.f;
-      if (qi < nq_cta) {
-        const int row = (blockIdx.x + qi * gridDim.x) * RPS_I + ri;
-        const size_t wo = (ee * H + row) * (GI * 8) + 8 * gi, so = (ee * H + row) * GI + gi;
-        const uint32_t dst =
-            tc::smem_u32(s_dn + ((size_t)(warp * kFusedMaxQ + qi) * 32 + lane) * 32);
-        tc::cp_async16(dst, m.w + wo, 16);
-        tc::cp_async16(dst + 16, m.w + wo + 4, 16);
-        dsv[qi] = bf16f(ld_u16(m.s + so));
-        dbv[qi] = bf16f(ld_u16(m.b + so));
-      }
+  for (int i = 0; i < kFusedStaged; ++i) {
+    const int j = jlo + i;
+    if (j < jhi) {
+      const int pr = j / nq_cta, qi = j - pr * nq_cta;
+      const int e = s_pair_e[pr];
+      const bool sh = (e == E);
+      const lily_q4_mat &m = sh ? a.sh_down : a.down;
+      const size_t ee = sh ? 0 : (size_t)e;
+      const int row = (blockIdx.x + qi * gridDim.x) * RPS_I + ri;
+      const size_t wo = (ee * H + row) * (GI * 8) + 8 * gi;
+      const uint32_t dst = tc::smem_u32(s_dn + ((size_t)j * 32 + lane) * 32);
+      tc::cp_async16(dst, m.w + wo, 16);
+      tc::cp_async16(dst + 16, m.w + wo + 4, 16);
+      if (gi < 2)
+        cp_async_row_scales<GI>(tc::smem_u32(s_dsc + j * 64 + gi * 32 + ri * GI),
+                                (gi ? m.b : m.s) + (ee * H + row) * GI);
     }
   }
   tc::cp_async_commit();
-  if (!grid_barrier(w.hdr, bbase + 2ull * gridDim.x, &s_abort)) return;
+  if (!grid_barrier(w.hdr, bbase + 2ull * gridDim.x, &s_abort)) {
+    tc::cp_async_wait_all();  // no copy may land after the block has left
+    return;
+  }
 
   // ------------------------------------------------------------------ phase C
-  stage_rows(reinterpret_cast<float *>(s_h), reinterpret_cast<const float *>(h16), P * I / 2);
+  // h of every pair, prepared in shared memory; block b owns down row-steps b, b + grid, ...;
+  // partials meet in shared memory and are summed per token in a fixed order (deterministic)
+  const FusedLayout LP = fused_layout(P, T, H, I);
+  uint32_t *s_hp = reinterpret_cast<uint32_t *>(fsm + LP.hp);
+  float *s_hX = reinterpret_cast<float *>(fsm + LP.hX);
+  xg_stage<false>(s_hp, s_hX, h16, P * I / 8, nullptr);
+  tc::cp_async_wait_all();
   __syncthreads();
   constexpr int ROWS = kFusedMaxQ * RPS_I;  // rows of this block, at most
   __shared__ float s_part[kFusedMaxT * (kMaxK + 1)][ROWS];
-  for (int pr = warp - 1; warp >= 1 && pr < P; pr += kDownWarps) {
-    DownRow dr[kFusedMaxQ];
-    if (pr == warp - 1) {
-      tc::cp_async_wait_all();
-      __syncwarp();
-#pragma unroll
-      for (int qi = 0; qi < kFusedMaxQ; ++qi) {
-        const uint4 *c =
-            reinterpret_cast<const uint4 *>(s_dn + ((size_t)(warp * kFusedMaxQ + qi) * 32 + lane) * 32);
-        dr[qi].w0 = c[0];
-        dr[qi].w1 = c[1];
-        dr[qi].s = dsv[qi];
-        dr[qi].b = dbv[qi];
-      }
-    } else {
-      load_down_rows<GI>(a, s_pair_e[pr], nq_cta, ri, gi, dr);
-    }
+  {
+    int cur = -1;  // pair whose h is in xg
     XGroupB xg;
-    {
-      uint4 c[8];
-      const uint4 *hp = reinterpret_cast<const uint4 *>(s_h + (size_t)pr * I + kGroup * gi);
-#pragma unroll
-      for (int q = 0; q < 8; ++q) c[q] = hp[q];
-      xgroupb_from_bf16(xg, c);
+    float pw = 0.f;
+#pragma unroll 1
+    for (int j = jlo; j < jhi; ++j) {
+      const int pr = j / nq_cta, qi = j - pr * nq_cta;
+      if (pr != cur) {
+        xg_load(xg, s_hp, s_hX, pr * GXI + gi);
+        pw = s_pair_w[pr];
+        cur = pr;
+      }
+      const uint4 *c = reinterpret_cast<const uint4 *>(s_dn + ((size_t)j * 32 + lane) * 32);
+      const float sv = bf16f(s_dsc[j * 64 + lane]), bv = bf16f(s_dsc[j * 64 + 32 + lane]);
+      const float dd = seg_sum<GI>(q4_group_dot_b(c[0], c[1], xg, sv, bv));
+      if (gi == 0) s_part[pr][qi * RPS_I + ri] = pw * dd;
     }
-    const float pw = s_pair_w[pr];
+    // tasks beyond the staged ones (batch above one token): from global memory, kFusedMaxQ
+    // at a time with all of their loads issued first
+    for (int j0 = nstaged + warp; j0 < ntask_c; j0 += kFusedMaxQ * kFusedWarps) {
+      DownRow dr[kFusedMaxQ];
 #pragma unroll
-    for (int qi = 0; qi < kFusedMaxQ; ++qi) {
-      if (qi < nq_cta) {
-        const float dd = seg_sum<GI>(q4_group_dot_b(dr[qi].w0, dr[qi].w1, xg, dr[qi].s, dr[qi].b));
-        if (gi == 0) s_part[pr][qi * RPS_I + ri] = pw * dd;
+      for (int q = 0; q < kFusedMaxQ; ++q) {
+        const int j = j0 + q * kFusedWarps;
+        if (j < ntask_c) {
+          const int pr = j / nq_cta, qi = j - pr * nq_cta;
+          const int e = s_pair_e[pr];
+          const int row = (blockIdx.x + qi * gridDim.x) * RPS_I + ri;
+          if (e == E)
+            load_down_mat<GI>(a.sh_down, 0, row, H, gi, dr[q]);
+          else
+            load_down_mat<GI>(a.down, e, row, H, gi, dr[q]);
+        }
+      }
+#pragma unroll
+      for (int q = 0; q < kFusedMaxQ; ++q) {
+        const int j = j0 + q * kFusedWarps;
+        if (j < ntask_c) {
+          const int pr = j / nq_cta, qi = j - pr * nq_cta;
+          if (pr != cur) {
+            xg_load(xg, s_hp, s_hX, pr * GXI + gi);
+            pw = s_pair_w[pr];
+            cur = pr;
+          }
+          const float dd = seg_sum<GI>(q4_group_dot_b(dr[q].w0, dr[q].w1, xg, dr[q].s, dr[q].b));
+          if (gi == 0) s_part[pr][qi * RPS_I + ri] = pw * dd;
+        }
       }
     }
   }
@@ -981,9 +1093,12 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
 }
 
 static bool fused_ok(const lily_q4_moe_layer &L, int T) {
-  const int P = T * L.top_k + (L.has_shared ? T : 0);
-  if (fused_dn_offset(P, L.inter) + kFusedDnStage > kFusedSmemMax) return false;
   if (T > kFusedMaxT) return false;
+  const int P = T * L.top_k + (L.has_shared ? T : 0);
+  if (fused_layout(P, T, L.hidden, L.inter).total > kFusedSmemMax) return false;
+  // x and h are prepared with at most kFusedMaxLoads 16-byte loads per thread
+  const size_t nload = (size_t)kFusedMaxLoads * kFusedThreads;
+  if ((size_t)T * L.hidden / 8 > nload || (size_t)P * L.inter / 8 > nload) return false;
   const int GH = L.hidden / kGroup, GI = L.inter / kGroup;
   // each block owns at most kFusedMaxQ down row-steps
   if (L.hidden / (32 / GI) > sm_count() * kFusedMaxQ) return false;
@@ -1067,7 +1182,7 @@ int launch_moe_decode(const lily_q4_moe_layer &L, const uint16_t *x, int T, uint
     FusedArgs fa{L.gate, L.up, L.down, L.sh_gate, L.sh_up, L.sh_down, L.router, L.router_bias,
                  L.shared_gate, x, y, T, L.n_experts, L.hidden, L.inter, L.top_k, L.has_shared,
                  topk_idx, topk_w};
-    const size_t smem = fused_dn_offset(l.P, L.inter) + kFusedDnStage;
+    const size_t smem = fused_layout(l.P, T, L.hidden, L.inter).total;
     if (L.hidden / kGroup == 32) {
       if (L.n_experts <= 256) return launch_fused<32, 8, 8>(fa, p, smem, st);
       if (L.n_experts <= 512) return launch_fused<32, 8, 16>(fa, p, smem, st);
