@@ -29,6 +29,11 @@
  *  - LM head with greedy argmax (Lily README first paragraph "always decodes
  *    greedily"; report "Measurement contract": greedy token selection without
  *    logprobs): fp64 logits, argmax with ties to the lower id.
+ *  - Full-vocabulary log-sum-exp and log-probabilities of those logits (report
+ *    "Measurement contract": the MLX path computes "full-vocabulary
+ *    log-sum-exp/logprobs"): lse = log sum_n exp(l_n), logprob_n = l_n - lse,
+ *    in fp64 (the sum is taken after subtracting the maximum, which changes
+ *    nothing mathematically).
  *
  * Parallelism: OpenMP only splits independent output rows / tokens across
  * threads; every dot product is summed in plain k order by one thread.
@@ -138,6 +143,28 @@ int orc_lm_head(const uint32_t *w, const uint16_t *s, const uint16_t *b,
     for (int n = 1; n < N; ++n)
         if (logits[n] > logits[best]) best = n;
     return best;
+}
+
+/* lse = log(sum_n exp(l[n])) over n < N, and logprob[n] = l[n] - lse when logprob is
+ * not NULL.  A NaN logit gives NaN; a +inf logit gives +inf; all -inf gives -inf. */
+double orc_log_sum_exp(const double *l, int N, double *logprob) {
+    double m = -INFINITY;
+    int nan = 0;
+    for (int n = 0; n < N; ++n) {
+        if (l[n] != l[n]) nan = 1;
+        else if (l[n] > m) m = l[n];
+    }
+    double lse;
+    if (nan) lse = NAN;
+    else if (isinf(m)) lse = m;
+    else {
+        double sum = 0.0;
+        for (int n = 0; n < N; ++n) sum += exp(l[n] - m);
+        lse = m + log(sum);
+    }
+    if (logprob)
+        for (int n = 0; n < N; ++n) logprob[n] = l[n] - lse;
+    return lse;
 }
 
 /* Router logits for one token. */

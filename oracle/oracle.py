@@ -60,6 +60,8 @@ def lib():
         L.orc_q4_matvec.argtypes = [vp, vp, vp, i32, i32, vp, vp]
         L.orc_lm_head.argtypes = [vp, vp, vp, i32, i32, vp, vp]
         L.orc_lm_head.restype = i32
+        L.orc_log_sum_exp.argtypes = [vp, i32, vp]
+        L.orc_log_sum_exp.restype = C.c_double
         L.orc_router.argtypes = [vp, vp, i32, i32, vp, vp]
         L.orc_topk.argtypes = [vp, i32, i32, vp, vp]
         L.orc_sigmoid_gate.argtypes = [vp, i32, vp]
@@ -134,6 +136,14 @@ def lm_head(m, x_bits: np.ndarray) -> Tuple[int, np.ndarray]:
     logits = np.empty(N, dtype=np.float64)
     tok = lib().orc_lm_head(_p(w), _p(s), _p(b), N, K, _p(x), _p(logits))
     return int(tok), logits
+
+
+def log_softmax(logits: np.ndarray) -> Tuple[float, np.ndarray]:
+    """Full-vocabulary log-sum-exp of fp64 logits and the log-probabilities l - lse."""
+    l = _c(logits, np.float64)
+    out = np.empty_like(l)
+    lse = lib().orc_log_sum_exp(_p(l), int(l.size), _p(out))
+    return float(lse), out
 
 
 def lm_head_rows(m, x_bits: np.ndarray, rows: np.ndarray) -> np.ndarray:

@@ -333,3 +333,44 @@ def test_lm_head_matches_matvec():
     want = orc.q4_matvec(m, bf16_to_f32(x).astype(np.float64))
     assert np.array_equal(lg, want)
     assert tok == int(np.argmax(want))
+
+
+# ----------------------------------------------------------------------------- log-sum-exp
+
+def test_lse_uniform_closed_form():
+    """N equal logits c: lse = c + log N, every logprob = -log N (catches returning the max
+    alone, or forgetting to add the maximum back)."""
+    for N, c in ((1, 0.0), (7, 2.5), (151936, -3.25)):
+        lse, lp = orc.log_softmax(np.full(N, c))
+        assert lse == pytest.approx(c + math.log(N), rel=0, abs=1e-12)
+        assert np.allclose(lp, -math.log(N), rtol=0, atol=1e-12)
+
+
+def test_lse_two_values_closed_form():
+    """lse(a, b) = max + log1p(exp(-|a - b|)) (catches a dropped term of the sum)."""
+    for a, b in ((0.0, 0.0), (3.0, -1.0), (-2.0, 5.5), (700.0, 699.0)):
+        lse, _ = orc.log_softmax(np.array([a, b]))
+        assert lse == pytest.approx(max(a, b) + math.log1p(math.exp(-abs(a - b))), rel=1e-15)
+
+
+def test_lse_matches_library_and_normalises():
+    """Random logits: scipy's logsumexp agrees, exp(logprobs) sums to one and the shift by a
+    constant moves lse by that constant (catches a wrong sign or a missing shift)."""
+    rng = np.random.default_rng(5)
+    l = rng.normal(0.0, 4.0, 5000)
+    lse, lp = orc.log_softmax(l)
+    assert lse == pytest.approx(float(sp.logsumexp(l)), rel=1e-14)
+    assert math.fsum(np.exp(lp)) == pytest.approx(1.0, abs=1e-12)
+    lse2, lp2 = orc.log_softmax(l + 123.0)
+    assert lse2 == pytest.approx(lse + 123.0, rel=1e-14)
+    assert np.allclose(lp2, lp, rtol=0, atol=1e-10)
+    assert np.all(lp <= 0.0) and lp.argmax() == l.argmax()
+
+
+def test_lse_non_finite():
+    inf, nan = math.inf, math.nan
+    assert orc.log_softmax(np.array([0.0, inf, 1.0]))[0] == inf
+    assert orc.log_softmax(np.array([-inf, -inf]))[0] == -inf
+    assert math.isnan(orc.log_softmax(np.array([0.0, nan, 1.0]))[0])
+    lse, lp = orc.log_softmax(np.array([-inf, 0.0]))   # a -inf logit adds nothing
+    assert lse == 0.0 and lp[0] == -inf
