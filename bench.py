@@ -289,6 +289,34 @@ def run_gb300(args):
             y_host.copy_(ydev, non_blocking=True)
         stream.synchronize()
 
+    # ---- LM head with the full-vocabulary log-sum-exp and log-probabilities (one graph replay
+    # per timing; the same weights and x as the argmax-only LM head above)
+    lse_d = torch.empty(1, dtype=torch.float32, device=dev)
+    lp_d = torch.empty(lmw.V, dtype=torch.float32, device=dev)
+
+    def lp_part():
+        q4.lily_q4_gemv_argmax_logprobs(W, xl, tok, lse_d, logprobs=lp_d, ws=lmws, stream=stream)
+
+    with torch.cuda.stream(stream):
+        lp_part()
+    stream.synchronize()
+    g_lp = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_lp, stream=stream):
+        lp_part()
+    lp_ms = []
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            g_lp.replay()
+        for _ in range(max(args.steps, 3)):
+            a0 = torch.cuda.Event(enable_timing=True)
+            a1 = torch.cuda.Event(enable_timing=True)
+            a0.record(stream)
+            g_lp.replay()
+            a1.record(stream)
+            a1.synchronize()
+            lp_ms.append(a0.elapsed_time(a1))
+    lp_mean = max_over_ranks([statistics.mean(lp_ms)], dev)[0]
+
     e2e_val = None
     if not args.no_e2e:
         for _ in range(2):
@@ -326,7 +354,8 @@ def run_gb300(args):
                    "bytes_per_layer": int(bytes_per_layer), "hbm_gbs": round(dec_gbs, 1),
                    "frac_of_measured_hbm": round(dec_gbs / pk["hbm_gbs"], 4)},
         "lm_head": {"us": round(lm_mean * 1e3, 2), "bytes": lm_bytes,
-                    "hbm_gbs": round(lm_gbs, 1), "frac_of_measured_hbm": round(lm_gbs / pk["hbm_gbs"], 4)},
+                    "hbm_gbs": round(lm_gbs, 1), "frac_of_measured_hbm": round(lm_gbs / pk["hbm_gbs"], 4),
+                    "with_logprobs_us": round(lp_mean * 1e3, 2)},
         "prefill": {"us": round(pf_mean * 1e3, 1), "gflop": round(pf_flops / 1e9, 2),
                     "tflops": round(pf_tflops, 1),
                     "frac_of_measured_bf16": round(pf_tflops / pk["bf16_tflops_sustained"], 4),

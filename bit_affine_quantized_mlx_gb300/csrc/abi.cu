@@ -157,6 +157,18 @@ int lily_q4_gemv_argmax(const lily_q4_mat *W, int32_t N, int32_t K, const uint16
   return launch_gemv_argmax(*W, N, K, x, token, logits, ws, (cudaStream_t)stream);
 }
 
+int lily_q4_gemv_argmax_logprobs(const lily_q4_mat *W, int32_t N, int32_t K, const uint16_t *x,
+                                 int32_t *token, float *lse, float *logprobs, void *ws,
+                                 size_t ws_bytes, lily_q4_stream_t stream) {
+  if (!W || !mat_ok(*W) || N <= 0 || K <= 0 || K % LILY_Q4_GROUP) return LILY_Q4_ERR_INVALID_ARG;
+  if (!x || !aligned(x, 16) || !token || !aligned(token, 4)) return LILY_Q4_ERR_INVALID_ARG;
+  if (!lse || !aligned(lse, 4) || (logprobs && !aligned(logprobs, 4))) return LILY_Q4_ERR_INVALID_ARG;
+  if (!ws || !aligned(ws, kAlign)) return LILY_Q4_ERR_INVALID_ARG;
+  if (!width_ok(K)) return LILY_Q4_ERR_UNSUPPORTED;
+  if (ws_bytes < lm_ws_layout(N, K).total) return LILY_Q4_ERR_WORKSPACE_TOO_SMALL;
+  return launch_gemv_argmax(*W, N, K, x, token, logprobs, ws, (cudaStream_t)stream, lse);
+}
+
 int lily_q4_moe_decode(const lily_q4_moe_layer *layer, const uint16_t *x, int32_t T,
                        uint16_t *y, int32_t *topk_idx, float *topk_w, void *ws,
                        size_t ws_bytes, lily_q4_stream_t stream) {

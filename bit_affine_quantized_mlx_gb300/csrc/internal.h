@@ -23,13 +23,18 @@ enum HeaderWord : int {
 
 // ---------------------------------------------------------------- LM head
 struct LmWsLayout {
-  size_t off_partial_v, off_partial_i, total;
+  size_t off_partial_v, off_partial_i;
+  size_t total_argmax;                  // bytes the argmax-only call needs
+  size_t off_partial_m, off_partial_s;  // per-block (max, sum of exp) for the log-sum-exp
+  size_t total;                         // bytes either call needs
   int grid;
   int rows_per_block;  // streaming kernel (K >= 512): contiguous rows per block
 };
 LmWsLayout lm_ws_layout(int N, int K);
+// lse == nullptr: greedy token (and logits) only.  Otherwise also *lse = log sum_n exp(logit[n])
+// and, with logits set, logits[n] - *lse in place of the logits (a second, elementwise launch).
 int launch_gemv_argmax(const lily_q4_mat &W, int N, int K, const uint16_t *x, int32_t *token,
-                       float *logits, void *ws, cudaStream_t st);
+                       float *logits, void *ws, cudaStream_t st, float *lse = nullptr);
 
 // ---------------------------------------------------------------- decode MoE
 struct DecodeWsLayout {

@@ -53,24 +53,83 @@ LmWsLayout lm_ws_layout(int N, int K) {
   off = align_up(off + sizeof(float) * (size_t)sms * kLmBlocksPerSm);
   l.off_partial_i = off;
   off = align_up(off + sizeof(int32_t) * (size_t)sms * kLmBlocksPerSm);
+  l.total_argmax = off;
+  l.off_partial_m = off;
+  off = align_up(off + sizeof(float) * (size_t)sms * kLmBlocksPerSm);
+  l.off_partial_s = off;
+  off = align_up(off + sizeof(float) * (size_t)sms * kLmBlocksPerSm);
   l.total = off;
   return l;
+}
+
+// Running log-sum-exp as (m, s) = (max, sum of exp(v - m)): fold in one value, or merge two
+// partials.  m = -inf means nothing folded in yet (s = 0); a NaN value makes s NaN.
+// (Equal maxima are added without exp, so that +inf values count rather than give NaN.)
+__device__ __forceinline__ void lse_add(float &m, float &s, float v) {
+  if (v > m) {
+    s = s * expf(m - v) + 1.0f;  // exp(-inf) = 0 on the first value
+    m = v;
+  } else if (v == m) {
+    s += 1.0f;
+  } else {
+    s += expf(v - m);
+  }
+}
+__device__ __forceinline__ void lse_merge(float &m, float &s, float m2, float s2) {
+  if (m2 > m) {
+    s = s * expf(m - m2) + s2;
+    m = m2;
+  } else if (m2 == m) {
+    s += s2;
+  } else {
+    s += s2 * expf(m2 - m);  // m2 = -inf: an empty partial adds 0 (or its NaN)
+  }
+}
+template <int W>
+__device__ __forceinline__ void lse_warp(float &m, float &s) {
+#pragma unroll
+  for (int o = W / 2; o > 0; o >>= 1) {
+    const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
+    const float s2 = __shfl_xor_sync(0xffffffffu, s, o);
+    lse_merge(m, s, m2, s2);
+  }
+}
+
+// logprob[n] = logit[n] - lse, in place.
+__global__ void sub_lse_kernel(float *__restrict__ v, int N, const float *__restrict__ lse) {
+  const float l = *lse;
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < N; i += gridDim.x * blockDim.x)
+    v[i] -= l;
 }
 
 // Block-wide then grid-wide argmax of the threads' (value, row) pairs: every block publishes
 // its best pair, and the last block to finish (ticket on header counter A) reduces the pairs
 // into *token and re-arms the counter for the next call.
-template <int NW>
+// With LSE, the threads' (m, s) log-sum-exp partials are reduced alongside, in a fixed order
+// (deterministic), into *lse = m + log(s).
+struct LseOut {
+  float *part_m, *part_s, *lse;
+};
+
+template <int NW, bool LSE = false>
 __device__ __forceinline__ void block_argmax_finish(float best_v, int best_i, int32_t *token,
-                                                    int32_t *hdr, float *part_v, int32_t *part_i) {
+                                                    int32_t *hdr, float *part_v, int32_t *part_i,
+                                                    float lm = -INFINITY, float ls = 0.f,
+                                                    LseOut lo = LseOut{}) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   warp_argmax(best_v, best_i);
   __shared__ float sv_[NW];
   __shared__ int si_[NW];
+  __shared__ float sm_[LSE ? NW : 1], ss_[LSE ? NW : 1];
   __shared__ int is_last;
+  if (LSE) lse_warp<32>(lm, ls);
   if (lane == 0) {
     sv_[warp] = best_v;
     si_[warp] = best_i;
+    if (LSE) {
+      sm_[warp] = lm;
+      ss_[warp] = ls;
+    }
   }
   __syncthreads();
   if (threadIdx.x == 0) {
@@ -83,6 +142,12 @@ __device__ __forceinline__ void block_argmax_finish(float best_v, int best_i, in
       }
     part_v[blockIdx.x] = bv_;
     part_i[blockIdx.x] = bi_;
+    if (LSE) {
+      float m_ = sm_[0], s_ = ss_[0];
+      for (int i = 1; i < NW; ++i) lse_merge(m_, s_, sm_[i], ss_[i]);
+      lo.part_m[blockIdx.x] = m_;
+      lo.part_s[blockIdx.x] = s_;
+    }
     __threadfence();
     const int ticket = atomicAdd(hdr + kHdrCounterA, 1);
     is_last = (ticket == (int)gridDim.x - 1);
@@ -92,6 +157,7 @@ __device__ __forceinline__ void block_argmax_finish(float best_v, int best_i, in
   __threadfence();
   float v = -INFINITY;
   int i = INT_MAX;
+  float m = -INFINITY, sm = 0.f;
   for (int j = threadIdx.x; j < (int)gridDim.x; j += NW * 32) {
     const float pv = __ldcg(part_v + j);
     const int pi = __ldcg(part_i + j);
@@ -99,12 +165,18 @@ __device__ __forceinline__ void block_argmax_finish(float best_v, int best_i, in
       v = pv;
       i = pi;
     }
+    if (LSE) lse_merge(m, sm, __ldcg(lo.part_m + j), __ldcg(lo.part_s + j));
   }
   warp_argmax(v, i);
+  if (LSE) lse_warp<32>(m, sm);
   __syncthreads();
   if (lane == 0) {
     sv_[warp] = v;
     si_[warp] = i;
+    if (LSE) {
+      sm_[warp] = m;
+      ss_[warp] = sm;
+    }
   }
   __syncthreads();
   if (threadIdx.x == 0) {
@@ -116,19 +188,24 @@ __device__ __forceinline__ void block_argmax_finish(float best_v, int best_i, in
         bi_ = si_[j];
       }
     *token = bi_;
+    if (LSE) {
+      float m_ = sm_[0], s_ = ss_[0];
+      for (int j = 1; j < NW; ++j) lse_merge(m_, s_, sm_[j], ss_[j]);
+      *lo.lse = m_ + logf(s_);
+    }
     hdr[kHdrCounterA] = 0;  // leave the counter ready for the next call
   }
 }
 
 // G = groups per row (K/64), U = row-steps per iteration: a warp issues the loads of U
 // row-steps (U*32 bytes of codes per lane) before computing them.
-template <int G, int U>
+template <int G, int U, bool LSE>
 __global__ void __launch_bounds__(kLmThreads, kLmBlocksPerSm)
     gemv_argmax_kernel(const uint32_t *__restrict__ w, const uint16_t *__restrict__ s,
                        const uint16_t *__restrict__ b, int N, const uint16_t *__restrict__ x,
                        float *__restrict__ logits, int32_t *__restrict__ token,
                        int32_t *__restrict__ hdr, float *__restrict__ part_v,
-                       int32_t *__restrict__ part_i) {
+                       int32_t *__restrict__ part_i, LseOut lo) {
   constexpr int RPS = 32 / G;  // rows per warp-step
   constexpr int K8 = G * 8;    // words per row
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -145,6 +222,7 @@ __global__ void __launch_bounds__(kLmThreads, kLmBlocksPerSm)
 
   float best_v = -INFINITY;
   int best_i = INT_MAX;
+  float lm = -INFINITY, ls = 0.f;  // log-sum-exp partial of this thread's rows
   const int gwarp = blockIdx.x * kLmWarps + warp;
   const int nwarps = gridDim.x * kLmWarps;
   constexpr int RPI = RPS * U;  // rows per warp-iteration
@@ -174,6 +252,7 @@ __global__ void __launch_bounds__(kLmThreads, kLmBlocksPerSm)
       const int row = r0 + u * RPS + rsub;
       if (g == 0 && row < N) {
         if (logits) logits[row] = d;
+        if (LSE) lse_add(lm, ls, d);
         if (better(dc, row, best_v, best_i)) {
           best_v = dc;
           best_i = row;
@@ -181,7 +260,7 @@ __global__ void __launch_bounds__(kLmThreads, kLmBlocksPerSm)
       }
     }
   }
-  block_argmax_finish<kLmWarps>(best_v, best_i, token, hdr, part_v, part_i);
+  block_argmax_finish<kLmWarps, LSE>(best_v, best_i, token, hdr, part_v, part_i, lm, ls, lo);
 }
 
 // ---------------------------------------------------------------------------------------
@@ -205,13 +284,14 @@ struct LsCfg {
   static_assert(G >= 8 && WR * kLsWarps * RPS == SR && STAGE % 128 == 0, "stage shape");
 };
 
-template <int G>
+template <int G, bool LSE>
 __global__ void __launch_bounds__(kLsThreads, 1)
     gemv_argmax_stream_kernel(const uint32_t *__restrict__ w, const uint16_t *__restrict__ s,
                               const uint16_t *__restrict__ b, int N, int rows_per_block,
                               const uint16_t *__restrict__ x, float *__restrict__ logits,
                               int32_t *__restrict__ token, int32_t *__restrict__ hdr,
-                              float *__restrict__ part_v, int32_t *__restrict__ part_i) {
+                              float *__restrict__ part_v, int32_t *__restrict__ part_i,
+                              LseOut lo) {
   using C = LsCfg<G>;
   extern __shared__ __align__(128) uint8_t ls_smem[];
   __shared__ volatile int s_abort;
@@ -236,6 +316,7 @@ __global__ void __launch_bounds__(kLsThreads, 1)
 
   float best_v = -INFINITY;
   int best_i = INT_MAX;
+  float lm = -INFINITY, ls = 0.f;  // log-sum-exp partial of this thread's rows
   if (warp == kLsWarps) {
     // ---------------------------------------------------------------- copy thread
     if (lane == 0) {
@@ -310,6 +391,7 @@ __global__ void __launch_bounds__(kLsThreads, 1)
         if (g == 0 && lr < rows) {
           const int row = r0 + lr;
           if (logits) logits[row] = d;
+          if (LSE) lse_add(lm, ls, d);
           const float dc = cand(d);
           if (better(dc, row, best_v, best_i)) {
             best_v = dc;
@@ -319,40 +401,58 @@ __global__ void __launch_bounds__(kLsThreads, 1)
       }
     }
   }
-  block_argmax_finish<kLsWarps + 1>(best_v, best_i, token, hdr, part_v, part_i);
+  block_argmax_finish<kLsWarps + 1, LSE>(best_v, best_i, token, hdr, part_v, part_i, lm, ls, lo);
 }
 
-template <int G>
+template <int G, bool LSE>
 static void launch_g(const lily_q4_mat &W, int N, const uint16_t *x, int32_t *token,
-                     float *logits, void *ws, const LmWsLayout &l, cudaStream_t st) {
+                     float *logits, void *ws, const LmWsLayout &l, cudaStream_t st, float *lse) {
   char *base = static_cast<char *>(ws);
   int32_t *hdr = reinterpret_cast<int32_t *>(base);
   float *pv = reinterpret_cast<float *>(base + l.off_partial_v);
   int32_t *pi = reinterpret_cast<int32_t *>(base + l.off_partial_i);
+  const LseOut lo = LSE ? LseOut{reinterpret_cast<float *>(base + l.off_partial_m),
+                                 reinterpret_cast<float *>(base + l.off_partial_s), lse}
+                        : LseOut{};
   if constexpr (G >= 8) {
     using C = LsCfg<G>;
     // set on every call: cheap, and correct for whichever device is current
-    cudaFuncSetAttribute(gemv_argmax_stream_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         C::BYTES);
-    gemv_argmax_stream_kernel<G><<<l.grid, kLsThreads, C::BYTES, st>>>(
-        W.w, W.s, W.b, N, l.rows_per_block, x, logits, token, hdr, pv, pi);
+    cudaFuncSetAttribute(gemv_argmax_stream_kernel<G, LSE>,
+                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::BYTES);
+    gemv_argmax_stream_kernel<G, LSE><<<l.grid, kLsThreads, C::BYTES, st>>>(
+        W.w, W.s, W.b, N, l.rows_per_block, x, logits, token, hdr, pv, pi, lo);
   } else {
-    gemv_argmax_kernel<G, (G >= 16 ? 8 : 4)><<<l.grid, kLmThreads, 0, st>>>(
-        W.w, W.s, W.b, N, x, logits, token, hdr, pv, pi);
+    gemv_argmax_kernel<G, (G >= 16 ? 8 : 4), LSE><<<l.grid, kLmThreads, 0, st>>>(
+        W.w, W.s, W.b, N, x, logits, token, hdr, pv, pi, lo);
   }
 }
 
-int launch_gemv_argmax(const lily_q4_mat &W, int N, int K, const uint16_t *x, int32_t *token,
-                       float *logits, void *ws, cudaStream_t st) {
-  const LmWsLayout l = lm_ws_layout(N, K);
+template <bool LSE>
+static int launch_k(const lily_q4_mat &W, int N, int K, const uint16_t *x, int32_t *token,
+                    float *logits, void *ws, const LmWsLayout &l, cudaStream_t st, float *lse) {
   switch (K / kGroup) {
-    case 1: launch_g<1>(W, N, x, token, logits, ws, l, st); break;
-    case 2: launch_g<2>(W, N, x, token, logits, ws, l, st); break;
-    case 4: launch_g<4>(W, N, x, token, logits, ws, l, st); break;
-    case 8: launch_g<8>(W, N, x, token, logits, ws, l, st); break;
-    case 16: launch_g<16>(W, N, x, token, logits, ws, l, st); break;
-    case 32: launch_g<32>(W, N, x, token, logits, ws, l, st); break;
+    case 1: launch_g<1, LSE>(W, N, x, token, logits, ws, l, st, lse); break;
+    case 2: launch_g<2, LSE>(W, N, x, token, logits, ws, l, st, lse); break;
+    case 4: launch_g<4, LSE>(W, N, x, token, logits, ws, l, st, lse); break;
+    case 8: launch_g<8, LSE>(W, N, x, token, logits, ws, l, st, lse); break;
+    case 16: launch_g<16, LSE>(W, N, x, token, logits, ws, l, st, lse); break;
+    case 32: launch_g<32, LSE>(W, N, x, token, logits, ws, l, st, lse); break;
     default: return LILY_Q4_ERR_UNSUPPORTED;
+  }
+  return LILY_Q4_OK;
+}
+
+int launch_gemv_argmax(const lily_q4_mat &W, int N, int K, const uint16_t *x, int32_t *token,
+                       float *logits, void *ws, cudaStream_t st, float *lse) {
+  const LmWsLayout l = lm_ws_layout(N, K);
+  const int rc = lse ? launch_k<true>(W, N, K, x, token, logits, ws, l, st, lse)
+                     : launch_k<false>(W, N, K, x, token, logits, ws, l, st, lse);
+  if (rc != LILY_Q4_OK) return rc;
+  if (lse && logits) {
+    int sms = sm_count();
+    if (sms <= 0) sms = 152;
+    const int want = (N + 1023) / 1024;
+    sub_lse_kernel<<<want < 4 * sms ? want : 4 * sms, 256, 0, st>>>(logits, N, lse);
   }
   return check_launch();
 }
@@ -401,7 +501,7 @@ extern "C" int lily_q4_gemv_argmax_noalloc(const lily_q4_mat *W, int32_t N, int3
   if (!x || !al(x, 16) || !token || !al(token, 4) || (logits && !al(logits, 4)))
     return LILY_Q4_ERR_INVALID_ARG;
   if (K > 2048 || (K & (K - 1))) return LILY_Q4_ERR_UNSUPPORTED;
-  if (lm_ws_layout(N, K).total > kNoAllocScratchBytes) return LILY_Q4_ERR_WORKSPACE_TOO_SMALL;
+  if (lm_ws_layout(N, K).total_argmax > kNoAllocScratchBytes) return LILY_Q4_ERR_WORKSPACE_TOO_SMALL;
   void *scratch = nullptr;
   int rc = noalloc_scratch(&scratch);
   if (rc != LILY_Q4_OK) return rc;

@@ -140,6 +140,25 @@ LILY_Q4_API int lily_q4_gemv_argmax(const lily_q4_mat *W, int32_t N, int32_t K, 
                         lily_q4_stream_t stream);
 
 /*
+ * lily_q4_gemv_argmax_logprobs -- lily_q4_gemv_argmax plus the full-vocabulary
+ * log-sum-exp and, optionally, the log-probability vector, in the same pass over W
+ * (the MLX path of the Lily-vs-MLX report, "Measurement contract", computes both for
+ * every prompt: "full-vocabulary log-sum-exp/logprobs").
+ *   token = argmax_n logit[n] (as lily_q4_gemv_argmax),
+ *   *lse = log sum_n exp(logit[n]) (fp32; running max and sum of exp, merged in a fixed
+ *   order, so repeated calls give identical bits),
+ *   logprobs[n] = logit[n] - *lse when logprobs is not NULL.
+ * lse: fp32 [1] device output (required).  logprobs: fp32 [N] device output, or NULL; it
+ * is written in a second, elementwise launch on `stream`.  Non-finite logits: +inf
+ * gives lse = +inf, NaN gives NaN.  The workspace is that of lily_q4_gemv_argmax
+ * (lily_q4_gemv_argmax_workspace_bytes covers both calls); errors as there.
+ */
+LILY_Q4_API int lily_q4_gemv_argmax_logprobs(const lily_q4_mat *W, int32_t N, int32_t K,
+                                             const uint16_t *x, int32_t *token, float *lse,
+                                             float *logprobs, void *ws, size_t ws_bytes,
+                                             lily_q4_stream_t stream);
+
+/*
  * lily_q4_gemv_argmax_noalloc -- lily_q4_gemv_argmax for callers that cannot allocate.
  *
  * The paper has no counterpart: this entry point exists for callers that cannot call

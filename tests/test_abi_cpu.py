@@ -117,6 +117,24 @@ def test_gemv_argument_errors(lib):
     assert f(C.byref(m), 10, 2048, FAKE, FAKE, None, ws, 16, None) == q4.ERR_WORKSPACE_TOO_SMALL
 
 
+def test_gemv_logprobs_argument_errors(lib):
+    m = q4.lily_q4_mat(FAKE, FAKE + 4096, FAKE + 8192)
+    f = lib.lily_q4_gemv_argmax_logprobs
+    ws, big = FAKE + (1 << 30), 1 << 20
+    lse, lp = FAKE + 512, FAKE + (1 << 24)
+    INV = q4.ERR_INVALID_ARG
+    assert f(None, 10, 2048, FAKE, FAKE, lse, lp, ws, big, None) == INV
+    assert f(C.byref(m), 10, 2048, FAKE, FAKE, None, lp, ws, big, None) == INV      # lse required
+    assert f(C.byref(m), 10, 2048, FAKE, FAKE, lse + 2, lp, ws, big, None) == INV   # misaligned
+    assert f(C.byref(m), 10, 2048, FAKE, FAKE, lse, lp + 2, ws, big, None) == INV
+    assert f(C.byref(m), 10, 2048, FAKE, None, lse, lp, ws, big, None) == INV
+    assert f(C.byref(m), 10, 4096, FAKE, FAKE, lse, lp, ws, big, None) == q4.ERR_UNSUPPORTED
+    # the logprobs call needs the per-block log-sum-exp partials on top of the argmax pairs
+    n = lib.lily_q4_gemv_argmax_workspace_bytes(151936, 2048)
+    assert f(C.byref(m), 151936, 2048, FAKE, FAKE, lse, None, ws, n - 256, None) == \
+        q4.ERR_WORKSPACE_TOO_SMALL
+
+
 def test_workspace_sizes(lib):
     L = _fake_layer()
     d1 = lib.lily_q4_moe_workspace_bytes(C.byref(L), 1, 0)

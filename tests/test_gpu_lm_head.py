@@ -101,3 +101,66 @@ def test_all_nan_logits_give_a_real_token(torch_dev):
     x = synth.draw_x(K, (63, 0), 0, 0)
     got_tok, _ = _run(torch, dev, W, x)
     assert got_tok == 0
+
+
+# ----------------------------------------------------------------------------- logprobs
+
+def _run_lp(torch, dev, W, x_bits, with_lp=True):
+    N, K = W.N, W.K
+    dW = q4.DeviceQ4.upload(W, dev)
+    xd = q4.to_device(x_bits, dev)
+    tok = torch.full((1,), -7, dtype=torch.int32, device=dev)
+    lse = torch.full((1,), float("nan"), dtype=torch.float32, device=dev)
+    lp = torch.empty(N, dtype=torch.float32, device=dev) if with_lp else None
+    ws = q4.new_workspace(q4.lily_q4_gemv_argmax_workspace_bytes(N, K), dev)
+    q4.lily_q4_gemv_argmax_logprobs(dW, xd, tok, lse, logprobs=lp, ws=ws)
+    torch.cuda.synchronize()
+    return (int(tok.item()), float(lse.item()),
+            lp.cpu().numpy().astype(np.float64) if with_lp else None)
+
+
+def _check_lp(got, tok, lg, what):
+    """Token identical; logprobs within the output tolerance; lse within the largest logit
+    error (log-sum-exp moves by at most the largest change of any logit) plus 1e-4 for the
+    fp32 sum of exponentials; the returned logprobs normalise."""
+    got_tok, got_lse, got_lp = got
+    lse, lp = orc.log_softmax(lg)
+    assert got_tok == tok, what
+    assert_close(got_lp, lp, f"logprobs {what}")
+    logit_err = np.abs((got_lp + got_lse) - lg).max()
+    assert abs(got_lse - lse) <= logit_err + 1e-4 + 1e-6 * abs(lse), (what, got_lse, lse)
+    import scipy.special as sp
+    assert abs(float(sp.logsumexp(got_lp))) <= 1e-4, what
+
+
+@pytest.mark.parametrize("N,K", [(1, 64), (37, 128), (1000, 256), (4097, 512), (7297, 2048)])
+def test_logprobs_shapes(torch_dev, N, K):
+    torch, dev = torch_dev
+    W = synth.draw_q4(N, K, 64, N, K)
+    if N == 1:
+        x = synth.draw_x(K, (64, N), 0, 0)
+        tok, lg = orc.lm_head(W, x)
+    else:
+        x, _, tok, lg = orc.lm_x_without_near_tie(W, lambda a: synth.draw_x(K, (64, N), 0, a))
+    got = _run_lp(torch, dev, W, x)
+    _check_lp(got, tok, lg, f"N={N} K={K}")
+    if N == 1:
+        assert got[2][0] == 0.0  # one row: lse is the logit itself
+    # lse alone (no vector): same token and the same lse bits
+    t2, lse2, _ = _run_lp(torch, dev, W, x, with_lp=False)
+    assert t2 == got[0] and lse2 == got[1]
+
+
+def test_logprobs_full_size(torch_dev):
+    """Vocabulary 151,936 x hidden 2048: every log-probability checked against the oracle,
+    and two calls give identical bits."""
+    torch, dev = torch_dev
+    wl = synth.LMHEAD
+    W = synth.draw_lm_head(wl.V, wl.H)
+    x, attempt, tok, lg = orc.lm_x_without_near_tie(W, lambda a: synth.draw_lm_x(wl.H, attempt=a))
+    a = _run_lp(torch, dev, W, x)
+    _check_lp(a, tok, lg, "full LM head")
+    b = _run_lp(torch, dev, W, x)
+    assert a[0] == b[0] and a[1] == b[1] and np.array_equal(a[2], b[2])
+    # the argmax-only call on the same inputs picks the same token
+    assert _run(torch, dev, W, x, with_logits=False)[0] == tok
