@@ -101,6 +101,27 @@ def test_prefill_workload_full_size_sampled(torch_dev):
     assert_close(y[sample], ref["y"], "prefill full-size sample")
 
 
+def test_prefill_4096_token_chunk_sampled(torch_dev):
+    """The same layer with a 4096-token chunk (the larger chunk size the pages use): every
+    token's routing, and y on a sample of tokens."""
+    torch, dev = torch_dev
+    wl = synth.PREFILL
+    L = wl.layer(0)
+    T = 4096
+    x = _inputs(L, (wl.wid, 4096), T)
+    dl = q4.DeviceLayer.upload(L, dev)
+    y, idx, w = run_prefill(torch, dev, dl, x)
+    lg = orc.router_tokens(L, x)
+    for t in range(T):
+        ref_idx, _ = orc.topk(lg[t], L.k)
+        assert sorted(idx[t].tolist()) == sorted(ref_idx.tolist()), t
+    rng = np.random.default_rng(1)
+    sample = np.sort(rng.choice(T, 64, replace=False))
+    ref = orc.moe(L, x[sample])
+    assert_topk_equal(idx[sample], w[sample], ref, "prefill 4096 sample")
+    assert_close(y[sample], ref["y"], "prefill 4096-token sample")
+
+
 def test_deterministic(torch_dev):
     torch, dev = torch_dev
     key = (82, 0)
