@@ -26,6 +26,7 @@ struct LmWsLayout {
   size_t off_partial_v, off_partial_i;
   size_t total_argmax;                  // bytes the argmax-only call needs
   size_t off_partial_m, off_partial_s;  // per-block (max, sum of exp) for the log-sum-exp
+  size_t off_logits;                    // f32 [N]: logits of a log-sum-exp call without logprobs
   size_t total;                         // bytes either call needs
   int grid;
   int rows_per_block;  // streaming kernel (K >= 512): contiguous rows per block

@@ -58,6 +58,8 @@ LmWsLayout lm_ws_layout(int N, int K) {
   off = align_up(off + sizeof(float) * (size_t)sms * kLmBlocksPerSm);
   l.off_partial_s = off;
   off = align_up(off + sizeof(float) * (size_t)sms * kLmBlocksPerSm);
+  l.off_logits = off;
+  off = align_up(off + sizeof(float) * (size_t)N);
   l.total = off;
   return l;
 }
@@ -85,14 +87,30 @@ __device__ __forceinline__ void lse_merge(float &m, float &s, float m2, float s2
     s += s2 * expf(m2 - m);  // m2 = -inf: an empty partial adds 0 (or its NaN)
   }
 }
-template <int W>
+// Merge the 32 lanes' partials, every lane getting the result: the warp maximum M first
+// (one reduction on the order-preserving key), then each lane's sum rescaled to M with one
+// exp, then a fixed-order butterfly sum -- no chain of dependent exps.
 __device__ __forceinline__ void lse_warp(float &m, float &s) {
+  const float M = key2f(__reduce_max_sync(0xffffffffu, f2key(m)));
+  float t = (m == M) ? s : s * expf(m - M);  // equal maxima (also +-inf) need no rescale
 #pragma unroll
-  for (int o = W / 2; o > 0; o >>= 1) {
-    const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
-    const float s2 = __shfl_xor_sync(0xffffffffu, s, o);
-    lse_merge(m, s, m2, s2);
+  for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+  m = M;
+  s = t;
+}
+
+// Rows' logits reach the log-sum-exp a warp at a time: lane j of the warp buffers the j-th
+// row since the last flush, and every 32 rows all lanes fold their row in at once (one exp
+// per lane instead of one per row on a single lane).  n is the warp-uniform buffer count.
+__device__ __forceinline__ void lse_buffer(float &m, float &s, float &buf, int &n, float v) {
+  if ((int)(threadIdx.x & 31) == n) buf = v;
+  if (++n == 32) {
+    lse_add(m, s, buf);
+    n = 0;
   }
+}
+__device__ __forceinline__ void lse_flush(float &m, float &s, float buf, int n) {
+  if ((int)(threadIdx.x & 31) < n) lse_add(m, s, buf);
 }
 
 // logprob[n] = logit[n] - lse, in place.
@@ -116,13 +134,14 @@ __device__ __forceinline__ void block_argmax_finish(float best_v, int best_i, in
                                                     int32_t *hdr, float *part_v, int32_t *part_i,
                                                     float lm = -INFINITY, float ls = 0.f,
                                                     LseOut lo = LseOut{}) {
+  static_assert(NW <= 32, "one warp merges the warps' partials");
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   warp_argmax(best_v, best_i);
   __shared__ float sv_[NW];
   __shared__ int si_[NW];
   __shared__ float sm_[LSE ? NW : 1], ss_[LSE ? NW : 1];
   __shared__ int is_last;
-  if (LSE) lse_warp<32>(lm, ls);
+  if (LSE) lse_warp(lm, ls);
   if (lane == 0) {
     sv_[warp] = best_v;
     si_[warp] = best_i;
@@ -132,6 +151,14 @@ __device__ __forceinline__ void block_argmax_finish(float best_v, int best_i, in
     }
   }
   __syncthreads();
+  if (LSE && warp == 0) {
+    float m_ = lane < NW ? sm_[lane] : -INFINITY, s_ = lane < NW ? ss_[lane] : 0.f;
+    lse_warp(m_, s_);
+    if (lane == 0) {
+      lo.part_m[blockIdx.x] = m_;
+      lo.part_s[blockIdx.x] = s_;
+    }
+  }
   if (threadIdx.x == 0) {
     float bv_ = sv_[0];
     int bi_ = si_[0];
@@ -142,12 +169,6 @@ __device__ __forceinline__ void block_argmax_finish(float best_v, int best_i, in
       }
     part_v[blockIdx.x] = bv_;
     part_i[blockIdx.x] = bi_;
-    if (LSE) {
-      float m_ = sm_[0], s_ = ss_[0];
-      for (int i = 1; i < NW; ++i) lse_merge(m_, s_, sm_[i], ss_[i]);
-      lo.part_m[blockIdx.x] = m_;
-      lo.part_s[blockIdx.x] = s_;
-    }
     __threadfence();
     const int ticket = atomicAdd(hdr + kHdrCounterA, 1);
     is_last = (ticket == (int)gridDim.x - 1);
@@ -168,7 +189,7 @@ __device__ __forceinline__ void block_argmax_finish(float best_v, int best_i, in
     if (LSE) lse_merge(m, sm, __ldcg(lo.part_m + j), __ldcg(lo.part_s + j));
   }
   warp_argmax(v, i);
-  if (LSE) lse_warp<32>(m, sm);
+  if (LSE) lse_warp(m, sm);
   __syncthreads();
   if (lane == 0) {
     sv_[warp] = v;
@@ -179,6 +200,11 @@ __device__ __forceinline__ void block_argmax_finish(float best_v, int best_i, in
     }
   }
   __syncthreads();
+  if (LSE && warp == 0) {
+    float m_ = lane < NW ? sm_[lane] : -INFINITY, s_ = lane < NW ? ss_[lane] : 0.f;
+    lse_warp(m_, s_);
+    if (lane == 0) *lo.lse = m_ + logf(s_);
+  }
   if (threadIdx.x == 0) {
     float bv_ = sv_[0];
     int bi_ = si_[0];
@@ -188,11 +214,6 @@ __device__ __forceinline__ void block_argmax_finish(float best_v, int best_i, in
         bi_ = si_[j];
       }
     *token = bi_;
-    if (LSE) {
-      float m_ = sm_[0], s_ = ss_[0];
-      for (int j = 1; j < NW; ++j) lse_merge(m_, s_, sm_[j], ss_[j]);
-      *lo.lse = m_ + logf(s_);
-    }
     hdr[kHdrCounterA] = 0;  // leave the counter ready for the next call
   }
 }
@@ -222,7 +243,8 @@ __global__ void __launch_bounds__(kLmThreads, kLmBlocksPerSm)
 
   float best_v = -INFINITY;
   int best_i = INT_MAX;
-  float lm = -INFINITY, ls = 0.f;  // log-sum-exp partial of this thread's rows
+  float lm = -INFINITY, ls = 0.f, lbuf = 0.f;  // log-sum-exp partial of this lane's rows
+  int lnb = 0;
   const int gwarp = blockIdx.x * kLmWarps + warp;
   const int nwarps = gridDim.x * kLmWarps;
   constexpr int RPI = RPS * U;  // rows per warp-iteration
@@ -252,14 +274,20 @@ __global__ void __launch_bounds__(kLmThreads, kLmBlocksPerSm)
       const int row = r0 + u * RPS + rsub;
       if (g == 0 && row < N) {
         if (logits) logits[row] = d;
-        if (LSE) lse_add(lm, ls, d);
         if (better(dc, row, best_v, best_i)) {
           best_v = dc;
           best_i = row;
         }
       }
+      if (LSE) {
+#pragma unroll
+        for (int r = 0; r < RPS; ++r)
+          if (r0 + u * RPS + r < N)
+            lse_buffer(lm, ls, lbuf, lnb, RPS == 1 ? d : __shfl_sync(0xffffffffu, d, r * G));
+      }
     }
   }
+  if (LSE) lse_flush(lm, ls, lbuf, lnb);
   block_argmax_finish<kLmWarps, LSE>(best_v, best_i, token, hdr, part_v, part_i, lm, ls, lo);
 }
 
@@ -316,7 +344,7 @@ __global__ void __launch_bounds__(kLsThreads, 1)
 
   float best_v = -INFINITY;
   int best_i = INT_MAX;
-  float lm = -INFINITY, ls = 0.f;  // log-sum-exp partial of this thread's rows
+  float lm = -INFINITY, ls = 0.f;  // log-sum-exp partial of this thread's share of the rows
   if (warp == kLsWarps) {
     // ---------------------------------------------------------------- copy thread
     if (lane == 0) {
@@ -391,7 +419,6 @@ __global__ void __launch_bounds__(kLsThreads, 1)
         if (g == 0 && lr < rows) {
           const int row = r0 + lr;
           if (logits) logits[row] = d;
-          if (LSE) lse_add(lm, ls, d);
           const float dc = cand(d);
           if (better(dc, row, best_v, best_i)) {
             best_v = dc;
@@ -400,6 +427,13 @@ __global__ void __launch_bounds__(kLsThreads, 1)
         }
       }
     }
+  }
+  if (LSE) {
+    // the block's rows have their logits in `logits` (global, just written): every thread
+    // folds a strided share of them into its partial, off the streaming loop
+    __syncthreads();
+    if (!s_abort)
+      for (int r = r_begin + (int)threadIdx.x; r < r_end; r += kLsThreads) lse_add(lm, ls, __ldcg(logits + r));
   }
   block_argmax_finish<kLsWarps + 1, LSE>(best_v, best_i, token, hdr, part_v, part_i, lm, ls, lo);
 }
@@ -416,6 +450,8 @@ static void launch_g(const lily_q4_mat &W, int N, const uint16_t *x, int32_t *to
                         : LseOut{};
   if constexpr (G >= 8) {
     using C = LsCfg<G>;
+    // the log-sum-exp pass reads the logits back: into the workspace when not requested
+    if (LSE && !logits) logits = reinterpret_cast<float *>(base + l.off_logits);
     // set on every call: cheap, and correct for whichever device is current
     cudaFuncSetAttribute(gemv_argmax_stream_kernel<G, LSE>,
                          cudaFuncAttributeMaxDynamicSharedMemorySize, C::BYTES);

@@ -625,90 +625,9 @@ __device__ bool grid_barrier(int32_t *hdr, unsigned long long target, volatile i
   return !*s_abort;
 }
 
-// Selection key of (logit v, expert e): the order-preserving bits of v above ~e, so that a
-// larger key is a better candidate -- larger logit, then lower index (ties), as every top-k
-// here orders them.  0 is below every candidate's key (padding).
-__device__ __forceinline__ unsigned long long route_key(float v, int e) {
-  return ((unsigned long long)f2key(v) << 32) | (uint32_t)~(uint32_t)e;
-}
-
-// Sort N keys held in registers, largest first (bitonic network, compile-time indices).
-template <int N>
-__device__ __forceinline__ void sort_keys_desc(unsigned long long (&a)[N]) {
-#pragma unroll
-  for (int kk = 2; kk <= N; kk <<= 1) {
-#pragma unroll
-    for (int j = kk >> 1; j > 0; j >>= 1) {
-#pragma unroll
-      for (int i = 0; i < N; ++i) {
-        const int l = i ^ j;
-        if (l > i) {
-          const unsigned long long hi = a[i] > a[l] ? a[i] : a[l];
-          const unsigned long long lo = a[i] > a[l] ? a[l] : a[i];
-          a[i] = (i & kk) == 0 ? hi : lo;
-          a[l] = (i & kk) == 0 ? lo : hi;
-        }
-      }
-    }
-  }
-}
-
-// a, b sorted largest first -> a = the N largest of both, sorted: the elementwise maximum of
-// a and b reversed is bitonic and holds them; a bitonic merge sorts it.
-template <int N>
-__device__ __forceinline__ void merge_top(unsigned long long (&a)[N],
-                                          const unsigned long long (&b)[N]) {
-#pragma unroll
-  for (int i = 0; i < N; ++i) a[i] = a[i] > b[N - 1 - i] ? a[i] : b[N - 1 - i];
-#pragma unroll
-  for (int j = N >> 1; j > 0; j >>= 1) {
-#pragma unroll
-    for (int i = 0; i < N; ++i) {
-      const int l = i ^ j;
-      if (l > i) {
-        const unsigned long long hi = a[i] > a[l] ? a[i] : a[l];
-        const unsigned long long lo = a[i] > a[l] ? a[l] : a[i];
-        a[i] = hi;
-        a[l] = lo;
-      }
-    }
-  }
-}
-
-// Warp top-KL of the 32 x EC keys: each lane sorts its keys (in runs of KL, merged), then a
-// butterfly over the lanes merges the lists pairwise, after which every lane holds the KL
-// largest keys in order, in top[0..KL) (top[KL..16) = 0).
-template <int EC, int KL>
-__device__ __forceinline__ void warp_topk(const unsigned long long (&lk)[EC],
-                                          unsigned long long (&top)[kMaxK]) {
-  static_assert(KL <= kMaxK, "top list");
-  constexpr int R = EC < KL ? EC : KL;  // keys per run
-  unsigned long long a[KL];
-#pragma unroll
-  for (int i = 0; i < KL; ++i) a[i] = i < R ? lk[i] : 0ull;
-  sort_keys_desc<KL>(a);
-#pragma unroll
-  for (int r = 1; r < EC / R; ++r) {
-    unsigned long long b[KL];
-#pragma unroll
-    for (int i = 0; i < KL; ++i) b[i] = i < R ? lk[r * R + i] : 0ull;
-    sort_keys_desc<KL>(b);
-    merge_top<KL>(a, b);
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    unsigned long long b[KL];
-#pragma unroll
-    for (int i = 0; i < KL; ++i) b[i] = __shfl_xor_sync(0xffffffffu, a[i], o);
-    merge_top<KL>(a, b);
-  }
-#pragma unroll
-  for (int i = 0; i < kMaxK; ++i) top[i] = i < KL ? a[i] : 0ull;
-}
-
 // Routing of up to 4 tokens by one block, for the single-launch path: warps 0..T-1 take
-// the top-k of one token each (warp_topk); warp 0 then builds the unique-expert table with a
-// bitmap of selected experts (ascending id) and places the (token, weight) pairs.
+// the top-k of one token each; warp 0 then builds the unique-expert table with a bitmap
+// of selected experts (ascending id) and places the (token, weight) pairs.
 template <int EC>
 __device__ void route_small(const float *logits, const float *sigma, int T, int E, int k,
                             int has_shared, const RouteDst &d) {
@@ -721,34 +640,34 @@ __device__ void route_small(const float *logits, const float *sigma, int T, int 
   if (warp < T) {
     const int t = warp;
     const float *lg = logits + (size_t)t * E;
-    unsigned long long lk[EC];
+    float lv[EC];
 #pragma unroll
-    for (int j = 0; j < EC; ++j) {
-      const int e = lane + 32 * j;
-      lk[j] = e < E ? route_key(cand(__ldcg(lg + e)), e) : 0ull;
-    }
-    unsigned long long top[kMaxK];  // every lane: the k selections in order
-    if (k <= 8)
-      warp_topk<EC, 8>(lk, top);
-    else
-      warp_topk<EC, 16>(lk, top);
-    // lane i keeps selection i; the softmax over the k selected logits (selection 0 holds
-    // the largest) and the ranks below use the list every lane holds (no shuffles)
-    float myv = 0.f, den = 0.f;
+    for (int j = 0; j < EC; ++j) lv[j] = (lane + 32 * j < E) ? cand(__ldcg(lg + lane + 32 * j)) : -INFINITY;
+    uint32_t taken = 0;
+    float myv = 0.f;
     int mye = 0;
-    const float v0 = key2f((uint32_t)(top[0] >> 32));
+    for (int i = 0; i < k; ++i) {
+      float bv = -INFINITY;
+      int be = INT_MAX;
 #pragma unroll
-    for (int j = 0; j < kMaxK; ++j) {
-      if (j < k) {
-        const float vj = key2f((uint32_t)(top[j] >> 32));
-        den += expf(vj - v0);
-        if (lane == j) {
-          myv = vj;
-          mye = (int)~(uint32_t)top[j];
+      for (int j = 0; j < EC; ++j) {
+        const int e = lane + 32 * j;
+        if (e < E && !(taken & (1u << j)) && better(lv[j], e, bv, be)) {
+          bv = lv[j];
+          be = e;
         }
       }
+      warp_argmax(bv, be);
+      if ((be & 31) == lane) taken |= 1u << (be >> 5);
+      if (lane == i) {  // lane i keeps selection i
+        myv = bv;
+        mye = be;
+      }
     }
-    const float pi = lane < k ? expf(myv - v0) / den : 0.f;
+    // softmax over the k selected logits (selection 0 holds the largest)
+    const float v0 = __shfl_sync(0xffffffffu, myv, 0);
+    const float ex = lane < k ? expf(myv - v0) : 0.f;
+    const float pi = ex / seg_sum<32>(ex);
     if (lane < k) {
       s_idx[t * k + lane] = mye;
       s_p[t * k + lane] = pi;
@@ -759,8 +678,7 @@ __device__ void route_small(const float *logits, const float *sigma, int T, int 
       // one token: the k selected experts are the unique experts, each with one pair;
       // lane i places selection i at the rank of its expert id among the k
       int rank = 0;
-#pragma unroll
-      for (int j = 0; j < kMaxK; ++j) rank += (j < k && (int)~(uint32_t)top[j] < mye);
+      for (int j = 0; j < k; ++j) rank += __shfl_sync(0xffffffffu, mye, j) < mye;
       if (lane < k) {
         d.uexp[rank] = mye;
         d.ubase[rank] = rank;
