@@ -1,8 +1,8 @@
 // Decode-step MoE feed-forward (1..16 tokens).
 //
-// "The MoE" kernels of a decode step, which is bandwidth-bound (fork page, "How the
-// speed was achieved": a decode step's reads, tuned toward "what its chain of reads
-// can stream").  Three launches on the caller's stream:
+// The MoE kernels of a decode step, which is bound by its reads (fork page, "How the
+// speed was achieved": the decode step was tuned toward the bandwidth its chain of
+// dependent reads can reach).  The general path is three launches on the caller's stream:
 //
 //  1. router_topk_kernel: fp32 router logits (one warp per expert row, bf16 weights)
 //     and the shared-expert gate sigmoid(x . g_shared); the last block to finish takes

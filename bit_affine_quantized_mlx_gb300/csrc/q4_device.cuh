@@ -1,7 +1,7 @@
 // Device helpers shared by the kernels of the Q4 library (not by the oracle).
 //
-// In-register dequantisation of the MLX-affine 4-bit format (Lily README,
-// "Requirements": "MLX affine 4-bit ... group size 64").  For one group of 64
+// In-register dequantisation of the MLX-affine 4-bit format with groups of 64 weights
+// (Lily README, first paragraph and "Requirements").  For one group of 64
 // weights with scale s and bias b:
 //
 //     sum_k (s*q_k + b) x_k  =  s * sum_k q_k x_k  +  b * sum_k x_k

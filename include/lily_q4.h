@@ -3,14 +3,14 @@
  *
  * The operations follow the Lily pages' statement of the problem:
  *
- *  - Weight format: "MLX affine 4-bit weights" with "group size 64" (Lily README,
- *    first paragraph and "Requirements"; Lily-vs-MLX report, "Hardware and
- *    software": "MLX affine Q4/group-64").  Reading taken: dequantised weight
+ *  - Weight format: MLX affine 4-bit weights in groups of 64 (Lily README, first
+ *    paragraph and "Requirements"; Lily-vs-MLX report, "Hardware and software").
+ *    Reading taken: dequantised weight
  *    w = s*q + b, q a 4-bit code, eight codes per uint32 along K with the lowest
  *    nibble first, one bf16 scale s and one bf16 bias b per 64 consecutive K.
- *  - The MoE feed-forward of a decode step and of a prefill chunk ("the MoE"
- *    kernels and "better tiling for the expert GEMM", fork page, "How the speed
- *    was achieved"; decode is bandwidth-bound, prefill compute-bound, same
+ *  - The MoE feed-forward of a decode step and of a prefill chunk (the MoE
+ *    kernels and the tiling of the expert GEMM, fork page, "How the speed was
+ *    achieved"; decode is bandwidth-bound, prefill compute-bound, same
  *    section): router logits, top-k with softmax over the k, SwiGLU experts,
  *    down projection with the weighted combine, and a shared expert gated by
  *    sigmoid(x . g_shared) (fork page, "The model": the shared expert).
@@ -142,8 +142,8 @@ LILY_Q4_API int lily_q4_gemv_argmax(const lily_q4_mat *W, int32_t N, int32_t K, 
 /*
  * lily_q4_gemv_argmax_logprobs -- lily_q4_gemv_argmax plus the full-vocabulary
  * log-sum-exp and, optionally, the log-probability vector, in the same pass over W
- * (the MLX path of the Lily-vs-MLX report, "Measurement contract", computes both for
- * every prompt: "full-vocabulary log-sum-exp/logprobs").
+ * (in the Lily-vs-MLX report, "Measurement contract", the MLX path computes both over
+ * the whole vocabulary for every token).
  *   token = argmax_n logit[n] (as lily_q4_gemv_argmax),
  *   *lse = log sum_n exp(logit[n]) (fp32; running max and sum of exp, merged in a fixed
  *   order, so repeated calls give identical bits),

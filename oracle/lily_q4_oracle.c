@@ -8,7 +8,7 @@
  *
  * What it computes (plain definitions, written out loop by loop):
  *
- *  - Weight format: "MLX affine 4-bit weights ... group size 64" (Lily README,
+ *  - Weight format: MLX affine 4-bit weights in groups of 64 (Lily README,
  *    first paragraph and "Requirements"; Lily-vs-MLX report, "Hardware and
  *    software").  The pages name the format only; the reading taken here is
  *    w = s*q + b with q the 4-bit code, eight codes per uint32 along K, lowest
@@ -26,12 +26,12 @@
  *    expert among the dense tensors): o_s the same way, scaled by
  *    sigmoid(g_shared . x).
  *  - Output: y = sum_i p_i o_i + sigma o_s.
- *  - LM head with greedy argmax (Lily README first paragraph "always decodes
- *    greedily"; report "Measurement contract": greedy token selection without
+ *  - LM head with greedy argmax (Lily README, first paragraph: Lily decodes
+ *    greedily; report "Measurement contract": greedy token selection without
  *    logprobs): fp64 logits, argmax with ties to the lower id.
  *  - Full-vocabulary log-sum-exp and log-probabilities of those logits (report
- *    "Measurement contract": the MLX path computes "full-vocabulary
- *    log-sum-exp/logprobs"): lse = log sum_n exp(l_n), logprob_n = l_n - lse,
+ *    "Measurement contract": the MLX path computes both over the whole
+ *    vocabulary): lse = log sum_n exp(l_n), logprob_n = l_n - lse,
  *    in fp64 (the sum is taken after subtracting the maximum, which changes
  *    nothing mathematically).
  *
