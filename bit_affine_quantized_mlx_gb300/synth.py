@@ -36,6 +36,7 @@ S_GATE, S_UP, S_DOWN = 10, 11, 12
 S_SH_GATE, S_SH_UP, S_SH_DOWN = 20, 21, 22
 S_X = 100
 S_LM = 30
+S_LM8 = 31
 
 
 def bf16_from_f32(a) -> np.ndarray:
@@ -75,6 +76,42 @@ class Q4Matrix:
     @property
     def nbytes(self) -> int:
         return self.w.nbytes + self.s.nbytes + self.b.nbytes
+
+
+@dataclass
+class Q8Matrix:
+    """One MLX-affine 8-bit matrix: codes uint32 [N, K/4] (four codes per word along K, lowest
+    byte first), bf16 scales and biases [N, K/64]."""
+    w: np.ndarray
+    s: np.ndarray
+    b: np.ndarray
+
+    @property
+    def N(self) -> int:
+        return int(self.w.shape[-2])
+
+    @property
+    def K(self) -> int:
+        return int(self.w.shape[-1]) * 4
+
+    @property
+    def nbytes(self) -> int:
+        return self.w.nbytes + self.s.nbytes + self.b.nbytes
+
+
+def draw_q8(N: int, K: int, *key: int) -> Q8Matrix:
+    """Draw one 8-bit matrix [N x K]: codes uniform 0..255, s ~ U(0.000125, 0.00125) (the 4-bit
+    range over 16x the levels), b = -128 s (1 + N(0, 0.05)), both rounded to bf16."""
+    if K % GROUP:
+        raise ValueError("K must be a multiple of 64")
+    g = _rng(*key)
+    w = g.integers(0, 2**32, size=(N, K // 4), dtype=np.uint32)
+    s64 = g.uniform(0.000125, 0.00125, size=(N, K // GROUP))
+    s = bf16_from_f32(s64.astype(np.float32))
+    eps = g.normal(0.0, 0.05, size=(N, K // GROUP))
+    b64 = -128.0 * bf16_to_f32(s).astype(np.float64) * (1.0 + eps)
+    b = bf16_from_f32(b64.astype(np.float32))
+    return Q8Matrix(w, s, b)
 
 
 def draw_q4(N: int, K: int, *key: int) -> Q4Matrix:
@@ -209,6 +246,11 @@ WORKLOADS: Dict[int, Workload] = {w.wid: w for w in (TINY, DECODE, LMHEAD, PREFI
 
 def draw_lm_head(V: int = 151936, H: int = 2048, key=(2, 0)) -> Q4Matrix:
     return draw_q4(V, H, *key, S_LM)
+
+
+def draw_lm_head_q8(V: int = 151936, H: int = 2048, key=(2, 0)) -> Q8Matrix:
+    """The LM head kept at 8 bits (the q4-xl conversion)."""
+    return draw_q8(V, H, *key, S_LM8)
 
 
 def draw_lm_x(H: int = 2048, key=(2, 0), attempt: int = 0) -> np.ndarray:

@@ -29,6 +29,11 @@
  *  - LM head with greedy argmax (Lily README, first paragraph: Lily decodes
  *    greedily; report "Measurement contract": greedy token selection without
  *    logprobs): fp64 logits, argmax with ties to the lower id.
+ *  - Affine 8-bit matrices (the report's checkpoint keeps its router gates at
+ *    8 bits, "Hardware and software"; the fork page's q4-xl conversion keeps the
+ *    shared expert and the LM head at 8 bits, "The model"): the same
+ *    w = s*q + b with q in 0..255, four codes per uint32 along K, lowest byte
+ *    first (the 4-bit packing with 8-bit fields), one bf16 (s, b) pair per 64 K.
  *  - Full-vocabulary log-sum-exp and log-probabilities of those logits (report
  *    "Measurement contract": the MLX path computes both over the whole
  *    vocabulary): lse = log sum_n exp(l_n), logprob_n = l_n - lse,
@@ -86,6 +91,64 @@ void orc_set_threads(int n) {
 #else
     (void)n;
 #endif
+}
+
+/* 8-bit code k of row n: word k/4, byte k%4 (lowest byte first). */
+static unsigned orc_code8(const uint32_t *w, int K, int n, int k) {
+    uint32_t word = w[(size_t)n * (size_t)(K / 4) + (size_t)(k / 4)];
+    return (word >> (8u * (unsigned)(k % 4))) & 0xFFu;
+}
+
+/* Dequantised 8-bit weight (n, k): fp32 s*q + b (s*q exact: 8 x 8 significant bits),
+ * widened to double. */
+static double orc_weight8(const uint32_t *w, const uint16_t *s, const uint16_t *b,
+                          int K, int n, int k) {
+    size_t gi = (size_t)n * (size_t)(K / ORC_GROUP) + (size_t)(k / ORC_GROUP);
+    float wf = orc_bf16(s[gi]) * (float)orc_code8(w, K, n, k) + orc_bf16(b[gi]);
+    return (double)wf;
+}
+
+void orc_q8_unpack(const uint32_t *w, int N, int K, uint8_t *q) {
+    for (int n = 0; n < N; ++n)
+        for (int k = 0; k < K; ++k)
+            q[(size_t)n * K + k] = (uint8_t)orc_code8(w, K, n, k);
+}
+
+void orc_q8_pack(const uint8_t *q, int N, int K, uint32_t *w) {
+    for (int n = 0; n < N; ++n)
+        for (int m = 0; m < K / 4; ++m) {
+            uint32_t word = 0;
+            for (int j = 0; j < 4; ++j)
+                word |= ((uint32_t)q[(size_t)n * K + 4 * m + j]) << (8 * j);
+            w[(size_t)n * (K / 4) + m] = word;
+        }
+}
+
+void orc_q8_dequant(const uint32_t *w, const uint16_t *s, const uint16_t *b,
+                    int N, int K, double *out) {
+    for (int n = 0; n < N; ++n)
+        for (int k = 0; k < K; ++k)
+            out[(size_t)n * K + k] = orc_weight8(w, s, b, K, n, k);
+}
+
+/* 8-bit LM head: logits[n] for bf16 x (rows split over threads); returns the argmax
+ * (ties to the lower id). */
+int orc_q8_lm_head(const uint32_t *w, const uint16_t *s, const uint16_t *b,
+                   int N, int K, const uint16_t *x, double *logits) {
+    double *xd = (double *)malloc(sizeof(double) * (size_t)K);
+    for (int k = 0; k < K; ++k) xd[k] = (double)orc_bf16(x[k]);
+#pragma omp parallel for schedule(static)
+    for (int n = 0; n < N; ++n) {
+        double acc = 0.0;
+        for (int k = 0; k < K; ++k)
+            acc += orc_weight8(w, s, b, K, n, k) * xd[k];
+        logits[n] = acc;
+    }
+    free(xd);
+    int best = 0;
+    for (int n = 1; n < N; ++n)
+        if (logits[n] > logits[best]) best = n;
+    return best;
 }
 
 /* out[N][K] = dequantised matrix. */

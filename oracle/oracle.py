@@ -60,6 +60,11 @@ def lib():
         L.orc_q4_matvec.argtypes = [vp, vp, vp, i32, i32, vp, vp]
         L.orc_lm_head.argtypes = [vp, vp, vp, i32, i32, vp, vp]
         L.orc_lm_head.restype = i32
+        L.orc_q8_unpack.argtypes = [vp, i32, i32, vp]
+        L.orc_q8_pack.argtypes = [vp, i32, i32, vp]
+        L.orc_q8_dequant.argtypes = [vp, vp, vp, i32, i32, vp]
+        L.orc_q8_lm_head.argtypes = [vp, vp, vp, i32, i32, vp, vp]
+        L.orc_q8_lm_head.restype = i32
         L.orc_log_sum_exp.argtypes = [vp, i32, vp]
         L.orc_log_sum_exp.restype = C.c_double
         L.orc_router.argtypes = [vp, vp, i32, i32, vp, vp]
@@ -135,6 +140,40 @@ def lm_head(m, x_bits: np.ndarray) -> Tuple[int, np.ndarray]:
     x = _c(x_bits, np.uint16)
     logits = np.empty(N, dtype=np.float64)
     tok = lib().orc_lm_head(_p(w), _p(s), _p(b), N, K, _p(x), _p(logits))
+    return int(tok), logits
+
+
+def q8_unpack(w: np.ndarray, N: int, K: int) -> np.ndarray:
+    w = _c(w, np.uint32)
+    q = np.empty((N, K), dtype=np.uint8)
+    lib().orc_q8_unpack(_p(w), N, K, _p(q))
+    return q
+
+
+def q8_pack(q: np.ndarray) -> np.ndarray:
+    q = _c(q, np.uint8)
+    N, K = q.shape
+    w = np.empty((N, K // 4), dtype=np.uint32)
+    lib().orc_q8_pack(_p(q), N, K, _p(w))
+    return w
+
+
+def q8_dequant(m) -> np.ndarray:
+    """Dense fp64 [N, K] of an affine 8-bit matrix."""
+    w, s, b = _c(m.w, np.uint32), _c(m.s, np.uint16), _c(m.b, np.uint16)
+    N, K = w.shape[-2], w.shape[-1] * 4
+    out = np.empty((N, K), dtype=np.float64)
+    lib().orc_q8_dequant(_p(w), _p(s), _p(b), N, K, _p(out))
+    return out
+
+
+def q8_lm_head(m, x_bits: np.ndarray) -> Tuple[int, np.ndarray]:
+    """fp64 logits of an 8-bit LM head for one bf16 token, and the greedy argmax."""
+    w, s, b = _c(m.w, np.uint32), _c(m.s, np.uint16), _c(m.b, np.uint16)
+    N, K = w.shape[-2], w.shape[-1] * 4
+    x = _c(x_bits, np.uint16)
+    logits = np.empty(N, dtype=np.float64)
+    tok = lib().orc_q8_lm_head(_p(w), _p(s), _p(b), N, K, _p(x), _p(logits))
     return int(tok), logits
 
 
@@ -287,11 +326,13 @@ def tokens_without_near_ties(L, draw, T: int, max_attempts: int = 64):
     return x, attempts
 
 
-def lm_x_without_near_tie(m, draw, max_attempts: int = 64):
-    """Redraw x until the oracle's top-2 LM-head logits differ by at least 1e-3."""
+def lm_x_without_near_tie(m, draw, max_attempts: int = 64, head=None):
+    """Redraw x until the oracle's top-2 LM-head logits differ by at least 1e-3 (head: the
+    oracle LM head to use, lm_head for 4-bit weights by default, q8_lm_head for 8-bit)."""
+    head = head or lm_head
     for a in range(max_attempts):
         x = draw(a)
-        tok, lg = lm_head(m, x)
+        tok, lg = head(m, x)
         srt = np.sort(lg)
         if srt[-1] - srt[-2] >= TIE_GAP:
             return x, a, tok, lg

@@ -374,3 +374,71 @@ def test_lse_non_finite():
     assert math.isnan(orc.log_softmax(np.array([0.0, nan, 1.0]))[0])
     lse, lp = orc.log_softmax(np.array([-inf, 0.0]))   # a -inf logit adds nothing
     assert lse == 0.0 and lp[0] == -inf
+
+
+# ----------------------------------------------------------------------------- affine 8-bit
+
+def _q8(q, s, b):
+    return synth.Q8Matrix(orc.q8_pack(q), np.asarray(s, np.uint16), np.asarray(b, np.uint16))
+
+
+def test_q8_byte_order_golden():
+    """Codes 1,2,3,4 pack to 0x04030201 (lowest byte first); catches a reversed byte order or
+    4-bit fields."""
+    for codes, word in _read_golden("q8_byte_order.txt"):
+        q = np.array([[int(c, 16) for c in codes.split(",")]], dtype=np.uint8)
+        assert orc.q8_pack(q)[0, 0] == int(word, 16)
+        assert list(orc.q8_unpack(np.array([[int(word, 16)]], np.uint32), 1, 4)[0]) == list(q[0])
+
+
+def test_q8_pack_unpack_roundtrip():
+    rng = np.random.default_rng(11)
+    w = rng.integers(0, 2**32, size=(5, 32), dtype=np.uint32)
+    q = orc.q8_unpack(w, 5, 128)
+    assert q.max() > 15   # all eight bits of a code are kept
+    assert np.array_equal(orc.q8_pack(q), w)
+
+
+def test_q8_dequant_extreme_codes_exact():
+    """With s = 2^-8 and b = -1/2: q=0 gives exactly -1/2, q=255 exactly 255/256 - 1/2."""
+    N, K = 4, 128
+    for code, want in ((0, -0.5), (255, 255.0 / 256.0 - 0.5), (128, 0.0)):
+        q = np.full((N, K), code, dtype=np.uint8)
+        m = _q8(q, np.full((N, 2), _bf16(2.0 ** -8), np.uint16), np.full((N, 2), _bf16(-0.5), np.uint16))
+        assert np.all(orc.q8_dequant(m) == want)
+
+
+def test_q8_dequant_group_and_row_indexing():
+    """A distinct scale per (row, group) and a code per column (N != K): catches k/4 vs k/64
+    group indexing and transposition."""
+    N, K = 3, 192
+    q = (np.arange(N * K).reshape(N, K) % 256).astype(np.uint8)
+    s = np.array([[_bf16(2.0 ** -(n + 3) * (g + 1)) for g in range(K // 64)] for n in range(N)],
+                 dtype=np.uint16)
+    b = np.array([[_bf16(-(n * 4 + g)) for g in range(K // 64)] for n in range(N)], dtype=np.uint16)
+    W = orc.q8_dequant(_q8(q, s, b))
+    for n in range(N):
+        for k in range(K):
+            g = k // 64
+            assert W[n, k] == 2.0 ** -(n + 3) * (g + 1) * ((n * K + k) % 256) - (n * 4 + g)
+
+
+def test_q8_lm_head_matches_library_matmul():
+    """Logits equal numpy's matrix-vector product of the dequantised matrix (both in fp64, up
+    to summation order), argmax included."""
+    m = synth.draw_q8(300, 256, 40, 1)
+    x = synth.draw_bf16_normal((256,), 1.0, 41)
+    tok, lg = orc.q8_lm_head(m, x)
+    want = orc.q8_dequant(m) @ bf16_to_f32(x).astype(np.float64)
+    assert np.allclose(lg, want, rtol=1e-12, atol=1e-12)
+    assert tok == int(np.argmax(want))
+
+
+def test_q8_lm_head_planted_tie():
+    """Rows 5 and 17 identical and dominant: the argmax is the lower id 5."""
+    N, K = 24, 128
+    q = np.zeros((N, K), np.uint8)
+    q[5] = q[17] = 255
+    m = _q8(q, np.full((N, 2), _bf16(1.0), np.uint16), np.zeros((N, 2), np.uint16))
+    tok, lg = orc.q8_lm_head(m, np.full(K, _bf16(1.0), np.uint16))
+    assert tok == 5 and lg[5] == lg[17] == 255.0 * K
