@@ -317,6 +317,36 @@ def run_gb300(args):
             lp_ms.append(a0.elapsed_time(a1))
     lp_mean = max_over_ranks([statistics.mean(lp_ms)], dev)[0]
 
+    # ---- the same LM head kept at 8 bits (q4-xl), argmax only, timed the same way
+    W8 = q4.DeviceQ4.upload(synth.draw_lm_head_q8(lmw.V, lmw.H), dev)
+    ws8 = q4.new_workspace(q4.lily_q8_gemv_argmax_workspace_bytes(lmw.V, lmw.H), dev)
+
+    def q8_part():
+        q4.lily_q8_gemv_argmax(W8, xl, tok, ws=ws8, stream=stream)
+
+    with torch.cuda.stream(stream):
+        q8_part()
+    stream.synchronize()
+    g_q8 = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_q8, stream=stream):
+        q8_part()
+    q8_ms = []
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            g_q8.replay()
+        for _ in range(max(args.steps, 3)):
+            a0 = torch.cuda.Event(enable_timing=True)
+            a1 = torch.cuda.Event(enable_timing=True)
+            a0.record(stream)
+            g_q8.replay()
+            a1.record(stream)
+            a1.synchronize()
+            q8_ms.append(a0.elapsed_time(a1))
+    q8_mean = max_over_ranks([statistics.mean(q8_ms)], dev)[0]
+    q8_bytes = lmw.V * lmw.H + lmw.V * (lmw.H // 64) * 4 + lmw.H * 2 + 4
+    q8_gbs = q8_bytes / (q8_mean / 1e3) / 1e9
+    del W8, ws8
+
     e2e_val = None
     if not args.no_e2e:
         for _ in range(2):
@@ -356,6 +386,8 @@ def run_gb300(args):
         "lm_head": {"us": round(lm_mean * 1e3, 2), "bytes": lm_bytes,
                     "hbm_gbs": round(lm_gbs, 1), "frac_of_measured_hbm": round(lm_gbs / pk["hbm_gbs"], 4),
                     "with_logprobs_us": round(lp_mean * 1e3, 2)},
+        "lm_head_q8": {"us": round(q8_mean * 1e3, 2), "bytes": q8_bytes, "hbm_gbs": round(q8_gbs, 1),
+                       "frac_of_measured_hbm": round(q8_gbs / pk["hbm_gbs"], 4)},
         "prefill": {"us": round(pf_mean * 1e3, 1), "gflop": round(pf_flops / 1e9, 2),
                     "tflops": round(pf_tflops, 1),
                     "frac_of_measured_bf16": round(pf_tflops / pk["bf16_tflops_sustained"], 4),

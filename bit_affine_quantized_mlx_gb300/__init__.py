@@ -80,6 +80,9 @@ def load(path: Optional[str] = None):
     L.lily_q4_gemv_argmax_noalloc.argtypes = [C.POINTER(lily_q4_mat), i32, i32, vp, vp, vp, vp]
     L.lily_q4_gemv_argmax_logprobs.argtypes = [C.POINTER(lily_q4_mat), i32, i32, vp, vp, vp, vp,
                                                vp, sz, vp]
+    L.lily_q8_gemv_argmax.argtypes = L.lily_q4_gemv_argmax.argtypes
+    L.lily_q8_gemv_argmax_workspace_bytes.argtypes = [i32, i32]
+    L.lily_q8_gemv_argmax_workspace_bytes.restype = sz
     L.lily_q4_workspace_init.argtypes = [vp, sz, vp]
     L.lily_q4_workspace_status.argtypes = [vp, vp]
     L.lily_q4_status_string.argtypes = [C.c_int]
@@ -89,7 +92,8 @@ def load(path: Optional[str] = None):
     for f in ("lily_q4_moe_decode", "lily_q4_moe_prefill", "lily_q4_gemv_argmax",
               "lily_q4_workspace_init", "lily_q4_workspace_status", "lily_q4_pack",
               "lily_q4_unpack", "lily_q4_version", "lily_q4_moe_launches",
-              "lily_q4_gemv_argmax_noalloc", "lily_q4_gemv_argmax_logprobs"):
+              "lily_q4_gemv_argmax_noalloc", "lily_q4_gemv_argmax_logprobs",
+              "lily_q8_gemv_argmax"):
         getattr(L, f).restype = C.c_int
     _lib = L
     return L
@@ -257,6 +261,20 @@ def lily_q4_gemv_argmax(W: DeviceQ4, x, token, logits=None, ws=None, stream=None
     return _check(load().lily_q4_gemv_argmax(C.byref(m), N, K, _ptr(x), _ptr(token), _ptr(logits),
                                              _ptr(ws), ws.numel() if ws is not None else 0,
                                              _stream(stream)), "lily_q4_gemv_argmax")
+
+
+def lily_q8_gemv_argmax(W, x, token, logits=None, ws=None, stream=None):
+    """Greedy token of an 8-bit LM head (W: a DeviceQ4 holding uint32 [N, K/4] codes);
+    see include/lily_q4.h."""
+    N, K = int(W.w.shape[-2]), int(W.w.shape[-1]) * 4
+    m = W.c()
+    return _check(load().lily_q8_gemv_argmax(C.byref(m), N, K, _ptr(x), _ptr(token), _ptr(logits),
+                                             _ptr(ws), ws.numel() if ws is not None else 0,
+                                             _stream(stream)), "lily_q8_gemv_argmax")
+
+
+def lily_q8_gemv_argmax_workspace_bytes(N: int, K: int) -> int:
+    return int(load().lily_q8_gemv_argmax_workspace_bytes(int(N), int(K)))
 
 
 def lily_q4_gemv_argmax_logprobs(W: DeviceQ4, x, token, lse, logprobs=None, ws=None, stream=None):

@@ -10,6 +10,7 @@
 #include <cfloat>
 #include <climits>
 #include <mutex>
+#include <type_traits>
 
 #include "internal.h"
 #include "q4_device.cuh"
@@ -26,16 +27,19 @@ constexpr int kLsWarps = 24;                     // compute warps
 constexpr int kLsThreads = (kLsWarps + 1) * 32;  // + the copy warp
 constexpr int kLsStages = 4;
 constexpr int kLsStageCodes = 49152;             // code bytes per stage
-__host__ __device__ constexpr int ls_rows_per_stage(int G) { return kLsStageCodes / (32 * G); }
+// code bytes of a 64-group: 32 for 4-bit codes, 64 for 8-bit codes
+__host__ __device__ constexpr int ls_rows_per_stage(int G, int bits = 4) {
+  return kLsStageCodes / (8 * bits * G);
+}
 
-LmWsLayout lm_ws_layout(int N, int K) {
+LmWsLayout lm_ws_layout(int N, int K, int bits) {
   LmWsLayout l{};
   int sms = sm_count();
   if (sms <= 0) sms = 152;
   if (K / kGroup >= 8) {
     // streaming kernel: one block per SM, at most one block per stage of rows, each block a
     // contiguous range of rows
-    const int sr = ls_rows_per_stage(K / kGroup);
+    const int sr = ls_rows_per_stage(K / kGroup, bits);
     const int want = (N + sr - 1) / sr;
     l.grid = want < sms ? want : sms;
     if (l.grid < 1) l.grid = 1;
@@ -300,10 +304,11 @@ __global__ void __launch_bounds__(kLmThreads, kLmBlocksPerSm)
 // loads of later stages are in flight while 24 warps dequantise and reduce the current one.
 // A warp copies its rows of a stage into registers and hands the stage back at once.
 // ---------------------------------------------------------------------------------------
-template <int G>
+template <int G, int BITS = 4>
 struct LsCfg {
+  static constexpr int CB = 8 * BITS;                     // code bytes of a 64-group
   static constexpr int RPS = 32 / G;                      // rows per warp-step
-  static constexpr int SR = kLsStageCodes / (32 * G);     // rows per stage (32*G code bytes a row)
+  static constexpr int SR = kLsStageCodes / (CB * G);     // rows per stage (CB*G code bytes a row)
   static constexpr int WR = SR / (kLsWarps * RPS);        // warp-steps per warp per stage
   static constexpr int SC = SR * 2 * G;                   // bytes of scales (and of biases)
   static constexpr int STAGE = kLsStageCodes + 2 * SC;
@@ -312,7 +317,7 @@ struct LsCfg {
   static_assert(G >= 8 && WR * kLsWarps * RPS == SR && STAGE % 128 == 0, "stage shape");
 };
 
-template <int G, bool LSE>
+template <int G, bool LSE, int BITS = 4>
 __global__ void __launch_bounds__(kLsThreads, 1)
     gemv_argmax_stream_kernel(const uint32_t *__restrict__ w, const uint16_t *__restrict__ s,
                               const uint16_t *__restrict__ b, int N, int rows_per_block,
@@ -320,7 +325,7 @@ __global__ void __launch_bounds__(kLsThreads, 1)
                               int32_t *__restrict__ token, int32_t *__restrict__ hdr,
                               float *__restrict__ part_v, int32_t *__restrict__ part_i,
                               LseOut lo) {
-  using C = LsCfg<G>;
+  using C = LsCfg<G, BITS>;
   extern __shared__ __align__(128) uint8_t ls_smem[];
   __shared__ volatile int s_abort;
   const uint32_t sbase = tc::smem_u32(ls_smem);
@@ -354,10 +359,10 @@ __global__ void __launch_bounds__(kLsThreads, 1)
         if (!tc::wait_bar(empty(slot), ((st / kLsStages) & 1) ^ 1, &s_abort, err)) break;
         const int r0 = r_begin + st * C::SR;
         const int rows = min(C::SR, r_end - r0);
-        const uint32_t cb = (uint32_t)rows * 32u * G, sb = (uint32_t)rows * 2u * G;
+        const uint32_t cb = (uint32_t)rows * (uint32_t)C::CB * G, sb = (uint32_t)rows * 2u * G;
         const uint32_t dst = sbase + (uint32_t)(slot * C::STAGE);
         tc::mbar_arrive_expect_tx(full(slot), cb + 2u * sb);
-        tc::bulk_g2s(dst, w + (size_t)r0 * 8 * G, cb, full(slot));
+        tc::bulk_g2s(dst, w + (size_t)r0 * (C::CB / 4) * G, cb, full(slot));
         tc::bulk_g2s(dst + kLsStageCodes, s + (size_t)r0 * G, sb, full(slot));
         tc::bulk_g2s(dst + kLsStageCodes + C::SC, b + (size_t)r0 * G, sb, full(slot));
       }
@@ -374,13 +379,17 @@ __global__ void __launch_bounds__(kLsThreads, 1)
   } else {
     // ---------------------------------------------------------------- compute warps
     const int g = lane % G, rsub = lane / G;
-    XGroupB xg;
+    // x pairs in the order the codes unpack in (4-bit: (x_j, x_j+4); 8-bit: (x_j, x_j+2))
+    std::conditional_t<BITS == 8, XGroup8, XGroupB> xg;
     {
       uint4 c[8];
       const uint4 *xp = reinterpret_cast<const uint4 *>(x + kGroup * g);
 #pragma unroll
       for (int i = 0; i < 8; ++i) c[i] = __ldg(xp + i);
-      xgroupb_from_bf16(xg, c);
+      if constexpr (BITS == 8)
+        xgroup8_from_bf16(xg, c);
+      else
+        xgroupb_from_bf16(xg, c);
     }
 #pragma unroll 1
     for (int st = 0; st < nst; ++st) {
@@ -393,19 +402,21 @@ __global__ void __launch_bounds__(kLsThreads, 1)
       const uint8_t *cs = ls_smem + slot * C::STAGE;
       const uint16_t *ss = reinterpret_cast<const uint16_t *>(cs + kLsStageCodes);
       const uint16_t *bs = reinterpret_cast<const uint16_t *>(cs + kLsStageCodes + C::SC);
-      uint4 wa[C::WR], wb[C::WR];
+      constexpr int NV = C::CB / 16;  // 16-byte code vectors of a lane's group
+      uint4 wc[C::WR][NV];
       float sv[C::WR], bv[C::WR];
 #pragma unroll
       for (int u = 0; u < C::WR; ++u) {
         const int lr = (warp * C::WR + u) * C::RPS + rsub;
         if (lr < rows) {
-          const uint4 *p = reinterpret_cast<const uint4 *>(cs + lr * 32 * G + 32 * g);
-          wa[u] = p[0];
-          wb[u] = p[1];
+          const uint4 *p = reinterpret_cast<const uint4 *>(cs + lr * C::CB * G + C::CB * g);
+#pragma unroll
+          for (int v = 0; v < NV; ++v) wc[u][v] = p[v];
           sv[u] = bf16f(ss[lr * G + g]);
           bv[u] = bf16f(bs[lr * G + g]);
         } else {
-          wa[u] = wb[u] = make_uint4(0, 0, 0, 0);
+#pragma unroll
+          for (int v = 0; v < NV; ++v) wc[u][v] = make_uint4(0, 0, 0, 0);
           sv[u] = bv[u] = 0.f;
         }
       }
@@ -414,7 +425,11 @@ __global__ void __launch_bounds__(kLsThreads, 1)
       if (lane == 0) tc::mbar_arrive(empty(slot));
 #pragma unroll
       for (int u = 0; u < C::WR; ++u) {
-        const float d = seg_sum<G>(q4_group_dot_b(wa[u], wb[u], xg, sv[u], bv[u]));
+        float d;
+        if constexpr (BITS == 8)
+          d = seg_sum<G>(q8_group_dot_b(wc[u], xg, sv[u], bv[u]));
+        else
+          d = seg_sum<G>(q4_group_dot_b(wc[u][0], wc[u][1], xg, sv[u], bv[u]));
         const int lr = (warp * C::WR + u) * C::RPS + rsub;
         if (g == 0 && lr < rows) {
           const int row = r0 + lr;
@@ -476,6 +491,31 @@ static int launch_k(const lily_q4_mat &W, int N, int K, const uint16_t *x, int32
     default: return LILY_Q4_ERR_UNSUPPORTED;
   }
   return LILY_Q4_OK;
+}
+
+template <int G>
+static void launch_q8_g(const lily_q4_mat &W, int N, const uint16_t *x, int32_t *token,
+                        float *logits, void *ws, const LmWsLayout &l, cudaStream_t st) {
+  char *base = static_cast<char *>(ws);
+  using C = LsCfg<G, 8>;
+  cudaFuncSetAttribute(gemv_argmax_stream_kernel<G, false, 8>,
+                       cudaFuncAttributeMaxDynamicSharedMemorySize, C::BYTES);
+  gemv_argmax_stream_kernel<G, false, 8><<<l.grid, kLsThreads, C::BYTES, st>>>(
+      W.w, W.s, W.b, N, l.rows_per_block, x, logits, token, reinterpret_cast<int32_t *>(base),
+      reinterpret_cast<float *>(base + l.off_partial_v),
+      reinterpret_cast<int32_t *>(base + l.off_partial_i), LseOut{});
+}
+
+int launch_q8_gemv_argmax(const lily_q4_mat &W, int N, int K, const uint16_t *x, int32_t *token,
+                          float *logits, void *ws, cudaStream_t st) {
+  const LmWsLayout l = lm_ws_layout(N, K, 8);
+  switch (K / kGroup) {
+    case 8: launch_q8_g<8>(W, N, x, token, logits, ws, l, st); break;
+    case 16: launch_q8_g<16>(W, N, x, token, logits, ws, l, st); break;
+    case 32: launch_q8_g<32>(W, N, x, token, logits, ws, l, st); break;
+    default: return LILY_Q4_ERR_UNSUPPORTED;
+  }
+  return check_launch();
 }
 
 int launch_gemv_argmax(const lily_q4_mat &W, int N, int K, const uint16_t *x, int32_t *token,

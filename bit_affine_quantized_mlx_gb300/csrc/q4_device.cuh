@@ -226,6 +226,76 @@ __device__ __forceinline__ float q4_group_dot_b(const uint4 w0, const uint4 w1, 
   return fmaf(s, q4_group_raw_b(w0, w1, g) - g.X128, b * g.X);
 }
 
+// ------------------------------------------------------------------ affine 8-bit codes
+// Four 8-bit codes per uint32, lowest byte first.  bf16 holds 128 + n exactly only for a
+// 4-bit n, so each code is taken as two nibbles, q = lo + 16 hi: one LOP3 with the magic
+// 0x4300 turns the low (or, after a 4-bit shift, high) nibbles of bytes 0 and 2 (or, after
+// an 8-bit shift, of bytes 1 and 3) into a bf16 pair, which multiplies the bf16 x pair
+// (x_j, x_j+2) in mixed-precision FMAs.  sum q x = (A_lo - 128 X) + 16 (A_hi - 128 X).
+// Per word (4 codes): three shifts, four LOP3, eight FMAs -- the 4-bit cost per code byte.
+
+// bf16 activations for 8-bit codes: one lane's 64 x values as the pairs (x_4m+j, x_4m+j+2),
+// j < 2, in word 2m + j, plus their sum.
+struct XGroup8 {
+  uint32_t xp[32];
+  float X128;  // 128 * sum of the 64 x values
+  float X;
+};
+
+// 64 bf16 values (8 x 16-byte chunks in K order) -> XGroup8.
+__device__ __forceinline__ void xgroup8_from_bf16(XGroup8 &g, const uint4 *chunks) {
+  float sum = 0.f;
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    const uint32_t w[4] = {chunks[c].x, chunks[c].y, chunks[c].z, chunks[c].w};
+    // w[i] = x[8c+2i] | x[8c+2i+1] << 16; word 2m+j of the group pairs x[4m+j] with x[4m+j+2]
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {  // the chunk's two 4-value words, m = 2c + h
+      const uint32_t a = w[2 * h], b = w[2 * h + 1];
+      g.xp[4 * c + 2 * h + 0] = (a & 0xFFFFu) | (b << 16);          // x[4m], x[4m+2]
+      g.xp[4 * c + 2 * h + 1] = (a >> 16) | (b & 0xFFFF0000u);      // x[4m+1], x[4m+3]
+      sum += __uint_as_float(a << 16) + __uint_as_float(a & 0xFFFF0000u) +
+             __uint_as_float(b << 16) + __uint_as_float(b & 0xFFFF0000u);
+    }
+  }
+  g.X = sum;
+  g.X128 = 128.0f * sum;
+}
+
+// s*(sum q x) + b*(sum x) for one 64-group of 8-bit codes (16 words in w[0..3]) and bf16 x.
+__device__ __forceinline__ float q8_group_dot_b(const uint4 (&wv)[4], const XGroup8 &g, float s,
+                                                float b) {
+  const uint32_t w[16] = {wv[0].x, wv[0].y, wv[0].z, wv[0].w, wv[1].x, wv[1].y, wv[1].z, wv[1].w,
+                          wv[2].x, wv[2].y, wv[2].z, wv[2].w, wv[3].x, wv[3].y, wv[3].z, wv[3].w};
+  float l0 = 0.f, l1 = 0.f, h0 = 0.f, h1 = 0.f;
+#pragma unroll
+  for (int m = 0; m < 16; ++m) {
+    uint32_t ws[4];
+    ws[0] = w[m];  // low nibbles of bytes 0, 2
+    asm("shr.b32 %0, %1, 8;" : "=r"(ws[1]) : "r"(w[m]));   // low nibbles of bytes 1, 3
+    asm("shr.b32 %0, %1, 4;" : "=r"(ws[2]) : "r"(w[m]));   // high nibbles of bytes 0, 2
+    asm("shr.b32 %0, %1, 12;" : "=r"(ws[3]) : "r"(w[m]));  // high nibbles of bytes 1, 3
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      uint32_t v;
+      asm("lop3.b32 %0, %1, 0x000F000F, 0x43004300, 0xEA;" : "=r"(v) : "r"(ws[j]));
+      const uint32_t xv = g.xp[2 * m + (j & 1)];
+      if (j < 2)
+        asm("{\n.reg .b16 vl, vh, xl, xh;\nmov.b32 {vl, vh}, %2;\nmov.b32 {xl, xh}, %3;\n"
+            "fma.rn.f32.bf16 %0, vl, xl, %0;\nfma.rn.f32.bf16 %1, vh, xh, %1;\n}"
+            : "+f"(l0), "+f"(l1)
+            : "r"(v), "r"(xv));
+      else
+        asm("{\n.reg .b16 vl, vh, xl, xh;\nmov.b32 {vl, vh}, %2;\nmov.b32 {xl, xh}, %3;\n"
+            "fma.rn.f32.bf16 %0, vl, xl, %0;\nfma.rn.f32.bf16 %1, vh, xh, %1;\n}"
+            : "+f"(h0), "+f"(h1)
+            : "r"(v), "r"(xv));
+    }
+  }
+  const float lo = (l0 + l1) - g.X128, hi = (h0 + h1) - g.X128;
+  return fmaf(s, fmaf(16.0f, hi, lo), b * g.X);
+}
+
 // Dot product of one dequantised 64-group with the prepared x: s*(sum q x) + b*(sum x).
 __device__ __forceinline__ float q4_group_dot(const uint4 w0, const uint4 w1, const XGroup &g,
                                               float s, float b) {

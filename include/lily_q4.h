@@ -159,6 +159,21 @@ LILY_Q4_API int lily_q4_gemv_argmax_logprobs(const lily_q4_mat *W, int32_t N, in
                                              lily_q4_stream_t stream);
 
 /*
+ * lily_q8_gemv_argmax -- lily_q4_gemv_argmax for an LM head kept at 8 bits (the fork page's
+ * q4-xl conversion, "The model", keeps the LM head, the shared expert and attention at 8
+ * bits; the report's checkpoint, "Hardware and software", keeps its router gates at 8 bits).
+ * Format: the same affine w = s*q + b with q in 0..255, four codes per uint32 along K,
+ * lowest byte first (code k of row n = (w[n][k/4] >> 8*(k%4)) & 255); s and b bf16
+ * [N][K/64] as for 4 bits.  W->w is uint32 [N][K/4].  K must be 512, 1024 or 2048
+ * (else LILY_Q4_ERR_UNSUPPORTED).  Arguments, results and errors otherwise as
+ * lily_q4_gemv_argmax; the workspace size comes from lily_q8_gemv_argmax_workspace_bytes.
+ */
+LILY_Q4_API int lily_q8_gemv_argmax(const lily_q4_mat *W, int32_t N, int32_t K, const uint16_t *x,
+                                    int32_t *token, float *logits, void *ws, size_t ws_bytes,
+                                    lily_q4_stream_t stream);
+LILY_Q4_API size_t lily_q8_gemv_argmax_workspace_bytes(int32_t N, int32_t K);
+
+/*
  * lily_q4_gemv_argmax_noalloc -- lily_q4_gemv_argmax for callers that cannot allocate.
  *
  * The paper has no counterpart: this entry point exists for callers that cannot call

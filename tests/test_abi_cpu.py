@@ -135,6 +135,20 @@ def test_gemv_logprobs_argument_errors(lib):
         q4.ERR_WORKSPACE_TOO_SMALL
 
 
+def test_q8_gemv_argument_errors(lib):
+    m = q4.lily_q4_mat(FAKE, FAKE + 4096, FAKE + 8192)
+    f = lib.lily_q8_gemv_argmax
+    ws = FAKE + (1 << 30)
+    assert f(None, 10, 2048, FAKE, FAKE, None, ws, 1 << 20, None) == q4.ERR_INVALID_ARG
+    assert f(C.byref(m), 10, 100, FAKE, FAKE, None, ws, 1 << 20, None) == q4.ERR_INVALID_ARG
+    assert f(C.byref(m), 10, 256, FAKE, FAKE, None, ws, 1 << 20, None) == q4.ERR_UNSUPPORTED
+    assert f(C.byref(m), 10, 4096, FAKE, FAKE, None, ws, 1 << 20, None) == q4.ERR_UNSUPPORTED
+    assert f(C.byref(m), 10, 2048, FAKE, None, None, ws, 1 << 20, None) == q4.ERR_INVALID_ARG
+    assert f(C.byref(m), 10, 2048, FAKE, FAKE, None, ws, 16, None) == q4.ERR_WORKSPACE_TOO_SMALL
+    assert lib.lily_q8_gemv_argmax_workspace_bytes(151936, 2048) > 0
+    assert lib.lily_q8_gemv_argmax_workspace_bytes(10, 100) == 0
+
+
 def test_workspace_sizes(lib):
     L = _fake_layer()
     d1 = lib.lily_q4_moe_workspace_bytes(C.byref(L), 1, 0)

@@ -164,3 +164,66 @@ def test_logprobs_full_size(torch_dev):
     assert a[0] == b[0] and a[1] == b[1] and np.array_equal(a[2], b[2])
     # the argmax-only call on the same inputs picks the same token
     assert _run(torch, dev, W, x, with_logits=False)[0] == tok
+
+
+# ----------------------------------------------------------------------------- 8-bit LM head
+
+def _run_q8(torch, dev, W, x_bits, with_logits=True):
+    N, K = W.N, W.K
+    dW = q4.DeviceQ4.upload(W, dev)
+    xd = q4.to_device(x_bits, dev)
+    tok = torch.full((1,), -7, dtype=torch.int32, device=dev)
+    lg = torch.empty(N, dtype=torch.float32, device=dev) if with_logits else None
+    ws = q4.new_workspace(q4.lily_q8_gemv_argmax_workspace_bytes(N, K), dev)
+    q4.lily_q8_gemv_argmax(dW, xd, tok, logits=lg, ws=ws)
+    torch.cuda.synchronize()
+    return int(tok.item()), (lg.cpu().numpy().astype(np.float64) if with_logits else None)
+
+
+@pytest.mark.parametrize("N,K", [(1, 512), (37, 1024), (4097, 512), (333, 2048), (7297, 2048),
+                                 (50001, 2048)])
+def test_q8_shapes(torch_dev, N, K):
+    torch, dev = torch_dev
+    W = synth.draw_q8(N, K, 65, N, K)
+    if N == 1:
+        x = synth.draw_x(K, (65, N), 0, 0)
+        tok, lg = orc.q8_lm_head(W, x)
+    else:
+        x, _, tok, lg = orc.lm_x_without_near_tie(W, lambda a: synth.draw_x(K, (65, N), 0, a),
+                                                  head=orc.q8_lm_head)
+    got_tok, got_lg = _run_q8(torch, dev, W, x)
+    assert got_tok == tok
+    assert_close(got_lg, lg, f"8-bit logits N={N} K={K}")
+
+
+def test_q8_full_size_lm_head(torch_dev):
+    """An 8-bit LM head of vocabulary 151,936 x hidden 2048 (the q4-xl conversion's), every
+    logit checked; the token also without the logits output; two calls identical."""
+    torch, dev = torch_dev
+    wl = synth.LMHEAD
+    W = synth.draw_lm_head_q8(wl.V, wl.H)
+    x, _, tok, lg = orc.lm_x_without_near_tie(W, lambda a: synth.draw_lm_x(wl.H, attempt=a),
+                                              head=orc.q8_lm_head)
+    a = _run_q8(torch, dev, W, x)
+    assert a[0] == tok
+    assert_close(a[1], lg, "full 8-bit LM head")
+    assert _run_q8(torch, dev, W, x, with_logits=False)[0] == tok
+    b = _run_q8(torch, dev, W, x)
+    assert np.array_equal(a[1], b[1])
+
+
+def test_q8_planted_tie_goes_to_lower_index(torch_dev):
+    torch, dev = torch_dev
+    N, K = 3000, 512
+    W = synth.draw_q8(N, K, 66, 0)
+    w, s, b = W.w.copy(), W.s.copy(), W.b.copy()
+    for r in (2345, 1234):
+        w[r] = 0xFFFFFFFF
+        s[r] = synth.bf16_from_f32(np.float32(0.003))
+        b[r] = 0
+    x = np.full(K, synth.bf16_from_f32(np.float32(0.5)).item(), np.uint16)
+    W2 = synth.Q8Matrix(w, s, b)
+    tok, lg = orc.q8_lm_head(W2, x)
+    assert tok == 1234 and lg[1234] == lg[2345]
+    got_tok, got_lg = _run_q8(torch, dev, W2, x)
+    assert got_tok == 1234 and got_lg[1234] == got_lg[2345]
