@@ -606,14 +606,22 @@ __global__ void __launch_bounds__(256) topk_prefill_kernel(TopkArgs a) {
   const int lane = threadIdx.x & 31;
   const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
   if (t >= a.T) return;
+  // every partial logit of the lane is loaded before any is summed (the split count is at most
+  // kRouterSplit(H) = 4), then the partials are summed in split order
   float lv[EC];
 #pragma unroll
   for (int j = 0; j < EC; ++j) {
     const int e = lane + 32 * j;
+    float pv[4];
+#pragma unroll
+    for (int sp = 0; sp < 4; ++sp)
+      pv[sp] = (sp < a.nsplit && e < a.E) ? __ldcg(a.logits + ((size_t)sp * a.T + t) * a.E + e) : 0.f;
     float v = -INFINITY;
     if (e < a.E) {
       v = 0.f;
-      for (int sp = 0; sp < a.nsplit; ++sp) v += a.logits[((size_t)sp * a.T + t) * a.E + e];
+#pragma unroll
+      for (int sp = 0; sp < 4; ++sp)
+        if (sp < a.nsplit) v += pv[sp];
       if (a.bias) v += a.bias[e];
       v = cand(v);
     }
@@ -644,10 +652,18 @@ __global__ void __launch_bounds__(256) topk_prefill_kernel(TopkArgs a) {
   if (a.has_shared) {
     const uint16_t *xt = a.x + (size_t)t * a.H;
     float acc = 0.f;
-    for (int h = lane * 8; h < a.H; h += 256) {
-      const uint4 xv = __ldg(reinterpret_cast<const uint4 *>(xt + h));
-      const uint4 gv = __ldg(reinterpret_cast<const uint4 *>(a.shared_gate + h));
-      const uint32_t xx[4] = {xv.x, xv.y, xv.z, xv.w}, gg[4] = {gv.x, gv.y, gv.z, gv.w};
+    // H <= 2048: at most 8 chunks per lane, all loaded before the dot products
+    uint4 xv[8], gv[8];
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      const int h = lane * 8 + 256 * c;
+      xv[c] = h < a.H ? __ldg(reinterpret_cast<const uint4 *>(xt + h)) : make_uint4(0, 0, 0, 0);
+      gv[c] = h < a.H ? __ldg(reinterpret_cast<const uint4 *>(a.shared_gate + h)) : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      if (lane * 8 + 256 * c >= a.H) break;
+      const uint32_t xx[4] = {xv[c].x, xv[c].y, xv[c].z, xv[c].w}, gg[4] = {gv[c].x, gv[c].y, gv[c].z, gv[c].w};
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         acc = fmaf(__uint_as_float(xx[i] << 16), __uint_as_float(gg[i] << 16), acc);
@@ -775,7 +791,20 @@ __global__ void __launch_bounds__(kPermThreads) perm_kernel(PermArgs a) {
   const int n = a.T * a.k;
   const bool staged = n <= kPermStaged;
   if (staged) {
-    for (int j = threadIdx.x; j < n; j += blockDim.x) s_idx[j] = __ldg(a.idx + j);
+    // eight loads in flight per thread before any store
+    for (int j0 = threadIdx.x; j0 < n; j0 += kPermThreads * 8) {
+      int v[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int j = j0 + u * kPermThreads;
+        v[u] = j < n ? __ldg(a.idx + j) : 0;
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int j = j0 + u * kPermThreads;
+        if (j < n) s_idx[j] = v[u];
+      }
+    }
     __syncthreads();
   }
   const int32_t *idx = staged ? s_idx : a.idx;
