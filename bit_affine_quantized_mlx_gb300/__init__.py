@@ -84,6 +84,7 @@ def load(path: Optional[str] = None):
     L.lily_q8_gemv_argmax_workspace_bytes.argtypes = [i32, i32]
     L.lily_q8_gemv_argmax_workspace_bytes.restype = sz
     L.lily_q4_workspace_init.argtypes = [vp, sz, vp]
+    L.lily_q4_selftest_timeout.argtypes = [vp, sz, i32, vp]
     L.lily_q4_workspace_status.argtypes = [vp, vp]
     L.lily_q4_status_string.argtypes = [C.c_int]
     L.lily_q4_status_string.restype = C.c_char_p
@@ -93,7 +94,7 @@ def load(path: Optional[str] = None):
               "lily_q4_workspace_init", "lily_q4_workspace_status", "lily_q4_pack",
               "lily_q4_unpack", "lily_q4_version", "lily_q4_moe_launches",
               "lily_q4_gemv_argmax_noalloc", "lily_q4_gemv_argmax_logprobs",
-              "lily_q8_gemv_argmax"):
+              "lily_q8_gemv_argmax", "lily_q4_selftest_timeout"):
         getattr(L, f).restype = C.c_int
     _lib = L
     return L
@@ -271,6 +272,13 @@ def lily_q8_gemv_argmax(W, x, token, logits=None, ws=None, stream=None):
     return _check(load().lily_q8_gemv_argmax(C.byref(m), N, K, _ptr(x), _ptr(token), _ptr(logits),
                                              _ptr(ws), ws.numel() if ws is not None else 0,
                                              _stream(stream)), "lily_q8_gemv_argmax")
+
+
+def lily_q4_selftest_timeout(ws, which: int, stream=None):
+    """Enqueue a wait that runs into its bound (which 0: grid barrier, 1: mbarrier); see
+    include/lily_q4.h."""
+    return _check(load().lily_q4_selftest_timeout(_ptr(ws), ws.numel(), int(which), _stream(stream)),
+                  "lily_q4_selftest_timeout")
 
 
 def lily_q8_gemv_argmax_workspace_bytes(N: int, K: int) -> int:

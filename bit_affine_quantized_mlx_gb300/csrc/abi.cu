@@ -150,6 +150,12 @@ int lily_q4_workspace_status(void *ws, lily_q4_stream_t stream) {
   return LILY_Q4_OK;
 }
 
+int lily_q4_selftest_timeout(void *ws, size_t ws_bytes, int32_t which, lily_q4_stream_t stream) {
+  if (!ws || ws_bytes < kAlign || !aligned(ws, kAlign)) return LILY_Q4_ERR_INVALID_ARG;
+  if (which != 0 && which != 1) return LILY_Q4_ERR_INVALID_ARG;
+  return selftest_wait(ws, which, (cudaStream_t)stream);
+}
+
 int lily_q4_gemv_argmax(const lily_q4_mat *W, int32_t N, int32_t K, const uint16_t *x,
                         int32_t *token, float *logits, void *ws, size_t ws_bytes,
                         lily_q4_stream_t stream) {

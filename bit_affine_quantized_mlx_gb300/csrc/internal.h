@@ -55,6 +55,9 @@ struct DecodeWsLayout {
 };
 DecodeWsLayout decode_ws_layout(const lily_q4_moe_layer &L, int T);
 int decode_launch_count(const lily_q4_moe_layer &L, int T);
+// One block waiting on a grid barrier (which = 0) or an mbarrier (1) that never completes,
+// until the bound; records the time-out in the workspace header.
+int selftest_wait(void *ws, int which, cudaStream_t st);
 int launch_moe_decode(const lily_q4_moe_layer &L, const uint16_t *x, int T, uint16_t *y,
                       int32_t *topk_idx, float *topk_w, void *ws, cudaStream_t st);
 

@@ -625,6 +625,34 @@ __device__ bool grid_barrier(int32_t *hdr, unsigned long long target, volatile i
   return !*s_abort;
 }
 
+// Diagnostic for the bounded waits: one block waits on something nothing provides -- a grid
+// barrier whose target no arrival reaches (which = 0) or an mbarrier phase nothing completes
+// (which = 1) -- until the wait's bound, then records the time-out in the workspace header as a
+// stalled launch of the library would.
+__global__ void selftest_wait_kernel(int32_t *hdr, int which) {
+  __shared__ volatile int s_abort;
+  __shared__ __align__(8) unsigned long long s_bar;
+  if (threadIdx.x == 0) s_abort = 0;
+  __syncthreads();
+  if (which == 0) {
+    const unsigned long long base = barrier_base(hdr);
+    grid_barrier(hdr, base + 1000ull * gridDim.x, &s_abort);
+  } else {
+    const uint32_t b = tc::smem_u32(&s_bar);
+    if (threadIdx.x == 0) {
+      tc::mbar_init(b, 1);
+      tc::mbar_init_fence();
+    }
+    __syncthreads();
+    tc::wait_bar(b, 0, &s_abort, hdr + kHdrError);
+  }
+}
+
+int selftest_wait(void *ws, int which, cudaStream_t st) {
+  selftest_wait_kernel<<<1, 32, 0, st>>>(static_cast<int32_t *>(ws), which);
+  return check_launch();
+}
+
 // Routing of up to 4 tokens by one block, for the single-launch path: warps 0..T-1 take
 // the top-k of one token each; warp 0 then builds the unique-expert table with a bitmap
 // of selected experts (ascending id) and places the (token, weight) pairs.

@@ -219,6 +219,19 @@ LILY_Q4_API int lily_q4_workspace_init(void *ws, size_t ws_bytes, lily_q4_stream
  * last check. */
 LILY_Q4_API int lily_q4_workspace_status(void *ws, lily_q4_stream_t stream);
 
+/*
+ * lily_q4_selftest_timeout -- diagnostic of the bounded device-side waits.  Enqueues on
+ * `stream` one single-block kernel that waits on something nothing provides -- which = 0: a
+ * grid barrier on the workspace's arrival counter whose target no arrival reaches; which = 1:
+ * an mbarrier phase that nothing completes -- until the wait's bound (about 1 s and 2 s of
+ * SM clock), then records the time-out in the workspace header and exits, as a stalled launch
+ * of this library would.  lily_q4_workspace_status then returns LILY_Q4_ERR_TIMEOUT.
+ * Afterwards the workspace's barrier count is off: re-initialise it (lily_q4_workspace_init)
+ * before the next decode.  ws: any workspace of at least 256 bytes.
+ */
+LILY_Q4_API int lily_q4_selftest_timeout(void *ws, size_t ws_bytes, int32_t which,
+                                         lily_q4_stream_t stream);
+
 /* Human-readable name of a status code (static string). */
 LILY_Q4_API const char *lily_q4_status_string(int status);
 

@@ -149,6 +149,14 @@ def test_q8_gemv_argument_errors(lib):
     assert lib.lily_q8_gemv_argmax_workspace_bytes(10, 100) == 0
 
 
+def test_selftest_argument_errors(lib):
+    f = lib.lily_q4_selftest_timeout
+    assert f(None, 1024, 0, None) == q4.ERR_INVALID_ARG
+    assert f(FAKE + 16, 1024, 0, None) == q4.ERR_INVALID_ARG     # not 256-aligned
+    assert f(FAKE, 64, 0, None) == q4.ERR_INVALID_ARG            # smaller than the header
+    assert f(FAKE, 1024, 2, None) == q4.ERR_INVALID_ARG          # no such wait
+
+
 def test_workspace_sizes(lib):
     L = _fake_layer()
     d1 = lib.lily_q4_moe_workspace_bytes(C.byref(L), 1, 0)

@@ -134,3 +134,22 @@ def test_non_finite_logits_select_lowest_experts(torch_dev, H, I, T):
     _, idx, _ = run_decode(torch, dev, dl, x)
     for t in range(T):
         assert sorted(idx[t].tolist()) == [0, 1, 2, 3]
+
+
+@pytest.mark.parametrize("which", [0, 1])
+def test_bounded_wait_reports_timeout_and_context_stays_usable(torch_dev, which):
+    """A wait that nothing completes (0: the decode kernel's grid barrier, 1: an mbarrier as in
+    the prefill GEMM and LM head) gives up at its bound and is reported as a time-out through
+    the workspace; after re-initialising the workspace the same context decodes correctly."""
+    torch, dev = torch_dev
+    wl = synth.TINY
+    L = wl.layer(0)
+    dl = q4.DeviceLayer.upload(L, dev)
+    x = _inputs(L, wl.tokens_key(0), 1)
+    ws = q4.new_workspace(q4.lily_q4_moe_workspace_bytes(dl, 1), dev)
+    q4.lily_q4_selftest_timeout(ws, which)
+    assert q4.lily_q4_workspace_status(ws) == q4.ERR_TIMEOUT
+    assert q4.lily_q4_workspace_status(ws) == q4.OK   # the status word is cleared on read
+    q4.lily_q4_workspace_init(ws)
+    check(torch, dev, L, x, f"decode after a time-out ({which})", ws=ws, dl=dl)
+    assert q4.lily_q4_workspace_status(ws) == q4.OK
