@@ -903,7 +903,9 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
   // the workspace).
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  if (threadIdx.x == 0) {
+  // The barrier base is read by the last warp, which has no phase-A rows: the acquire load
+  // holds up only that warp while the others issue their weight loads.
+  if (threadIdx.x == kFusedThreads - 32) {
     s_abort = 0;
     s_bbase = barrier_base(w.hdr);
   }
