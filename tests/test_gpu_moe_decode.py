@@ -64,10 +64,11 @@ def test_tiny_workload_seed0(torch_dev):
     (1024, 64, 16, 128, True, True, 2),   # largest k
     (2048, 40, 3, 2048, True, False, 2),  # widest intermediate
     (256, 1024, 5, 128, True, False, 3),  # most experts
-    # hidden 2048 / intermediate 512: the single-launch cluster path
-    (2048, 64, 16, 512, True, True, 4),   # top-16 of 64, 4 tokens: several units per cluster
+    # hidden 2048 / intermediate 512: the single-launch path (batch <= 4)
+    (2048, 64, 16, 512, True, True, 4),   # top-16 of 64, 4 tokens: beyond the staged down tasks
     (2048, 8, 2, 512, False, False, 3),   # one router row per CTA, no shared expert
     (2048, 24, 3, 512, True, False, 2),   # a partial router chunk
+    (2048, 256, 8, 512, True, False, 16),  # decode shapes at the largest batch (three launches)
 ])
 def test_shapes(torch_dev, H, E, k, I, shared, bias, T):
     torch, dev = torch_dev

@@ -46,6 +46,7 @@ def run_prefill(torch, dev, dl, x_bits, ws=None):
     (512, 32, 8, 128, False, True, 129),
     (2048, 4, 2, 512, True, False, 1),      # a single token
     (256, 64, 6, 1024, True, True, 200),
+    (256, 32, 8, 128, True, False, 8192),   # the largest chunk: selections not staged in bucketing
 ])
 def test_shapes(torch_dev, H, E, k, I, shared, bias, T):
     torch, dev = torch_dev
