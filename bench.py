@@ -34,7 +34,7 @@ EXPERT_BYTES = 1769472  # gate + up + down of one expert at H=2048, I=512 (codes
 # DRAM bytes (read + write) of one single-launch decode-layer kernel at batch 1, from the ncu
 # capture summarised in profiles/moe_decode_fused_decode-layer_H2048_E256_k8.md.  Set to None
 # whenever that kernel changes until it is captured again.
-DECODE_TRAFFIC_BYTES = 17058048  # ncu dram__bytes_read+write of one moe_decode_fused launch
+DECODE_TRAFFIC_BYTES = 17057792  # ncu dram__bytes_read+write of one moe_decode_fused launch
 
 
 def peaks():
