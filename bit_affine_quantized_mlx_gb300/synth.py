@@ -37,6 +37,8 @@ S_SH_GATE, S_SH_UP, S_SH_DOWN = 20, 21, 22
 S_X = 100
 S_LM = 30
 S_LM8 = 31
+S_ROUTER8 = 4
+S_SH_GATE8, S_SH_UP8, S_SH_DOWN8 = 24, 25, 26
 
 
 def bf16_from_f32(a) -> np.ndarray:
@@ -160,10 +162,21 @@ class MoELayer:
     sh_up: Optional[Q4Matrix] = None         # [I, H]
     sh_down: Optional[Q4Matrix] = None       # [H, I]
     shared_gate: Optional[np.ndarray] = None  # uint16 bf16 [H]
+    router_q8: Optional["Q8Matrix"] = None   # [E, H] affine 8-bit router (replaces router)
 
     @property
     def has_shared(self) -> bool:
         return self.sh_gate is not None
+
+    @property
+    def shared_bits(self) -> int:
+        """Code width of the shared expert: 8 for Q8Matrix matrices (q4-xl), else 4."""
+        return 8 if isinstance(self.sh_gate, Q8Matrix) else 4
+
+    @property
+    def router_bits(self) -> int:
+        """16 for the bf16 router, 8 for an affine 8-bit router."""
+        return 8 if self.router_q8 is not None else 16
 
     def expert_bytes(self) -> int:
         """Bytes of one routed expert (gate + up + down, codes and scales)."""
@@ -171,8 +184,11 @@ class MoELayer:
 
 
 def draw_layer(H: int, E: int, k: int, I: int, *, shared: bool, router_std: float,
-               router_bias: bool, key: Tuple[int, ...]) -> MoELayer:
-    """Draw one MoE layer.  ``key`` = (workload id, layer index)."""
+               router_bias: bool, key: Tuple[int, ...], router_bits: int = 16,
+               shared_bits: int = 4) -> MoELayer:
+    """Draw one MoE layer.  ``key`` = (workload id, layer index).  router_bits = 8 draws an
+    affine 8-bit router (the checkpoint's router gates); shared_bits = 8 an 8-bit shared expert
+    (the q4-xl conversion)."""
     gate = draw_q4_stack(E, I, H, *key, S_GATE)
     up = draw_q4_stack(E, I, H, *key, S_UP)
     down = draw_q4_stack(E, H, I, *key, S_DOWN)
@@ -181,10 +197,18 @@ def draw_layer(H: int, E: int, k: int, I: int, *, shared: bool, router_std: floa
     if router_bias:
         rb = _rng(*key, S_RBIAS).normal(0.0, 1.0, size=E).astype(np.float32)
     L = MoELayer(H, E, k, I, gate, up, down, router, rb)
+    if router_bits == 8:
+        L.router = None
+        L.router_q8 = draw_q8(E, H, *key, S_ROUTER8)
     if shared:
-        L.sh_gate = draw_q4(I, H, *key, S_SH_GATE)
-        L.sh_up = draw_q4(I, H, *key, S_SH_UP)
-        L.sh_down = draw_q4(H, I, *key, S_SH_DOWN)
+        if shared_bits == 8:
+            L.sh_gate = draw_q8(I, H, *key, S_SH_GATE8)
+            L.sh_up = draw_q8(I, H, *key, S_SH_UP8)
+            L.sh_down = draw_q8(H, I, *key, S_SH_DOWN8)
+        else:
+            L.sh_gate = draw_q4(I, H, *key, S_SH_GATE)
+            L.sh_up = draw_q4(I, H, *key, S_SH_UP)
+            L.sh_down = draw_q4(H, I, *key, S_SH_DOWN)
         L.shared_gate = draw_bf16_normal((H,), 0.05, *key, S_GSHARED)
     return L
 

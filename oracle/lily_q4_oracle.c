@@ -131,6 +131,17 @@ void orc_q8_dequant(const uint32_t *w, const uint16_t *s, const uint16_t *b,
             out[(size_t)n * K + k] = orc_weight8(w, s, b, K, n, k);
 }
 
+/* out[n] = sum_k W^[n,k] x[k] for an 8-bit matrix, x given in fp64. */
+void orc_q8_matvec(const uint32_t *w, const uint16_t *s, const uint16_t *b,
+                   int N, int K, const double *x, double *out) {
+    for (int n = 0; n < N; ++n) {
+        double acc = 0.0;
+        for (int k = 0; k < K; ++k)
+            acc += orc_weight8(w, s, b, K, n, k) * x[k];
+        out[n] = acc;
+    }
+}
+
 /* 8-bit LM head: logits[n] for bf16 x (rows split over threads); returns the argmax
  * (ties to the lower id). */
 int orc_q8_lm_head(const uint32_t *w, const uint16_t *s, const uint16_t *b,
@@ -275,21 +286,37 @@ double orc_sigmoid_gate(const uint16_t *g, int H, const uint16_t *x) {
     return 1.0 / (1.0 + exp(-acc));
 }
 
-/* One SwiGLU expert: o[H] = Wd (silu(Wg x) * (Wu x)); gate/up [I x H], down [H x I]. */
+/* W^ x for 4-bit (bits = 4) or 8-bit (bits = 8) codes. */
+static void orc_matvec_bits(int bits, const uint32_t *w, const uint16_t *s, const uint16_t *b,
+                            int N, int K, const double *x, double *out) {
+    if (bits == 8) orc_q8_matvec(w, s, b, N, K, x, out);
+    else orc_q4_matvec(w, s, b, N, K, x, out);
+}
+
+/* One SwiGLU expert with codes of `bits` bits: o[H] = Wd (silu(Wg x) * (Wu x)); gate/up
+ * [I x H], down [H x I]. */
+static void orc_expert_bits(int bits, const uint32_t *gw, const uint16_t *gs, const uint16_t *gb,
+                            const uint32_t *uw, const uint16_t *us, const uint16_t *ub,
+                            const uint32_t *dw, const uint16_t *ds, const uint16_t *db,
+                            int H, int I, const double *x, double *o) {
+    double *g = (double *)malloc(sizeof(double) * (size_t)I);
+    double *u = (double *)malloc(sizeof(double) * (size_t)I);
+    double *h = (double *)malloc(sizeof(double) * (size_t)I);
+    orc_matvec_bits(bits, gw, gs, gb, I, H, x, g);
+    orc_matvec_bits(bits, uw, us, ub, I, H, x, u);
+    for (int i = 0; i < I; ++i) h[i] = g[i] / (1.0 + exp(-g[i])) * u[i];
+    orc_matvec_bits(bits, dw, ds, db, H, I, h, o);
+    free(g);
+    free(u);
+    free(h);
+}
+
+/* One SwiGLU expert with 4-bit codes. */
 void orc_expert(const uint32_t *gw, const uint16_t *gs, const uint16_t *gb,
                 const uint32_t *uw, const uint16_t *us, const uint16_t *ub,
                 const uint32_t *dw, const uint16_t *ds, const uint16_t *db,
                 int H, int I, const double *x, double *o) {
-    double *g = (double *)malloc(sizeof(double) * (size_t)I);
-    double *u = (double *)malloc(sizeof(double) * (size_t)I);
-    double *h = (double *)malloc(sizeof(double) * (size_t)I);
-    orc_q4_matvec(gw, gs, gb, I, H, x, g);
-    orc_q4_matvec(uw, us, ub, I, H, x, u);
-    for (int i = 0; i < I; ++i) h[i] = g[i] / (1.0 + exp(-g[i])) * u[i];
-    orc_q4_matvec(dw, ds, db, H, I, h, o);
-    free(g);
-    free(u);
-    free(h);
+    orc_expert_bits(4, gw, gs, gb, uw, us, ub, dw, ds, db, H, I, x, o);
 }
 
 typedef struct {
@@ -303,10 +330,30 @@ typedef struct {
     orc_mat gate, up, down;          /* stacked over E: [E][N][..] */
     int32_t has_shared;
     orc_mat sh_gate, sh_up, sh_down; /* single matrices */
-    const uint16_t *router;          /* bf16 [E][H] */
+    const uint16_t *router;          /* bf16 [E][H] (router_bits 16) */
     const float *router_bias;        /* fp32 [E] or NULL */
     const uint16_t *shared_gate;     /* bf16 [H] or NULL */
+    int32_t shared_bits;             /* 4 (or 0) or 8: codes of the shared expert */
+    int32_t router_bits;             /* 16 (or 0): bf16 router; 8: router8 */
+    orc_mat router8;                 /* affine 8-bit router [E][H/4] codes, [E][H/64] s, b */
 } orc_layer;
+
+/* Router logits of one token from an affine 8-bit router, fp64 (+ offsets). */
+static void orc_router8(const orc_mat *R, const float *bias, int E, int H, const uint16_t *x,
+                        double *logits) {
+    for (int e = 0; e < E; ++e) {
+        double acc = 0.0;
+        for (int h = 0; h < H; ++h)
+            acc += orc_weight8(R->w, R->s, R->b, H, e, h) * (double)orc_bf16(x[h]);
+        if (bias) acc += (double)bias[e];
+        logits[e] = acc;
+    }
+}
+
+static void orc_layer_router(const orc_layer *L, const uint16_t *xt, double *lg) {
+    if (L->router_bits == 8) orc_router8(&L->router8, L->router_bias, L->E, L->H, xt, lg);
+    else orc_router(L->router, L->router_bias, L->E, L->H, xt, lg);
+}
 
 static orc_mat orc_expert_mat(orc_mat m, int e, int N, int K) {
     orc_mat r;
@@ -330,7 +377,7 @@ void orc_moe(const orc_layer *L, const uint16_t *x, int T, double *y,
         int32_t *idx = (int32_t *)malloc(sizeof(int32_t) * (size_t)k);
         double *p = (double *)malloc(sizeof(double) * (size_t)k);
         for (int h = 0; h < H; ++h) xd[h] = (double)orc_bf16(xt[h]);
-        orc_router(L->router, L->router_bias, E, H, xt, lg);
+        orc_layer_router(L, xt, lg);
         orc_topk(lg, E, k, idx, p);
         double *yt = y + (size_t)t * H;
         for (int h = 0; h < H; ++h) yt[h] = 0.0;
@@ -345,8 +392,9 @@ void orc_moe(const orc_layer *L, const uint16_t *x, int T, double *y,
         double sigma = 0.0;
         if (L->has_shared) {
             sigma = orc_sigmoid_gate(L->shared_gate, H, xt);
-            orc_expert(L->sh_gate.w, L->sh_gate.s, L->sh_gate.b, L->sh_up.w, L->sh_up.s,
-                       L->sh_up.b, L->sh_down.w, L->sh_down.s, L->sh_down.b, H, I, xd, o);
+            orc_expert_bits(L->shared_bits == 8 ? 8 : 4, L->sh_gate.w, L->sh_gate.s, L->sh_gate.b,
+                            L->sh_up.w, L->sh_up.s, L->sh_up.b, L->sh_down.w, L->sh_down.s,
+                            L->sh_down.b, H, I, xd, o);
             for (int h = 0; h < H; ++h) yt[h] += sigma * o[h];
         }
         if (idx_out) memcpy(idx_out + (size_t)t * k, idx, sizeof(int32_t) * (size_t)k);
@@ -365,6 +413,5 @@ void orc_moe(const orc_layer *L, const uint16_t *x, int T, double *y,
 void orc_router_tokens(const orc_layer *L, const uint16_t *x, int T, double *logits) {
 #pragma omp parallel for schedule(static)
     for (int t = 0; t < T; ++t)
-        orc_router(L->router, L->router_bias, L->E, L->H, x + (size_t)t * L->H,
-                   logits + (size_t)t * L->E);
+        orc_layer_router(L, x + (size_t)t * L->H, logits + (size_t)t * L->E);
 }

@@ -45,7 +45,8 @@ class _Layer(C.Structure):
                 ("has_shared", C.c_int32),
                 ("sh_gate", _Mat), ("sh_up", _Mat), ("sh_down", _Mat),
                 ("router", C.c_void_p), ("router_bias", C.c_void_p),
-                ("shared_gate", C.c_void_p)]
+                ("shared_gate", C.c_void_p),
+                ("shared_bits", C.c_int32), ("router_bits", C.c_int32), ("router8", _Mat)]
 
 
 def lib():
@@ -262,6 +263,9 @@ def _layer_struct(L) -> Tuple[_Layer, _Keep]:
     st.router = keep.ptr(L.router, np.uint16)
     st.router_bias = keep.ptr(L.router_bias, np.float32)
     st.shared_gate = keep.ptr(L.shared_gate, np.uint16)
+    st.shared_bits = getattr(L, "shared_bits", 4)
+    st.router_bits = getattr(L, "router_bits", 16)
+    st.router8 = mat(getattr(L, "router_q8", None))
     return st, keep
 
 

@@ -260,9 +260,23 @@ def _np_dense(m):
     return (s * q.astype(np.float32) + b).astype(np.float64)
 
 
+def _np_dense8(m):
+    """Independent dense dequantisation of 8-bit codes with numpy byte views."""
+    w = np.ascontiguousarray(m.w, np.uint32)
+    q = w.astype("<u4").view(np.uint8).reshape(*w.shape[:-1], w.shape[-1] * 4)  # little-endian bytes
+    s = np.repeat(bf16_to_f32(m.s), 64, axis=-1)
+    b = np.repeat(bf16_to_f32(m.b), 64, axis=-1)
+    return (s * q.astype(np.float32) + b).astype(np.float64)
+
+
+def _np_any(m):
+    return _np_dense8(m) if isinstance(m, synth.Q8Matrix) else _np_dense(m)
+
+
 def _np_moe(L, x_bits):
     x = bf16_to_f32(x_bits).astype(np.float64)
-    lg = x @ bf16_to_f32(L.router).astype(np.float64).T
+    R = _np_dense8(L.router_q8) if L.router_q8 is not None else bf16_to_f32(L.router).astype(np.float64)
+    lg = x @ R.T
     if L.router_bias is not None:
         lg = lg + L.router_bias.astype(np.float64)
     G, U, D = _np_dense(L.gate), _np_dense(L.up), _np_dense(L.down)
@@ -277,9 +291,9 @@ def _np_moe(L, x_bits):
             y[t] += wi * np.einsum("hi,i->h", D[e], g * sp.expit(g) * u)
         if L.has_shared:
             sg = sp.expit(bf16_to_f32(L.shared_gate).astype(np.float64) @ x[t])
-            g = _np_dense(L.sh_gate) @ x[t]
-            u = _np_dense(L.sh_up) @ x[t]
-            y[t] += sg * (_np_dense(L.sh_down) @ (g * sp.expit(g) * u))
+            g = _np_any(L.sh_gate) @ x[t]
+            u = _np_any(L.sh_up) @ x[t]
+            y[t] += sg * (_np_any(L.sh_down) @ (g * sp.expit(g) * u))
     return y
 
 
@@ -292,6 +306,24 @@ def test_whole_layer_vs_independent_numpy(H, E, k, I, shared, bias):
     got = orc.moe(L, x)["y"]
     want = _np_moe(L, x)
     np.testing.assert_allclose(got, want, rtol=1e-12, atol=1e-12 * np.abs(want).max())
+
+
+@pytest.mark.parametrize("router_bits,shared_bits", [(8, 4), (16, 8), (8, 8)])
+def test_whole_layer_8bit_parts_vs_independent_numpy(router_bits, shared_bits):
+    """An 8-bit router (the checkpoint's router gates) and/or an 8-bit shared expert (q4-xl):
+    the oracle layer against numpy with byte-view dequantisation (catches the 8-bit parts read
+    as 4-bit, or the bf16 router used in place of the 8-bit one)."""
+    L = synth.draw_layer(128, 8, 3, 64, shared=True, router_std=0.05, router_bias=True,
+                         key=(93, router_bits + shared_bits), router_bits=router_bits,
+                         shared_bits=shared_bits)
+    assert L.router_bits == router_bits and L.shared_bits == shared_bits
+    x = synth.draw_tokens(128, 3, (93, 1))
+    out = orc.moe(L, x)
+    want = _np_moe(L, x)
+    np.testing.assert_allclose(out["y"], want, rtol=1e-12, atol=1e-12 * np.abs(want).max())
+    R = _np_dense8(L.router_q8) if router_bits == 8 else bf16_to_f32(L.router).astype(np.float64)
+    lg = bf16_to_f32(x).astype(np.float64) @ R.T + L.router_bias.astype(np.float64)
+    np.testing.assert_allclose(out["logits"], lg, rtol=1e-12, atol=1e-12)
 
 
 def test_moe_tokens_independent():
