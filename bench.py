@@ -347,6 +347,33 @@ def run_gb300(args):
     q8_gbs = q8_bytes / (q8_mean / 1e3) / 1e9
     del W8, ws8
 
+    # ---- decode layers in the q4-xl layout (8-bit router and shared expert), batch 1: eight
+    # independently seeded layers (3.6 GB, beyond L2) cycled, stream launches as above
+    xl_layers = [q4.DeviceLayer.upload(synth.draw_layer(wl.H, wl.E, wl.k, wl.I, shared=True,
+                                                        router_std=0.02, router_bias=False,
+                                                        key=(wl.wid, 1000 + l), router_bits=8,
+                                                        shared_bits=8), dev) for l in range(8)]
+    xl_x = [q4.to_device(synth.draw_tokens(wl.H, T, (wl.wid, 1000 + l)), dev) for l in range(8)]
+    xl_y = torch.empty_like(xl_x[0])
+    xl_ws = q4.new_workspace(q4.lily_q4_moe_workspace_bytes(xl_layers[0], T), dev)
+
+    def xl_part(n):
+        for i in range(n):
+            q4.lily_q4_moe_decode(xl_layers[i % 8], xl_x[i % 8], xl_y, ws=xl_ws, stream=stream)
+
+    with torch.cuda.stream(stream):
+        xl_part(16)
+        a0 = torch.cuda.Event(enable_timing=True)
+        a1 = torch.cuda.Event(enable_timing=True)
+        a0.record(stream)
+        xl_part(200)
+        a1.record(stream)
+        a1.synchronize()
+    xl_us = max_over_ranks([a0.elapsed_time(a1) * 1e3 / 200], dev)[0]
+    if q4.lily_q4_workspace_status(xl_ws, stream) != 0:
+        raise RuntimeError("q4-xl decode reported a device-side timeout")
+    del xl_layers
+
     e2e_val = None
     if not args.no_e2e:
         for _ in range(2):
@@ -388,6 +415,8 @@ def run_gb300(args):
                     "with_logprobs_us": round(lp_mean * 1e3, 2)},
         "lm_head_q8": {"us": round(q8_mean * 1e3, 2), "bytes": q8_bytes, "hbm_gbs": round(q8_gbs, 1),
                        "frac_of_measured_hbm": round(q8_gbs / pk["hbm_gbs"], 4)},
+        "decode_q4xl": {"us_per_layer": round(xl_us, 3), "tok_s_per_layer": round(T / (xl_us * 1e-6), 1),
+                        "layout": "8-bit router and shared expert, 4-bit routed experts; 8 layers cycled"},
         "prefill": {"us": round(pf_mean * 1e3, 1), "gflop": round(pf_flops / 1e9, 2),
                     "tflops": round(pf_tflops, 1),
                     "frac_of_measured_bf16": round(pf_tflops / pk["bf16_tflops_sustained"], 4),

@@ -53,7 +53,9 @@ class lily_q4_moe_layer(C.Structure):
                 ("has_shared", C.c_int32),
                 ("sh_gate", lily_q4_mat), ("sh_up", lily_q4_mat), ("sh_down", lily_q4_mat),
                 ("router", C.c_void_p), ("router_bias", C.c_void_p),
-                ("shared_gate", C.c_void_p)]
+                ("shared_gate", C.c_void_p),
+                ("shared_bits", C.c_int32), ("router_bits", C.c_int32),
+                ("router_q8", lily_q4_mat)]
 
 
 _lib = None
@@ -163,12 +165,14 @@ class DeviceLayer:
     """One MoE layer on the GPU plus its C struct."""
 
     def __init__(self, H, E, k, I, gate, up, down, router, router_bias=None, sh_gate=None,
-                 sh_up=None, sh_down=None, shared_gate=None):
+                 sh_up=None, sh_down=None, shared_gate=None, shared_bits=4, router_q8=None):
         self.H, self.E, self.k, self.I = H, E, k, I
         self.gate, self.up, self.down = gate, up, down
         self.router, self.router_bias = router, router_bias
         self.sh_gate, self.sh_up, self.sh_down = sh_gate, sh_up, sh_down
         self.shared_gate = shared_gate
+        self.shared_bits = shared_bits   # 8: the shared expert's codes are 8-bit
+        self.router_q8 = router_q8       # an 8-bit router (DeviceQ4 of [E, H/4] codes) or None
         self._c = None
 
     @property
@@ -181,7 +185,8 @@ class DeviceLayer:
         arr = lambda a: None if a is None else to_device(a, device)
         return cls(L.H, L.E, L.k, L.I, up(L.gate), up(L.up), up(L.down), arr(L.router),
                    arr(L.router_bias), up(L.sh_gate), up(L.sh_up), up(L.sh_down),
-                   arr(L.shared_gate))
+                   arr(L.shared_gate), getattr(L, "shared_bits", 4),
+                   up(getattr(L, "router_q8", None)))
 
     def c(self) -> lily_q4_moe_layer:
         if self._c is None:
@@ -196,12 +201,15 @@ class DeviceLayer:
             st.router = _ptr(self.router)
             st.router_bias = _ptr(self.router_bias)
             st.shared_gate = _ptr(self.shared_gate)
+            st.shared_bits = 8 if (self.has_shared and self.shared_bits == 8) else 4
+            st.router_bits = 8 if self.router_q8 is not None else 16
+            st.router_q8 = self.router_q8.c() if self.router_q8 is not None else z
             self._c = st
         return self._c
 
     def weight_bytes(self) -> int:
         n = self.gate.nbytes + self.up.nbytes + self.down.nbytes
-        n += self.router.numel() * 2
+        n += self.router.numel() * 2 if self.router is not None else self.router_q8.nbytes
         if self.has_shared:
             n += self.sh_gate.nbytes + self.sh_up.nbytes + self.sh_down.nbytes
             n += self.shared_gate.numel() * 2

@@ -44,7 +44,13 @@ static int check_layer(const lily_q4_moe_layer *L) {
   if (L->n_experts > 1024 || L->top_k > 16) return LILY_Q4_ERR_INVALID_ARG;
   if (L->has_shared != 0 && L->has_shared != 1) return LILY_Q4_ERR_INVALID_ARG;
   if (!mat_ok(L->gate) || !mat_ok(L->up) || !mat_ok(L->down)) return LILY_Q4_ERR_INVALID_ARG;
-  if (!L->router || !aligned(L->router, 16)) return LILY_Q4_ERR_INVALID_ARG;
+  if (L->shared_bits != 0 && L->shared_bits != 4 && L->shared_bits != 8) return LILY_Q4_ERR_INVALID_ARG;
+  if (L->router_bits != 0 && L->router_bits != 16 && L->router_bits != 8) return LILY_Q4_ERR_INVALID_ARG;
+  if (L->router_bits == 8) {
+    if (!mat_ok(L->router_q8)) return LILY_Q4_ERR_INVALID_ARG;
+  } else if (!L->router || !aligned(L->router, 16)) {
+    return LILY_Q4_ERR_INVALID_ARG;
+  }
   if (L->router_bias && !aligned(L->router_bias, 4)) return LILY_Q4_ERR_INVALID_ARG;
   if (L->has_shared) {
     if (!mat_ok(L->sh_gate) || !mat_ok(L->sh_up) || !mat_ok(L->sh_down))
@@ -53,6 +59,10 @@ static int check_layer(const lily_q4_moe_layer *L) {
   }
   if (!width_ok(L->hidden) || !width_ok(L->inter)) return LILY_Q4_ERR_UNSUPPORTED;
   return LILY_Q4_OK;
+}
+
+static bool has_8bit_parts(const lily_q4_moe_layer &L) {
+  return L.router_bits == 8 || (L.has_shared && L.shared_bits == 8);
 }
 
 static int check_io(const uint16_t *x, uint16_t *y, int32_t *idx, float *w, void *ws) {
@@ -126,7 +136,8 @@ size_t lily_q4_moe_workspace_bytes(const lily_q4_moe_layer *layer, int32_t T, in
 
 int lily_q4_moe_launches(const lily_q4_moe_layer *layer, int32_t T, int32_t prefill) {
   if (check_layer(layer) != LILY_Q4_OK || T <= 0) return 0;
-  if (prefill) return T <= 8192 && layer->hidden >= 128 && layer->inter >= 128 ? 8 : 0;
+  if (prefill)
+    return !has_8bit_parts(*layer) && T <= 8192 && layer->hidden >= 128 && layer->inter >= 128 ? 8 : 0;
   return T <= 16 ? decode_launch_count(*layer, T) : 0;
 }
 
@@ -210,6 +221,7 @@ int lily_q4_moe_prefill(const lily_q4_moe_layer *layer, const uint16_t *x, int32
                         size_t ws_bytes, lily_q4_stream_t stream) {
   int rc = check_layer(layer);
   if (rc != LILY_Q4_OK) return rc;
+  if (has_8bit_parts(*layer)) return LILY_Q4_ERR_UNSUPPORTED;
   if (T < 0 || T > 8192) return LILY_Q4_ERR_INVALID_ARG;
   if (T == 0) return LILY_Q4_OK;
   rc = check_io(x, y, topk_idx, topk_w, ws);

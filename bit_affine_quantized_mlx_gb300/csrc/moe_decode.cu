@@ -516,6 +516,8 @@ struct FusedArgs {
   int T, E, H, I, k, has_shared;
   int32_t *out_idx;
   float *out_w;
+  lily_q4_mat router8;  // the 8-bit router when router_bits == 8
+  int router_bits, shared_bits;
 };
 
 // Word offset of chunk c (8 values) of 64-value group g in a prepared vector: each group's
@@ -846,11 +848,22 @@ __device__ __forceinline__ void load_down_mat(const lily_q4_mat &m, int e, int r
 // Weights of one phase-A task into registers: a router row (bf16; the lane's chunks
 // lane + 32 j) or one row-step of the shared expert's gate and up rows (codes in wv[0..3],
 // raw bf16 scales and biases in sc, converted where they are used).
-template <int GH>
+template <int GH, bool Q8P>
 __device__ __forceinline__ void load_phase_a(const FusedArgs &a, int task, int nrouter, int lane,
                                              uint4 (&wv)[8], uint32_t (&sc)[4]) {
   constexpr int RPS_H = 32 / GH;
   if (task < nrouter) {
+    if (Q8P && task < a.E && a.router_bits == 8) {
+      // an 8-bit router row: lane g < GH holds group g (64 code bytes, its s and b)
+      if (lane < GH) {
+        const size_t wo = (size_t)task * (GH * 16) + 16 * lane, so = (size_t)task * GH + lane;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) wv[j] = ld_stream(a.router8.w + wo + 4 * j);
+        sc[0] = ld_u16(a.router8.s + so);
+        sc[1] = ld_u16(a.router8.b + so);
+      }
+      return;
+    }
     const uint16_t *wr = task < a.E ? a.router + (size_t)task * a.H : a.shared_gate;
     const int nchunk = a.H / 8;
 #pragma unroll
@@ -861,11 +874,22 @@ __device__ __forceinline__ void load_phase_a(const FusedArgs &a, int task, int n
   } else {
     const int gh = lane % GH, rh = lane / GH;
     const int row = (task - nrouter) * RPS_H + rh;
-    const size_t wo = (size_t)row * (GH * 8) + 8 * gh, so = (size_t)row * GH + gh;
-    wv[0] = ld_stream(a.sh_gate.w + wo);
-    wv[1] = ld_stream(a.sh_gate.w + wo + 4);
-    wv[2] = ld_stream(a.sh_up.w + wo);
-    wv[3] = ld_stream(a.sh_up.w + wo + 4);
+    const size_t so = (size_t)row * GH + gh;
+    if (Q8P && a.shared_bits == 8) {
+      // 8-bit shared rows: 64 code bytes of the lane's group in each matrix
+      const size_t wo = (size_t)row * (GH * 16) + 16 * gh;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        wv[j] = ld_stream(a.sh_gate.w + wo + 4 * j);
+        wv[4 + j] = ld_stream(a.sh_up.w + wo + 4 * j);
+      }
+    } else {
+      const size_t wo = (size_t)row * (GH * 8) + 8 * gh;
+      wv[0] = ld_stream(a.sh_gate.w + wo);
+      wv[1] = ld_stream(a.sh_gate.w + wo + 4);
+      wv[2] = ld_stream(a.sh_up.w + wo);
+      wv[3] = ld_stream(a.sh_up.w + wo + 4);
+    }
     sc[0] = ld_u16(a.sh_gate.s + so);
     sc[1] = ld_u16(a.sh_gate.b + so);
     sc[2] = ld_u16(a.sh_up.s + so);
@@ -873,7 +897,9 @@ __device__ __forceinline__ void load_phase_a(const FusedArgs &a, int task, int n
   }
 }
 
-template <int GH, int GI, int EC>
+// Q8P: the layer has 8-bit parts (router and/or shared expert); the instantiation without
+// them carries none of their branches.
+template <int GH, int GI, int EC, bool Q8P>
 __global__ void __launch_bounds__(kFusedThreads, 1)
     moe_decode_fused_kernel(FusedArgs a, DecodePtrs w) {
   static_assert(kFusedThreads % 8 == 0, "xg_stage groups 8 consecutive threads");
@@ -924,13 +950,30 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
   const int ntasks_a = nrouter + nshared_tasks;
   uint4 wv[8];
   uint32_t sc[4];
-  if (gw < ntasks_a) load_phase_a<GH>(a, gw, nrouter, lane, wv, sc);
+  if (gw < ntasks_a) load_phase_a<GH, Q8P>(a, gw, nrouter, lane, wv, sc);
   xg_stage<true>(s_xp, s_xX, a.x, T * H / 8, reinterpret_cast<uint4 *>(fsm + L0.xr));
   __syncthreads();
   const unsigned long long bbase = s_bbase;
   for (int task = gw; task < ntasks_a; task += nw) {
-    if (task != gw) load_phase_a<GH>(a, task, nrouter, lane, wv, sc);
-    if (task < nrouter) {
+    if (task != gw) load_phase_a<GH, Q8P>(a, task, nrouter, lane, wv, sc);
+    if (Q8P && task < E && a.router_bits == 8) {
+      // 8-bit router row: lane g < GH dots its group with x re-paired for 8-bit codes
+      const int row = task;
+      const uint4 w4[4] = {wv[0], wv[1], wv[2], wv[3]};
+      const float rs = bf16f(sc[0]), rb = bf16f(sc[1]);
+      for (int t = 0; t < T; ++t) {
+        float d = 0.f;
+        if (lane < GH) {
+          XGroupB xg;
+          xg_load(xg, s_xp, s_xX, t * GXH + lane);
+          XGroup8 x8;
+          xgroup8_from_b(x8, xg);
+          d = q8_group_dot_b(w4, x8, rs, rb);
+        }
+        d = seg_sum<32>(d);
+        if (lane == 0) __stcg(w.logits + (size_t)t * E + row, d + (a.bias ? a.bias[row] : 0.f));
+      }
+    } else if (task < nrouter) {
       const int row = task;
       const int nchunk = H / 8;
       for (int t = 0; t < T; ++t) {
@@ -966,8 +1009,17 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
       for (int t = 0; t < T; ++t) {
         XGroupB xg;
         xg_load(xg, s_xp, s_xX, t * GXH + gh);
-        const float gd = seg_sum<GH>(q4_group_dot_b(wv[0], wv[1], xg, gs, gb));
-        const float ud = seg_sum<GH>(q4_group_dot_b(wv[2], wv[3], xg, us, ub));
+        float gd, ud;
+        if (Q8P && a.shared_bits == 8) {
+          XGroup8 x8;
+          xgroup8_from_b(x8, xg);
+          const uint4 g4[4] = {wv[0], wv[1], wv[2], wv[3]}, u4[4] = {wv[4], wv[5], wv[6], wv[7]};
+          gd = seg_sum<GH>(q8_group_dot_b(g4, x8, gs, gb));
+          ud = seg_sum<GH>(q8_group_dot_b(u4, x8, us, ub));
+        } else {
+          gd = seg_sum<GH>(q4_group_dot_b(wv[0], wv[1], xg, gs, gb));
+          ud = seg_sum<GH>(q4_group_dot_b(wv[2], wv[3], xg, us, ub));
+        }
         // shared pairs sit after the T*k routed pairs
         if (gh == 0) h16[(size_t)(T * k + t) * I + row] = f2bf16_rne(silu_mul(gd, ud));
       }
@@ -1022,7 +1074,10 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
   const int P = s_ubase[U];  // routed pairs, then the shared expert's T pairs
   const int nq_cta = (nquads - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x;
   const int ntask_c = P * nq_cta;
-  const int nstaged = min(ntask_c, kFusedSlots);
+  // 8-bit shared-expert rows (q4-xl) have twice the code bytes: their tasks (the last T pairs)
+  // are run from global memory after the others
+  const int ntask_q4 = (Q8P && a.has_shared && a.shared_bits == 8) ? T * k * nq_cta : ntask_c;
+  const int nstaged = min(ntask_q4, kFusedSlots);
   const int jlo = warp * nstaged / kFusedWarps, jhi = (warp + 1) * nstaged / kFusedWarps;
 #pragma unroll
   for (int i = 0; i < kFusedStaged; ++i) {
@@ -1079,12 +1134,12 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
     }
     // tasks beyond the staged ones (batch above one token): from global memory, kFusedMaxQ
     // at a time with all of their loads issued first
-    for (int j0 = nstaged + warp; j0 < ntask_c; j0 += kFusedMaxQ * kFusedWarps) {
+    for (int j0 = nstaged + warp; j0 < ntask_q4; j0 += kFusedMaxQ * kFusedWarps) {
       DownRow dr[kFusedMaxQ];
 #pragma unroll
       for (int q = 0; q < kFusedMaxQ; ++q) {
         const int j = j0 + q * kFusedWarps;
-        if (j < ntask_c) {
+        if (j < ntask_q4) {
           const int pr = j / nq_cta, qi = j - pr * nq_cta;
           const int e = s_pair_e[pr];
           const int row = (blockIdx.x + qi * gridDim.x) * RPS_I + ri;
@@ -1097,7 +1152,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
 #pragma unroll
       for (int q = 0; q < kFusedMaxQ; ++q) {
         const int j = j0 + q * kFusedWarps;
-        if (j < ntask_c) {
+        if (j < ntask_q4) {
           const int pr = j / nq_cta, qi = j - pr * nq_cta;
           if (pr != cur) {
             xg_load(xg, s_hp, s_hX, pr * GXI + gi);
@@ -1108,6 +1163,24 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
           if (gi == 0) s_part[pr][qi * RPS_I + ri] = pw * dd;
         }
       }
+    }
+    // 8-bit shared-expert down rows: one task at a time, h re-paired for 8-bit codes
+    for (int j = ntask_q4 + warp; Q8P && j < ntask_c; j += kFusedWarps) {
+      const int pr = j / nq_cta, qi = j - pr * nq_cta;
+      const int row = (blockIdx.x + qi * gridDim.x) * RPS_I + ri;
+      const size_t wo = (size_t)row * (GI * 16) + 16 * gi, so = (size_t)row * GI + gi;
+      uint4 w4[4];
+#pragma unroll
+      for (int v = 0; v < 4; ++v) w4[v] = ld_stream(a.sh_down.w + wo + 4 * v);
+      const float sv = bf16f(ld_u16(a.sh_down.s + so)), bv = bf16f(ld_u16(a.sh_down.b + so));
+      XGroup8 x8;
+      {
+        XGroupB hb;
+        xg_load(hb, s_hp, s_hX, pr * GXI + gi);
+        xgroup8_from_b(x8, hb);
+      }
+      const float dd = seg_sum<GI>(q8_group_dot_b(w4, x8, sv, bv));
+      if (gi == 0) s_part[pr][qi * RPS_I + ri] = s_pair_w[pr] * dd;
     }
   }
   __syncthreads();
@@ -1135,12 +1208,12 @@ static bool fused_ok(const lily_q4_moe_layer &L, int T) {
   return (GH == 32 && GI == 8) || (GH == 4 && GI == 2 && L.n_experts <= 256);
 }
 
-template <int GH, int GI, int EC>
-static int launch_fused(const FusedArgs &fa, const DecodePtrs &p, size_t smem, cudaStream_t st) {
+template <int GH, int GI, int EC, bool Q8P>
+static int launch_fused_q(const FusedArgs &fa, const DecodePtrs &p, size_t smem, cudaStream_t st) {
   static int attr_done[64] = {0};  // per instantiation and device
   int dev = 0;
   cudaGetDevice(&dev);
-  auto fn = moe_decode_fused_kernel<GH, GI, EC>;
+  auto fn = moe_decode_fused_kernel<GH, GI, EC, Q8P>;
   if (dev < 64 && !attr_done[dev]) {
     if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kFusedSmemMax) !=
         cudaSuccess)
@@ -1175,6 +1248,13 @@ static int launch_fused(const FusedArgs &fa, const DecodePtrs &p, size_t smem, c
   return check_launch();
 }
 
+template <int GH, int GI, int EC>
+static int launch_fused(const FusedArgs &fa, const DecodePtrs &p, size_t smem, cudaStream_t st) {
+  const bool q8 = fa.router_bits == 8 || (fa.has_shared && fa.shared_bits == 8);
+  return q8 ? launch_fused_q<GH, GI, EC, true>(fa, p, smem, st)
+            : launch_fused_q<GH, GI, EC, false>(fa, p, smem, st);
+}
+
 template <int G>
 static void launch_gateup(const GateUpArgs &a, const DecodePtrs &p, int Umax, cudaStream_t st) {
   constexpr int RPS = 32 / G;
@@ -1200,8 +1280,13 @@ static void launch_down(const DownArgs &a, const DecodePtrs &p, cudaStream_t st)
     default: return LILY_Q4_ERR_UNSUPPORTED; \
   }
 
+static bool has_8bit(const lily_q4_moe_layer &L) {
+  return L.router_bits == 8 || (L.has_shared && L.shared_bits == 8);
+}
+
 int decode_launch_count(const lily_q4_moe_layer &L, int T) {
-  return fused_ok(L, T) && sm_count() > 0 ? 1 : 3;
+  if (fused_ok(L, T) && sm_count() > 0) return 1;
+  return has_8bit(L) ? 0 : 3;
 }
 
 int launch_moe_decode(const lily_q4_moe_layer &L, const uint16_t *x, int T, uint16_t *y,
@@ -1211,7 +1296,8 @@ int launch_moe_decode(const lily_q4_moe_layer &L, const uint16_t *x, int T, uint
   if (fused_ok(L, T) && sm_count() > 0) {
     FusedArgs fa{L.gate, L.up, L.down, L.sh_gate, L.sh_up, L.sh_down, L.router, L.router_bias,
                  L.shared_gate, x, y, T, L.n_experts, L.hidden, L.inter, L.top_k, L.has_shared,
-                 topk_idx, topk_w};
+                 topk_idx, topk_w, L.router_q8, L.router_bits == 8 ? 8 : 16,
+                 (L.has_shared && L.shared_bits == 8) ? 8 : 4};
     const size_t smem = fused_layout(l.P, T, L.hidden, L.inter).total;
     if (L.hidden / kGroup == 32) {
       if (L.n_experts <= 256) return launch_fused<32, 8, 8>(fa, p, smem, st);
@@ -1220,6 +1306,7 @@ int launch_moe_decode(const lily_q4_moe_layer &L, const uint16_t *x, int T, uint
     }
     return launch_fused<4, 2, 8>(fa, p, smem, st);
   }
+  if (has_8bit(L)) return LILY_Q4_ERR_UNSUPPORTED;  // 8-bit parts: single-launch path only
   RouterArgs ra{L.router, L.router_bias, L.shared_gate, x, T, L.n_experts, L.hidden, L.top_k,
                 L.has_shared, topk_idx, topk_w};
   const int nrows = L.n_experts + L.has_shared;

@@ -262,6 +262,22 @@ __device__ __forceinline__ void xgroup8_from_bf16(XGroup8 &g, const uint4 *chunk
   g.X128 = 128.0f * sum;
 }
 
+// The same 64 x values re-paired for 8-bit codes from their 4-bit pairing: chunk c's words
+// (x_8c+j, x_8c+j+4), j < 4, give (x_8c, x_8c+2), (x_8c+1, x_8c+3), (x_8c+4, x_8c+6),
+// (x_8c+5, x_8c+7) by byte permutes.
+__device__ __forceinline__ void xgroup8_from_b(XGroup8 &o, const XGroupB &g) {
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    const uint32_t b0 = g.xp[4 * c], b1 = g.xp[4 * c + 1], b2 = g.xp[4 * c + 2], b3 = g.xp[4 * c + 3];
+    o.xp[4 * c + 0] = __byte_perm(b0, b2, 0x5410);
+    o.xp[4 * c + 1] = __byte_perm(b1, b3, 0x5410);
+    o.xp[4 * c + 2] = __byte_perm(b0, b2, 0x7632);
+    o.xp[4 * c + 3] = __byte_perm(b1, b3, 0x7632);
+  }
+  o.X = g.X;
+  o.X128 = g.X128;
+}
+
 // s*(sum q x) + b*(sum x) for one 64-group of 8-bit codes (16 words in w[0..3]) and bf16 x.
 __device__ __forceinline__ float q8_group_dot_b(const uint4 (&wv)[4], const XGroup8 &g, float s,
                                                 float b) {

@@ -90,6 +90,15 @@ typedef struct {
   const uint16_t *router;      /* bf16 [E][H] (row e = the weights of expert e's logit) */
   const float *router_bias;    /* fp32 [E] added to the logits, or NULL */
   const uint16_t *shared_gate; /* bf16 [H] (g_shared); required iff has_shared */
+  /* Affine 8-bit parts (the report's checkpoint keeps its router gates at 8 bits, "Hardware
+   * and software"; the fork page's q4-xl conversion keeps the shared expert at 8 bits, "The
+   * model").  8-bit codes: four per uint32 along K, lowest byte first, same bf16 s/b per 64.
+   * Zero-initialised fields mean the 4-bit / bf16 layout above.  The 8-bit parts are served by
+   * lily_q4_moe_decode at T <= 4 (the single-launch kernel, H/64 and I/64 of 32/8 or 4/2);
+   * other calls with them return LILY_Q4_ERR_UNSUPPORTED. */
+  int32_t shared_bits;         /* 0 or 4: sh_* as above; 8: sh_gate/sh_up [I][H/4], sh_down [H][I/4] */
+  int32_t router_bits;         /* 0 or 16: bf16 router; 8: router_q8 [E][H/4] codes (router unused) */
+  lily_q4_mat router_q8;       /* the 8-bit router when router_bits == 8 */
 } lily_q4_moe_layer;
 
 /* Shapes built: H and I in {64,128,256,512,1024,2048}; E <= 1024; k <= 16.

@@ -104,6 +104,23 @@ def test_moe_argument_errors(lib, fn):
     assert _decode(lib, _fake_layer(), T=too_many, fn=fn) == INV
 
 
+def test_8bit_layer_argument_errors(lib):
+    INV = q4.ERR_INVALID_ARG
+    L = _fake_layer()
+    L.shared_bits = 5                                                      # no such width
+    assert _decode(lib, L) == INV
+    L = _fake_layer()
+    L.router_bits = 12
+    assert _decode(lib, L) == INV
+    L = _fake_layer()
+    L.router_bits = 8                                                      # 8-bit router without its matrix
+    assert _decode(lib, L) == INV
+    L.router_q8 = q4.lily_q4_mat(FAKE, FAKE + 4096, FAKE + 8192)
+    L.router = None                                                        # the bf16 router is then unused
+    assert _decode(lib, L, T=0) == q4.OK
+    assert lib.lily_q4_moe_launches(C.byref(L), 4, 1) == 0                 # no 8-bit prefill
+
+
 def test_gemv_argument_errors(lib):
     m = q4.lily_q4_mat(FAKE, FAKE + 4096, FAKE + 8192)
     f = lib.lily_q4_gemv_argmax

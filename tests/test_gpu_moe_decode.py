@@ -154,3 +154,43 @@ def test_bounded_wait_reports_timeout_and_context_stays_usable(torch_dev, which)
     q4.lily_q4_workspace_init(ws)
     check(torch, dev, L, x, f"decode after a time-out ({which})", ws=ws, dl=dl)
     assert q4.lily_q4_workspace_status(ws) == q4.OK
+
+
+# ----------------------------------------------------------------------------- 8-bit parts
+
+@pytest.mark.parametrize("H,E,k,I,router_bits,shared_bits,T", [
+    (256, 16, 2, 128, 8, 4, 1),
+    (256, 16, 4, 128, 16, 8, 3),
+    (256, 32, 4, 128, 8, 8, 4),
+    (2048, 256, 8, 512, 8, 8, 1),   # the decode shapes with the q4-xl shared expert and 8-bit router
+    (2048, 256, 8, 512, 8, 8, 4),
+    (2048, 256, 8, 512, 16, 8, 2),
+])
+def test_8bit_router_and_shared_expert(torch_dev, H, E, k, I, router_bits, shared_bits, T):
+    """An affine 8-bit router (the checkpoint's router gates) and/or an 8-bit shared expert
+    (q4-xl) in the single-launch decode path, against the oracle."""
+    torch, dev = torch_dev
+    key = (84, H + E + router_bits + shared_bits)
+    L = synth.draw_layer(H, E, k, I, shared=True, router_std=0.05, router_bias=True, key=key,
+                         router_bits=router_bits, shared_bits=shared_bits)
+    check(torch, dev, L, _inputs(L, key, T), f"8-bit parts r{router_bits} s{shared_bits} T{T}")
+
+
+def test_8bit_parts_unsupported_outside_single_launch(torch_dev):
+    """8-bit parts at a batch above four (three launches) and in prefill are refused."""
+    torch, dev = torch_dev
+    L = synth.draw_layer(256, 16, 2, 128, shared=True, router_std=0.05, router_bias=False,
+                         key=(85, 0), router_bits=8, shared_bits=8)
+    dl = q4.DeviceLayer.upload(L, dev)
+    assert q4.lily_q4_moe_launches(dl, 4) == 1 and q4.lily_q4_moe_launches(dl, 5) == 0
+    assert q4.lily_q4_moe_launches(dl, 64, prefill=True) == 0
+    x = q4.to_device(synth.draw_tokens(256, 5, (85, 0)), dev)
+    y = torch.empty_like(x)
+    ws = q4.new_workspace(q4.lily_q4_moe_workspace_bytes(dl, 5), dev)
+    with pytest.raises(q4.Q4Error) as e:
+        q4.lily_q4_moe_decode(dl, x, y, ws=ws)
+    assert e.value.status == q4.ERR_UNSUPPORTED
+    wsp = q4.new_workspace(q4.lily_q4_moe_workspace_bytes(dl, 5, prefill=True), dev)
+    with pytest.raises(q4.Q4Error) as e:
+        q4.lily_q4_moe_prefill(dl, x, y, ws=wsp)
+    assert e.value.status == q4.ERR_UNSUPPORTED
