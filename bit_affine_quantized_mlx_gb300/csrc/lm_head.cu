@@ -1,12 +1,13 @@
-// Q4 LM-head GEMV fused with greedy argmax.
+// Q4 (and 8-bit) LM-head GEMV fused with greedy argmax, and optionally with the
+// full-vocabulary log-sum-exp and log-probabilities.
 //
-// Greedy token selection without logprobs, with the generated id kept on the
-// device (Lily README, first paragraph; Lily-vs-MLX report, "Measurement
-// contract").  One pass over the weights: each warp dequantises rows in
-// registers (lane = one 64-wide group of the row), reduces the row with
-// shuffles, keeps a running (max, argmax); blocks publish their best pair to
-// the workspace and the last block to finish reduces those pairs into the token.
-// The pass is bound by HBM bandwidth: 0.5625 bytes per weight.
+// Greedy token selection with the generated id kept on the device (Lily README, first
+// paragraph; Lily-vs-MLX report, "Measurement contract", where the MLX path also computes
+// log-probabilities over the whole vocabulary).  One pass over the weights: each warp
+// dequantises rows in registers (lane = one 64-wide group of the row), reduces the row with
+// shuffles, keeps a running (max, argmax); blocks publish their best pair to the workspace
+// and the last block to finish reduces those pairs into the token.  The pass streams
+// 0.5625 bytes per 4-bit weight (1.0625 per 8-bit weight).
 #include <cfloat>
 #include <climits>
 #include <mutex>

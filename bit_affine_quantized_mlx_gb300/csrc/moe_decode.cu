@@ -2,7 +2,9 @@
 //
 // The MoE kernels of a decode step, which is bound by its reads (fork page, "How the
 // speed was achieved": the decode step was tuned toward the bandwidth its chain of
-// dependent reads can reach).  The general path is three launches on the caller's stream:
+// dependent reads can reach).  Up to four tokens, the layer is one launch
+// (moe_decode_fused_kernel, below), which also takes layers with an 8-bit router and/or
+// 8-bit shared expert.  The general path is three launches on the caller's stream:
 //
 //  1. router_topk_kernel: fp32 router logits (one warp per expert row, bf16 weights)
 //     and the shared-expert gate sigmoid(x . g_shared); the last block to finish takes
