@@ -83,6 +83,7 @@ def load(path: Optional[str] = None):
     L.lily_q4_gemv_argmax_logprobs.argtypes = [C.POINTER(lily_q4_mat), i32, i32, vp, vp, vp, vp,
                                                vp, sz, vp]
     L.lily_q8_gemv_argmax.argtypes = L.lily_q4_gemv_argmax.argtypes
+    L.lily_q8_gemv_argmax_logprobs.argtypes = L.lily_q4_gemv_argmax_logprobs.argtypes
     L.lily_q8_gemv_argmax_workspace_bytes.argtypes = [i32, i32]
     L.lily_q8_gemv_argmax_workspace_bytes.restype = sz
     L.lily_q4_workspace_init.argtypes = [vp, sz, vp]
@@ -96,7 +97,7 @@ def load(path: Optional[str] = None):
               "lily_q4_workspace_init", "lily_q4_workspace_status", "lily_q4_pack",
               "lily_q4_unpack", "lily_q4_version", "lily_q4_moe_launches",
               "lily_q4_gemv_argmax_noalloc", "lily_q4_gemv_argmax_logprobs",
-              "lily_q8_gemv_argmax", "lily_q4_selftest_timeout"):
+              "lily_q8_gemv_argmax", "lily_q4_selftest_timeout", "lily_q8_gemv_argmax_logprobs"):
         getattr(L, f).restype = C.c_int
     _lib = L
     return L
@@ -287,6 +288,17 @@ def lily_q4_selftest_timeout(ws, which: int, stream=None):
     include/lily_q4.h."""
     return _check(load().lily_q4_selftest_timeout(_ptr(ws), ws.numel(), int(which), _stream(stream)),
                   "lily_q4_selftest_timeout")
+
+
+def lily_q8_gemv_argmax_logprobs(W, x, token, lse, logprobs=None, ws=None, stream=None):
+    """lily_q4_gemv_argmax_logprobs for an 8-bit LM head; see include/lily_q4.h."""
+    N, K = int(W.w.shape[-2]), int(W.w.shape[-1]) * 4
+    m = W.c()
+    return _check(load().lily_q8_gemv_argmax_logprobs(C.byref(m), N, K, _ptr(x), _ptr(token),
+                                                      _ptr(lse), _ptr(logprobs), _ptr(ws),
+                                                      ws.numel() if ws is not None else 0,
+                                                      _stream(stream)),
+                  "lily_q8_gemv_argmax_logprobs")
 
 
 def lily_q8_gemv_argmax_workspace_bytes(N: int, K: int) -> int:

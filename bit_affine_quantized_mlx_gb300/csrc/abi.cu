@@ -121,7 +121,7 @@ size_t lily_q4_gemv_argmax_workspace_bytes(int32_t N, int32_t K) {
 
 size_t lily_q8_gemv_argmax_workspace_bytes(int32_t N, int32_t K) {
   if (N <= 0 || K <= 0 || K % LILY_Q4_GROUP) return 0;
-  return lm_ws_layout(N, K, 8).total_argmax;
+  return lm_ws_layout(N, K, 8).total;
 }
 
 size_t lily_q4_moe_workspace_bytes(const lily_q4_moe_layer *layer, int32_t T, int32_t prefill) {
@@ -201,6 +201,18 @@ int lily_q8_gemv_argmax(const lily_q4_mat *W, int32_t N, int32_t K, const uint16
   if (K != 512 && K != 1024 && K != 2048) return LILY_Q4_ERR_UNSUPPORTED;
   if (ws_bytes < lm_ws_layout(N, K, 8).total_argmax) return LILY_Q4_ERR_WORKSPACE_TOO_SMALL;
   return launch_q8_gemv_argmax(*W, N, K, x, token, logits, ws, (cudaStream_t)stream);
+}
+
+int lily_q8_gemv_argmax_logprobs(const lily_q4_mat *W, int32_t N, int32_t K, const uint16_t *x,
+                                 int32_t *token, float *lse, float *logprobs, void *ws,
+                                 size_t ws_bytes, lily_q4_stream_t stream) {
+  if (!W || !mat_ok(*W) || N <= 0 || K <= 0 || K % LILY_Q4_GROUP) return LILY_Q4_ERR_INVALID_ARG;
+  if (!x || !aligned(x, 16) || !token || !aligned(token, 4)) return LILY_Q4_ERR_INVALID_ARG;
+  if (!lse || !aligned(lse, 4) || (logprobs && !aligned(logprobs, 4))) return LILY_Q4_ERR_INVALID_ARG;
+  if (!ws || !aligned(ws, kAlign)) return LILY_Q4_ERR_INVALID_ARG;
+  if (K != 512 && K != 1024 && K != 2048) return LILY_Q4_ERR_UNSUPPORTED;
+  if (ws_bytes < lm_ws_layout(N, K, 8).total) return LILY_Q4_ERR_WORKSPACE_TOO_SMALL;
+  return launch_q8_gemv_argmax(*W, N, K, x, token, logprobs, ws, (cudaStream_t)stream, lse);
 }
 
 int lily_q4_moe_decode(const lily_q4_moe_layer *layer, const uint16_t *x, int32_t T,

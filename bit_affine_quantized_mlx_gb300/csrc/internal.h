@@ -34,7 +34,7 @@ struct LmWsLayout {
 LmWsLayout lm_ws_layout(int N, int K, int bits = 4);
 // 8-bit codes (four per uint32): greedy token (and logits) for K = 512, 1024 or 2048.
 int launch_q8_gemv_argmax(const lily_q4_mat &W, int N, int K, const uint16_t *x, int32_t *token,
-                          float *logits, void *ws, cudaStream_t st);
+                          float *logits, void *ws, cudaStream_t st, float *lse = nullptr);
 // lse == nullptr: greedy token (and logits) only.  Otherwise also *lse = log sum_n exp(logit[n])
 // and, with logits set, logits[n] - *lse in place of the logits (a second, elementwise launch).
 int launch_gemv_argmax(const lily_q4_mat &W, int N, int K, const uint16_t *x, int32_t *token,

@@ -494,27 +494,46 @@ static int launch_k(const lily_q4_mat &W, int N, int K, const uint16_t *x, int32
   return LILY_Q4_OK;
 }
 
-template <int G>
+template <int G, bool LSE>
 static void launch_q8_g(const lily_q4_mat &W, int N, const uint16_t *x, int32_t *token,
-                        float *logits, void *ws, const LmWsLayout &l, cudaStream_t st) {
+                        float *logits, void *ws, const LmWsLayout &l, cudaStream_t st, float *lse) {
   char *base = static_cast<char *>(ws);
   using C = LsCfg<G, 8>;
-  cudaFuncSetAttribute(gemv_argmax_stream_kernel<G, false, 8>,
+  const LseOut lo = LSE ? LseOut{reinterpret_cast<float *>(base + l.off_partial_m),
+                                 reinterpret_cast<float *>(base + l.off_partial_s), lse}
+                        : LseOut{};
+  if (LSE && !logits) logits = reinterpret_cast<float *>(base + l.off_logits);
+  cudaFuncSetAttribute(gemv_argmax_stream_kernel<G, LSE, 8>,
                        cudaFuncAttributeMaxDynamicSharedMemorySize, C::BYTES);
-  gemv_argmax_stream_kernel<G, false, 8><<<l.grid, kLsThreads, C::BYTES, st>>>(
+  gemv_argmax_stream_kernel<G, LSE, 8><<<l.grid, kLsThreads, C::BYTES, st>>>(
       W.w, W.s, W.b, N, l.rows_per_block, x, logits, token, reinterpret_cast<int32_t *>(base),
       reinterpret_cast<float *>(base + l.off_partial_v),
-      reinterpret_cast<int32_t *>(base + l.off_partial_i), LseOut{});
+      reinterpret_cast<int32_t *>(base + l.off_partial_i), lo);
+}
+
+template <bool LSE>
+static int launch_q8_k(const lily_q4_mat &W, int N, int K, const uint16_t *x, int32_t *token,
+                       float *logits, void *ws, const LmWsLayout &l, cudaStream_t st, float *lse) {
+  switch (K / kGroup) {
+    case 8: launch_q8_g<8, LSE>(W, N, x, token, logits, ws, l, st, lse); break;
+    case 16: launch_q8_g<16, LSE>(W, N, x, token, logits, ws, l, st, lse); break;
+    case 32: launch_q8_g<32, LSE>(W, N, x, token, logits, ws, l, st, lse); break;
+    default: return LILY_Q4_ERR_UNSUPPORTED;
+  }
+  return LILY_Q4_OK;
 }
 
 int launch_q8_gemv_argmax(const lily_q4_mat &W, int N, int K, const uint16_t *x, int32_t *token,
-                          float *logits, void *ws, cudaStream_t st) {
+                          float *logits, void *ws, cudaStream_t st, float *lse) {
   const LmWsLayout l = lm_ws_layout(N, K, 8);
-  switch (K / kGroup) {
-    case 8: launch_q8_g<8>(W, N, x, token, logits, ws, l, st); break;
-    case 16: launch_q8_g<16>(W, N, x, token, logits, ws, l, st); break;
-    case 32: launch_q8_g<32>(W, N, x, token, logits, ws, l, st); break;
-    default: return LILY_Q4_ERR_UNSUPPORTED;
+  const int rc = lse ? launch_q8_k<true>(W, N, K, x, token, logits, ws, l, st, lse)
+                     : launch_q8_k<false>(W, N, K, x, token, logits, ws, l, st, lse);
+  if (rc != LILY_Q4_OK) return rc;
+  if (lse && logits) {
+    int sms = sm_count();
+    if (sms <= 0) sms = 152;
+    const int want = (N + 1023) / 1024;
+    sub_lse_kernel<<<want < 4 * sms ? want : 4 * sms, 256, 0, st>>>(logits, N, lse);
   }
   return check_launch();
 }

@@ -180,6 +180,13 @@ LILY_Q4_API int lily_q4_gemv_argmax_logprobs(const lily_q4_mat *W, int32_t N, in
 LILY_Q4_API int lily_q8_gemv_argmax(const lily_q4_mat *W, int32_t N, int32_t K, const uint16_t *x,
                                     int32_t *token, float *logits, void *ws, size_t ws_bytes,
                                     lily_q4_stream_t stream);
+/* lily_q8_gemv_argmax_logprobs -- lily_q4_gemv_argmax_logprobs for the 8-bit LM head (same
+ * outputs and rules; K as lily_q8_gemv_argmax).  lily_q8_gemv_argmax_workspace_bytes covers
+ * both 8-bit calls. */
+LILY_Q4_API int lily_q8_gemv_argmax_logprobs(const lily_q4_mat *W, int32_t N, int32_t K,
+                                             const uint16_t *x, int32_t *token, float *lse,
+                                             float *logprobs, void *ws, size_t ws_bytes,
+                                             lily_q4_stream_t stream);
 LILY_Q4_API size_t lily_q8_gemv_argmax_workspace_bytes(int32_t N, int32_t K);
 
 /*

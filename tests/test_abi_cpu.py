@@ -164,6 +164,13 @@ def test_q8_gemv_argument_errors(lib):
     assert f(C.byref(m), 10, 2048, FAKE, FAKE, None, ws, 16, None) == q4.ERR_WORKSPACE_TOO_SMALL
     assert lib.lily_q8_gemv_argmax_workspace_bytes(151936, 2048) > 0
     assert lib.lily_q8_gemv_argmax_workspace_bytes(10, 100) == 0
+    g = lib.lily_q8_gemv_argmax_logprobs
+    lse = FAKE + 512
+    assert g(C.byref(m), 10, 2048, FAKE, FAKE, None, None, ws, 1 << 20, None) == q4.ERR_INVALID_ARG
+    assert g(C.byref(m), 10, 256, FAKE, FAKE, lse, None, ws, 1 << 20, None) == q4.ERR_UNSUPPORTED
+    n = lib.lily_q8_gemv_argmax_workspace_bytes(151936, 2048)
+    assert g(C.byref(m), 151936, 2048, FAKE, FAKE, lse, None, ws, n - 256, None) == \
+        q4.ERR_WORKSPACE_TOO_SMALL
 
 
 def test_selftest_argument_errors(lib):

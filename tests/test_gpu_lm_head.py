@@ -227,3 +227,42 @@ def test_q8_planted_tie_goes_to_lower_index(torch_dev):
     assert tok == 1234 and lg[1234] == lg[2345]
     got_tok, got_lg = _run_q8(torch, dev, W2, x)
     assert got_tok == 1234 and got_lg[1234] == got_lg[2345]
+
+
+def _run_q8_lp(torch, dev, W, x_bits, with_lp=True):
+    N, K = W.N, W.K
+    dW = q4.DeviceQ4.upload(W, dev)
+    xd = q4.to_device(x_bits, dev)
+    tok = torch.full((1,), -7, dtype=torch.int32, device=dev)
+    lse = torch.full((1,), float("nan"), dtype=torch.float32, device=dev)
+    lp = torch.empty(N, dtype=torch.float32, device=dev) if with_lp else None
+    ws = q4.new_workspace(q4.lily_q8_gemv_argmax_workspace_bytes(N, K), dev)
+    q4.lily_q8_gemv_argmax_logprobs(dW, xd, tok, lse, logprobs=lp, ws=ws)
+    torch.cuda.synchronize()
+    return (int(tok.item()), float(lse.item()),
+            lp.cpu().numpy().astype(np.float64) if with_lp else None)
+
+
+@pytest.mark.parametrize("N,K", [(37, 1024), (4097, 512), (7297, 2048)])
+def test_q8_logprobs_shapes(torch_dev, N, K):
+    torch, dev = torch_dev
+    W = synth.draw_q8(N, K, 67, N, K)
+    x, _, tok, lg = orc.lm_x_without_near_tie(W, lambda a: synth.draw_x(K, (67, N), 0, a),
+                                              head=orc.q8_lm_head)
+    got = _run_q8_lp(torch, dev, W, x)
+    _check_lp(got, tok, lg, f"8-bit N={N} K={K}")
+    t2, lse2, _ = _run_q8_lp(torch, dev, W, x, with_lp=False)
+    assert t2 == got[0] and lse2 == got[1]
+
+
+def test_q8_logprobs_full_size(torch_dev):
+    """The 8-bit LM head (151,936 x 2048) with the log-sum-exp and every log-probability."""
+    torch, dev = torch_dev
+    wl = synth.LMHEAD
+    W = synth.draw_lm_head_q8(wl.V, wl.H)
+    x, _, tok, lg = orc.lm_x_without_near_tie(W, lambda a: synth.draw_lm_x(wl.H, attempt=a),
+                                              head=orc.q8_lm_head)
+    a = _run_q8_lp(torch, dev, W, x)
+    _check_lp(a, tok, lg, "full 8-bit LM head")
+    b = _run_q8_lp(torch, dev, W, x)
+    assert a[0] == b[0] and a[1] == b[1] and np.array_equal(a[2], b[2])
