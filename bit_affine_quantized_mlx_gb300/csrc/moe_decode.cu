@@ -104,6 +104,8 @@ struct RouterArgs {
   int T, E, H, k, has_shared;
   int32_t *out_idx;
   float *out_w;
+  lily_q4_mat router8;  // the 8-bit router when router_bits == 8
+  int router_bits;
 };
 
 // Routing bookkeeping of T tokens by one block of NT threads: top-k per token (a warp per
@@ -241,7 +243,33 @@ __global__ void __launch_bounds__(kRouterThreads)
   const int nrows = a.E + a.has_shared;
   const int row = blockIdx.x * (kRouterThreads / 32) + warp;
   const int nchunk = a.H / 8;  // 16-byte chunks per row
-  if (row < nrows) {
+  if (row < a.E && a.router_bits == 8) {
+    // an 8-bit router row: lane g < H/64 holds group g (64 code bytes, its s and b)
+    const int G = a.H / kGroup;
+    uint4 w4[4] = {};
+    float rs = 0.f, rb = 0.f;
+    if (lane < G) {
+      const size_t wo = (size_t)row * (G * 16) + 16 * lane, so = (size_t)row * G + lane;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) w4[j] = ld_stream(a.router8.w + wo + 4 * j);
+      rs = bf16f(ld_u16(a.router8.s + so));
+      rb = bf16f(ld_u16(a.router8.b + so));
+    }
+    for (int t = 0; t < a.T; ++t) {
+      float d = 0.f;
+      if (lane < G) {
+        uint4 c[8];
+        const uint4 *xp = reinterpret_cast<const uint4 *>(a.x + (size_t)t * a.H + kGroup * lane);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) c[i] = __ldg(xp + i);
+        XGroup8 x8;
+        xgroup8_from_bf16(x8, c);
+        d = q8_group_dot_b(w4, x8, rs, rb);
+      }
+      d = seg_sum<32>(d);
+      if (lane == 0) w.logits[(size_t)t * a.E + row] = d + (a.bias ? a.bias[row] : 0.f);
+    }
+  } else if (row < nrows) {
     const uint16_t *wr = row < a.E ? a.router + (size_t)row * a.H : a.shared_gate;
     uint4 wv[8];
 #pragma unroll
@@ -299,6 +327,7 @@ struct GateUpArgs {
   lily_q4_mat gate, up, sh_gate, sh_up;
   const uint16_t *x;
   int E, H, I;
+  int shared_bits;  // 8: the shared unit is left to gateup_shared8_kernel
 };
 
 template <int G>  // groups per row = H / 64
@@ -316,6 +345,7 @@ __global__ void __launch_bounds__(kGateUpThreads)
   const int pb = max(w.ubase()[u], 0), pe = min(w.ubase()[u + 1], w.P);
   if (e < 0 || e > a.E) return;
   const bool shared = (e == a.E);
+  if (shared && a.shared_bits == 8) return;
   const size_t eoff_w = shared ? 0 : (size_t)e * a.I * K8;
   const size_t eoff_s = shared ? 0 : (size_t)e * a.I * G;
   const uint32_t *gw = (shared ? a.sh_gate.w : a.gate.w) + eoff_w;
@@ -367,6 +397,51 @@ __global__ void __launch_bounds__(kGateUpThreads)
   }
 }
 
+// The 8-bit shared expert's gate/up rows (q4-xl): one row-step per warp, applied to every
+// token (the shared expert is the last unique unit); h in fp32 as above.
+template <int G>  // groups per row = H / 64
+__global__ void __launch_bounds__(kGateUpThreads)
+    gateup_shared8_kernel(GateUpArgs a, DecodePtrs w) {
+  constexpr int RPS = 32 / G;
+  const int U = w.meta[0];
+  if (U < 1 || U > w.Umax) return;
+  const int u = U - 1;
+  if (w.uexp()[u] != a.E) return;
+  const int pb = max(w.ubase()[u], 0), pe = min(w.ubase()[u + 1], w.P);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int g = lane % G, rsub = lane / G;
+  const int row = (blockIdx.x * (kGateUpThreads / 32) + warp) * RPS + rsub;
+  const bool valid = row < a.I;
+  uint4 gq[4] = {}, uq[4] = {};
+  float gs = 0.f, gb = 0.f, us = 0.f, ub = 0.f;
+  if (valid) {
+    const size_t wo = (size_t)row * (G * 16) + 16 * g, so = (size_t)row * G + g;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      gq[j] = ld_stream(a.sh_gate.w + wo + 4 * j);
+      uq[j] = ld_stream(a.sh_up.w + wo + 4 * j);
+    }
+    gs = bf16f(ld_u16(a.sh_gate.s + so));
+    gb = bf16f(ld_u16(a.sh_gate.b + so));
+    us = bf16f(ld_u16(a.sh_up.s + so));
+    ub = bf16f(ld_u16(a.sh_up.b + so));
+  }
+  for (int pr = pb; pr < pe; ++pr) {
+    const int t = w.pair_tok[pr];
+    XGroup8 x8;
+    {
+      uint4 c[8];
+      const uint4 *xp = reinterpret_cast<const uint4 *>(a.x + (size_t)t * a.H + kGroup * g);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) c[i] = __ldg(xp + i);
+      xgroup8_from_bf16(x8, c);
+    }
+    const float gd = seg_sum<G>(q8_group_dot_b(gq, x8, gs, gb));
+    const float ud = seg_sum<G>(q8_group_dot_b(uq, x8, us, ub));
+    if (g == 0 && valid) w.h[(size_t)pr * a.I + row] = silu_mul(gd, ud);
+  }
+}
+
 // ---------------------------------------------------------------------------------------
 // 3. down GEMV + weighted combine (fixed-order sum per token)
 // ---------------------------------------------------------------------------------------
@@ -374,9 +449,10 @@ struct DownArgs {
   lily_q4_mat down, sh_down;
   uint16_t *y;
   int T, E, H, I;
+  int shared_bits;
 };
 
-template <int G>  // groups per row = I / 64
+template <int G, bool Q8P>  // groups per row = I / 64; Q8P: the shared expert's codes are 8-bit
 __global__ void __launch_bounds__(kDownThreads)
     down_kernel(DownArgs a, DecodePtrs w) {
   constexpr int RPS = 32 / G;
@@ -393,6 +469,38 @@ __global__ void __launch_bounds__(kDownThreads)
   for (int pr = warp; pr < P; pr += kDownThreads / 32) {
     const int e = min(max(w.pair_e()[pr], 0), a.E);
     const bool shared = (e == a.E);
+    if (Q8P && shared) {
+      // 8-bit shared down rows: 64 code bytes of the lane's group per row-step, fp32 h
+      float v[64];
+      const float4 *hp = reinterpret_cast<const float4 *>(w.h + (size_t)pr * a.I + kGroup * g);
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const float4 f = __ldcg(hp + i);
+        v[4 * i] = f.x;
+        v[4 * i + 1] = f.y;
+        v[4 * i + 2] = f.z;
+        v[4 * i + 3] = f.w;
+      }
+      const float pw = w.pair_w[pr];
+#pragma unroll
+      for (int st = 0; st < STEPS; ++st) {
+        const int rr = st * RPS + rsub;
+        const int row = r0 + rr;
+        uint4 w4[4] = {};
+        float sv = 0.f, bv = 0.f;
+        if (rr < kDownRows && row < a.H) {
+          const size_t wo = (size_t)row * (G * 16) + 16 * g, so = (size_t)row * G + g;
+#pragma unroll
+          for (int j = 0; j < 4; ++j) w4[j] = ld_stream(a.sh_down.w + wo + 4 * j);
+          sv = bf16f(ld_u16(a.sh_down.s + so));
+          bv = bf16f(ld_u16(a.sh_down.b + so));
+        }
+        const float d = seg_sum<G>(q8_group_dot_f32(w4, v, sv, bv));
+        if (g == 0 && rr < kDownRows) part[pr][rr] = pw * d;
+      }
+      if (lane == 0) s_tok[pr] = w.pair_tok[pr];
+      continue;
+    }
     const uint32_t *dw = shared ? a.sh_down.w : a.down.w + (size_t)e * a.H * K8;
     const uint16_t *ds = shared ? a.sh_down.s : a.down.s + (size_t)e * a.H * G;
     const uint16_t *db = shared ? a.sh_down.b : a.down.b + (size_t)e * a.H * G;
@@ -1263,12 +1371,19 @@ static void launch_gateup(const GateUpArgs &a, const DecodePtrs &p, int Umax, cu
   constexpr int ROWS = (kGateUpThreads / 32) * kGateUpSteps * RPS;
   dim3 grid((a.I + ROWS - 1) / ROWS, Umax);
   gateup_kernel<G><<<grid, kGateUpThreads, 0, st>>>(a, p);
+  if (a.shared_bits == 8) {
+    constexpr int ROWS8 = (kGateUpThreads / 32) * RPS;
+    gateup_shared8_kernel<G><<<(a.I + ROWS8 - 1) / ROWS8, kGateUpThreads, 0, st>>>(a, p);
+  }
 }
 
 template <int G>
 static void launch_down(const DownArgs &a, const DecodePtrs &p, cudaStream_t st) {
   dim3 grid((a.H + kDownRows - 1) / kDownRows);
-  down_kernel<G><<<grid, kDownThreads, 0, st>>>(a, p);
+  if (a.shared_bits == 8)
+    down_kernel<G, true><<<grid, kDownThreads, 0, st>>>(a, p);
+  else
+    down_kernel<G, false><<<grid, kDownThreads, 0, st>>>(a, p);
 }
 
 #define LQ4_DISPATCH_G(gval, FN, ...)      \
@@ -1282,13 +1397,9 @@ static void launch_down(const DownArgs &a, const DecodePtrs &p, cudaStream_t st)
     default: return LILY_Q4_ERR_UNSUPPORTED; \
   }
 
-static bool has_8bit(const lily_q4_moe_layer &L) {
-  return L.router_bits == 8 || (L.has_shared && L.shared_bits == 8);
-}
-
 int decode_launch_count(const lily_q4_moe_layer &L, int T) {
   if (fused_ok(L, T) && sm_count() > 0) return 1;
-  return has_8bit(L) ? 0 : 3;
+  return (L.has_shared && L.shared_bits == 8) ? 4 : 3;
 }
 
 int launch_moe_decode(const lily_q4_moe_layer &L, const uint16_t *x, int T, uint16_t *y,
@@ -1308,9 +1419,9 @@ int launch_moe_decode(const lily_q4_moe_layer &L, const uint16_t *x, int T, uint
     }
     return launch_fused<4, 2, 8>(fa, p, smem, st);
   }
-  if (has_8bit(L)) return LILY_Q4_ERR_UNSUPPORTED;  // 8-bit parts: single-launch path only
   RouterArgs ra{L.router, L.router_bias, L.shared_gate, x, T, L.n_experts, L.hidden, L.top_k,
-                L.has_shared, topk_idx, topk_w};
+                L.has_shared, topk_idx, topk_w, L.router_q8, L.router_bits == 8 ? 8 : 16};
+  const int shared_bits = (L.has_shared && L.shared_bits == 8) ? 8 : 4;
   const int nrows = L.n_experts + L.has_shared;
   const int rgrid = (nrows + kRouterThreads / 32 - 1) / (kRouterThreads / 32);
   if (L.n_experts <= 256)
@@ -1320,10 +1431,10 @@ int launch_moe_decode(const lily_q4_moe_layer &L, const uint16_t *x, int T, uint
   else
     router_topk_kernel<32><<<rgrid, kRouterThreads, 0, st>>>(ra, p);
 
-  GateUpArgs ga{L.gate, L.up, L.sh_gate, L.sh_up, x, L.n_experts, L.hidden, L.inter};
+  GateUpArgs ga{L.gate, L.up, L.sh_gate, L.sh_up, x, L.n_experts, L.hidden, L.inter, shared_bits};
   LQ4_DISPATCH_G(L.hidden / kGroup, launch_gateup, ga, p, l.Umax, st);
 
-  DownArgs da{L.down, L.sh_down, y, T, L.n_experts, L.hidden, L.inter};
+  DownArgs da{L.down, L.sh_down, y, T, L.n_experts, L.hidden, L.inter, shared_bits};
   LQ4_DISPATCH_G(L.inter / kGroup, launch_down, da, p, st);
   return check_launch();
 }

@@ -312,6 +312,30 @@ __device__ __forceinline__ float q8_group_dot_b(const uint4 (&wv)[4], const XGro
   return fmaf(s, fmaf(16.0f, hi, lo), b * g.X);
 }
 
+// s*(sum q v) + b*(sum v) for one 64-group of 8-bit codes (16 words in w[0..3]) and fp32
+// activations v[0..63] in K order (the three-launch decode path keeps h in fp32).
+__device__ __forceinline__ float q8_group_dot_f32(const uint4 (&wv)[4], const float *v, float s,
+                                                  float b) {
+  const uint32_t w[16] = {wv[0].x, wv[0].y, wv[0].z, wv[0].w, wv[1].x, wv[1].y, wv[1].z, wv[1].w,
+                          wv[2].x, wv[2].y, wv[2].z, wv[2].w, wv[3].x, wv[3].y, wv[3].z, wv[3].w};
+  float a0 = 0.f, a1 = 0.f, x0 = 0.f, x1 = 0.f;
+#pragma unroll
+  for (int m = 0; m < 16; ++m) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float q = (float)((w[m] >> (8 * j)) & 0xFFu);
+      if (j & 1) {
+        a1 = fmaf(q, v[4 * m + j], a1);
+        x1 += v[4 * m + j];
+      } else {
+        a0 = fmaf(q, v[4 * m + j], a0);
+        x0 += v[4 * m + j];
+      }
+    }
+  }
+  return fmaf(s, a0 + a1, b * (x0 + x1));
+}
+
 // Dot product of one dequantised 64-group with the prepared x: s*(sum q x) + b*(sum x).
 __device__ __forceinline__ float q4_group_dot(const uint4 w0, const uint4 w1, const XGroup &g,
                                               float s, float b) {

@@ -94,8 +94,8 @@ typedef struct {
    * and software"; the fork page's q4-xl conversion keeps the shared expert at 8 bits, "The
    * model").  8-bit codes: four per uint32 along K, lowest byte first, same bf16 s/b per 64.
    * Zero-initialised fields mean the 4-bit / bf16 layout above.  The 8-bit parts are served by
-   * lily_q4_moe_decode at T <= 4 (the single-launch kernel, H/64 and I/64 of 32/8 or 4/2);
-   * other calls with them return LILY_Q4_ERR_UNSUPPORTED. */
+   * lily_q4_moe_decode (H <= 2048); lily_q4_moe_prefill returns LILY_Q4_ERR_UNSUPPORTED for a
+   * layer with them. */
   int32_t shared_bits;         /* 0 or 4: sh_* as above; 8: sh_gate/sh_up [I][H/4], sh_down [H][I/4] */
   int32_t router_bits;         /* 0 or 16: bf16 router; 8: router_q8 [E][H/4] codes (router unused) */
   lily_q4_mat router_q8;       /* the 8-bit router when router_bits == 8 */
@@ -224,7 +224,7 @@ LILY_Q4_API size_t lily_q4_gemv_argmax_workspace_bytes(int32_t N, int32_t K);
  * (prefill = 1) call enqueues for this layer and T; 0 when the arguments are invalid.
  * Decode uses one launch when its single-launch kernel covers the shapes and batch (one
  * block per SM, enqueued as a programmatic dependent of the previous kernel on the
- * stream), three launches otherwise. */
+ * stream), three launches otherwise (four with an 8-bit shared expert). */
 LILY_Q4_API int lily_q4_moe_launches(const lily_q4_moe_layer *layer, int32_t T, int32_t prefill);
 
 /* Zero-fill a workspace on `stream` (asynchronous). */

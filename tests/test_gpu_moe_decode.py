@@ -165,10 +165,16 @@ def test_bounded_wait_reports_timeout_and_context_stays_usable(torch_dev, which)
     (2048, 256, 8, 512, 8, 8, 1),   # the decode shapes with the q4-xl shared expert and 8-bit router
     (2048, 256, 8, 512, 8, 8, 4),
     (2048, 256, 8, 512, 16, 8, 2),
+    # above four tokens: the three-launch path
+    (256, 16, 2, 128, 8, 4, 5),
+    (256, 32, 4, 128, 16, 8, 9),
+    (2048, 256, 8, 512, 8, 8, 16),
+    (1024, 64, 6, 256, 8, 8, 7),
 ])
 def test_8bit_router_and_shared_expert(torch_dev, H, E, k, I, router_bits, shared_bits, T):
     """An affine 8-bit router (the checkpoint's router gates) and/or an 8-bit shared expert
-    (q4-xl) in the single-launch decode path, against the oracle."""
+    (q4-xl) in the decode paths (one launch up to four tokens, three or four above), against
+    the oracle."""
     torch, dev = torch_dev
     key = (84, H + E + router_bits + shared_bits)
     L = synth.draw_layer(H, E, k, I, shared=True, router_std=0.05, router_bias=True, key=key,
@@ -176,20 +182,17 @@ def test_8bit_router_and_shared_expert(torch_dev, H, E, k, I, router_bits, share
     check(torch, dev, L, _inputs(L, key, T), f"8-bit parts r{router_bits} s{shared_bits} T{T}")
 
 
-def test_8bit_parts_unsupported_outside_single_launch(torch_dev):
-    """8-bit parts at a batch above four (three launches) and in prefill are refused."""
+def test_8bit_parts_launch_counts_and_prefill_refused(torch_dev):
+    """Launch counts of a layer with 8-bit parts (one up to four tokens; four above: the
+    8-bit shared expert's gate/up runs as its own launch), and prefill refuses them."""
     torch, dev = torch_dev
     L = synth.draw_layer(256, 16, 2, 128, shared=True, router_std=0.05, router_bias=False,
                          key=(85, 0), router_bits=8, shared_bits=8)
     dl = q4.DeviceLayer.upload(L, dev)
-    assert q4.lily_q4_moe_launches(dl, 4) == 1 and q4.lily_q4_moe_launches(dl, 5) == 0
+    assert q4.lily_q4_moe_launches(dl, 4) == 1 and q4.lily_q4_moe_launches(dl, 5) == 4
     assert q4.lily_q4_moe_launches(dl, 64, prefill=True) == 0
     x = q4.to_device(synth.draw_tokens(256, 5, (85, 0)), dev)
     y = torch.empty_like(x)
-    ws = q4.new_workspace(q4.lily_q4_moe_workspace_bytes(dl, 5), dev)
-    with pytest.raises(q4.Q4Error) as e:
-        q4.lily_q4_moe_decode(dl, x, y, ws=ws)
-    assert e.value.status == q4.ERR_UNSUPPORTED
     wsp = q4.new_workspace(q4.lily_q4_moe_workspace_bytes(dl, 5, prefill=True), dev)
     with pytest.raises(q4.Q4Error) as e:
         q4.lily_q4_moe_prefill(dl, x, y, ws=wsp)
