@@ -694,9 +694,9 @@ template <int GI>
 __device__ __forceinline__ void cp_async_row_scales(uint32_t dst, const uint16_t *src) {
   static_assert(GI == 8 || GI == 2, "row scales of 16 or 4 bytes");
   if constexpr (GI == 8)
-    tc::cp_async16(dst, src, 16);
+    cp_async16_stream(dst, src);
   else
-    tc::cp_async4(dst, src);
+    cp_async4_stream(dst, src);
 }
 
 // Grid barrier on a 64-bit arrival counter that only grows: each block adds 1 per barrier
@@ -779,31 +779,9 @@ __device__ void route_small(const float *logits, const float *sigma, int T, int 
   const float sig = (has_shared && warp == 0 && lane < T) ? __ldcg(sigma + lane) : 0.f;
   if (warp < T) {
     const int t = warp;
-    const float *lg = logits + (size_t)t * E;
-    float lv[EC];
-#pragma unroll
-    for (int j = 0; j < EC; ++j) lv[j] = (lane + 32 * j < E) ? cand(__ldcg(lg + lane + 32 * j)) : -INFINITY;
-    uint32_t taken = 0;
-    float myv = 0.f;
-    int mye = 0;
-    for (int i = 0; i < k; ++i) {
-      float bv = -INFINITY;
-      int be = INT_MAX;
-#pragma unroll
-      for (int j = 0; j < EC; ++j) {
-        const int e = lane + 32 * j;
-        if (e < E && !(taken & (1u << j)) && better(lv[j], e, bv, be)) {
-          bv = lv[j];
-          be = e;
-        }
-      }
-      warp_argmax(bv, be);
-      if ((be & 31) == lane) taken |= 1u << (be >> 5);
-      if (lane == i) {  // lane i keeps selection i
-        myv = bv;
-        mye = be;
-      }
-    }
+    float myv;
+    int mye;
+    warp_topk<EC>(logits + (size_t)t * E, E, k, mye, myv);  // lane i: selection i
     // softmax over the k selected logits (selection 0 holds the largest)
     const float v0 = __shfl_sync(0xffffffffu, myv, 0);
     const float ex = lane < k ? expf(myv - v0) : 0.f;
@@ -1038,6 +1016,14 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
   // for the previous kernel to complete before touching anything it may have written (x,
   // the workspace).
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  // Weights do not depend on the previous kernel: each warp issues the loads of its first
+  // phase-A row (router row, or shared-expert gate/up row-step) before it waits for that
+  // kernel, so they are in flight while it drains.
+  const int nshared_tasks = a.has_shared ? I / RPS_H : 0;
+  const int ntasks_a = nrouter + nshared_tasks;
+  uint4 wv[8];
+  uint32_t sc[4];
+  if (gw < ntasks_a) load_phase_a<GH, Q8P>(a, gw, nrouter, lane, wv, sc);
   asm volatile("griddepcontrol.wait;" ::: "memory");
   // The barrier base is read by the last warp, which has no phase-A rows: the acquire load
   // holds up only that warp while the others issue their weight loads.
@@ -1054,13 +1040,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
   uint16_t *h16 = reinterpret_cast<uint16_t *>(w.h);  // this path keeps h as bf16 [pair][I]
 
   // ------------------------------------------------------------------ phase A
-  // Each warp issues its first task's weight loads, then the block prepares x in shared
-  // memory while they are in flight.
-  const int nshared_tasks = a.has_shared ? I / RPS_H : 0;
-  const int ntasks_a = nrouter + nshared_tasks;
-  uint4 wv[8];
-  uint32_t sc[4];
-  if (gw < ntasks_a) load_phase_a<GH, Q8P>(a, gw, nrouter, lane, wv, sc);
+  // The first task's weight loads are in flight (above); the block prepares x in shared memory.
   xg_stage<true>(s_xp, s_xX, a.x, T * H / 8, reinterpret_cast<uint4 *>(fsm + L0.xr));
   __syncthreads();
   const unsigned long long bbase = s_bbase;
@@ -1145,15 +1125,57 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
   }
   const int U = s_U;
   const int Ur = a.has_shared ? U - 1 : U;  // routed unique experts
+  // Down tasks (pair pr, row-step qi) -> j = pr * nq_cta + qi.  The first kFusedSlots are
+  // split into contiguous runs, one per warp (neighbouring tasks share the pair, so a warp
+  // prepares few h vectors); their codes and scales depend on the routing only, so each warp
+  // copies its staged tasks into shared memory (cp.async, nothing held in registers) right
+  // after issuing the loads of its first gate/up rows: all of the layer's routed weights are
+  // then in flight at once, and the copies have landed before the second grid barrier.  Warp
+  // w takes the rest, j = nstaged + w + kFusedWarps i, in phase C.
+  const int P = s_ubase[U];  // routed pairs, then the shared expert's T pairs
+  const int nq_cta = (nquads - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x;
+  const int ntask_c = P * nq_cta;
+  // 8-bit shared-expert rows (q4-xl) have twice the code bytes: their tasks (the last T pairs)
+  // are run from global memory after the others
+  const int ntask_q4 = (Q8P && a.has_shared && a.shared_bits == 8) ? T * k * nq_cta : ntask_c;
+  const int nstaged = min(ntask_q4, kFusedSlots);
+  const int jlo = warp * nstaged / kFusedWarps, jhi = (warp + 1) * nstaged / kFusedWarps;
+  auto stage_down = [&]() {
+#pragma unroll
+    for (int i = 0; i < kFusedStaged; ++i) {
+      const int j = jlo + i;
+      if (j < jhi) {
+        const int pr = j / nq_cta, qi = j - pr * nq_cta;
+        const int e = s_pair_e[pr];
+        const bool sh = (e == E);
+        const lily_q4_mat &m = sh ? a.sh_down : a.down;
+        const size_t ee = sh ? 0 : (size_t)e;
+        const int row = (blockIdx.x + qi * gridDim.x) * RPS_I + ri;
+        const size_t wo = (ee * H + row) * (GI * 8) + 8 * gi;
+        const uint32_t dst = tc::smem_u32(s_dn + ((size_t)j * 32 + lane) * 32);
+        cp_async16_stream(dst, m.w + wo);
+        cp_async16_stream(dst + 16, m.w + wo + 4);
+        if (gi < 2)
+          cp_async_row_scales<GI>(tc::smem_u32(s_dsc + j * 64 + gi * 32 + ri * GI),
+                                  (gi ? m.b : m.s) + (ee * H + row) * GI);
+      }
+    }
+    tc::cp_async_commit();
+  };
   // routed gate/up: tasks (unique expert, row-step), a batch of kFusedBatch per warp with
   // all of the batch's loads issued before any is computed
   const int steps_h = I / RPS_H;
   const int ntasks_b = Ur * steps_h;
+  bool staged = false;
   for (int base = gw; base < ntasks_b; base += nw * kFusedBatch) {
     RowPair rp[kFusedBatch];
 #pragma unroll
     for (int i = 0; i < kFusedBatch; ++i)
       if (base + i * nw < ntasks_b) load_gateup<GH>(a, s_uexp, base + i * nw, steps_h, I, gh, rh, rp[i]);
+    if (!staged) {
+      stage_down();
+      staged = true;
+    }
     int xg_tok = -1;
     XGroupB xg;
 #pragma unroll
@@ -1176,39 +1198,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
       }
     }
   }
-  // Down tasks (pair pr, row-step qi) -> j = pr * nq_cta + qi.  The first kFusedSlots are
-  // split into contiguous runs, one per warp (neighbouring tasks share the pair, so a warp
-  // prepares few h vectors); their codes and scales do not depend on h and are copied into
-  // shared memory now (cp.async, nothing held in registers), so the traffic is in flight
-  // across the barrier.  Warp w takes the rest, j = nstaged + w + kFusedWarps i, in phase C.
-  const int P = s_ubase[U];  // routed pairs, then the shared expert's T pairs
-  const int nq_cta = (nquads - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x;
-  const int ntask_c = P * nq_cta;
-  // 8-bit shared-expert rows (q4-xl) have twice the code bytes: their tasks (the last T pairs)
-  // are run from global memory after the others
-  const int ntask_q4 = (Q8P && a.has_shared && a.shared_bits == 8) ? T * k * nq_cta : ntask_c;
-  const int nstaged = min(ntask_q4, kFusedSlots);
-  const int jlo = warp * nstaged / kFusedWarps, jhi = (warp + 1) * nstaged / kFusedWarps;
-#pragma unroll
-  for (int i = 0; i < kFusedStaged; ++i) {
-    const int j = jlo + i;
-    if (j < jhi) {
-      const int pr = j / nq_cta, qi = j - pr * nq_cta;
-      const int e = s_pair_e[pr];
-      const bool sh = (e == E);
-      const lily_q4_mat &m = sh ? a.sh_down : a.down;
-      const size_t ee = sh ? 0 : (size_t)e;
-      const int row = (blockIdx.x + qi * gridDim.x) * RPS_I + ri;
-      const size_t wo = (ee * H + row) * (GI * 8) + 8 * gi;
-      const uint32_t dst = tc::smem_u32(s_dn + ((size_t)j * 32 + lane) * 32);
-      tc::cp_async16(dst, m.w + wo, 16);
-      tc::cp_async16(dst + 16, m.w + wo + 4, 16);
-      if (gi < 2)
-        cp_async_row_scales<GI>(tc::smem_u32(s_dsc + j * 64 + gi * 32 + ri * GI),
-                                (gi ? m.b : m.s) + (ee * H + row) * GI);
-    }
-  }
-  tc::cp_async_commit();
+  if (!staged) stage_down();
   if (!grid_barrier(w.hdr, bbase + 2ull * gridDim.x, &s_abort)) {
     tc::cp_async_wait_all();  // no copy may land after the block has left
     return;

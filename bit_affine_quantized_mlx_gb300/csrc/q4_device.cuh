@@ -35,19 +35,40 @@ __device__ __forceinline__ uint16_t f2bf16_rne(float f) {
   return r;
 }
 
-// Streaming 16-byte load: read-only, no L1 allocation (weights are read once).
+// L2 policy of the weight streams: evict first.  A layer's weights are read once per step and
+// are far larger than L2; left at normal priority they would push out what is reused -- the
+// kernels' code, activations, routing scratch.
+__device__ __forceinline__ uint64_t l2_evict_first() {
+  uint64_t p;
+  asm("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+// Streaming 16-byte load: read-only, no L1 allocation, evict-first in L2 (weights are read once).
 __device__ __forceinline__ uint4 ld_stream(const void *p) {
   uint4 r;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+  asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0,%1,%2,%3}, [%4], %5;"
                : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-               : "l"(p));
+               : "l"(p), "l"(l2_evict_first()));
   return r;
 }
 
 __device__ __forceinline__ uint16_t ld_u16(const uint16_t *p) {
   uint16_t r;
-  asm volatile("ld.global.nc.u16 %0, [%1];" : "=h"(r) : "l"(p));
+  asm volatile("ld.global.nc.L2::cache_hint.u16 %0, [%1], %2;" : "=h"(r) : "l"(p), "l"(l2_evict_first()));
   return r;
+}
+
+// 16- and 4-byte global -> shared copies of weights (cp.async), evict-first in L2.
+__device__ __forceinline__ void cp_async16_stream(uint32_t dst, const void *src) {
+  asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
+               "l"(l2_evict_first())
+               : "memory");
+}
+__device__ __forceinline__ void cp_async4_stream(uint32_t dst, const void *src) {
+  asm volatile("cp.async.ca.shared.global.L2::cache_hint [%0], [%1], 4, %2;" ::"r"(dst), "l"(src),
+               "l"(l2_evict_first())
+               : "memory");
 }
 
 // One lane's share of an activation row for one 64-wide group, prepared for q4_group_dot.
@@ -392,6 +413,54 @@ __device__ __forceinline__ void warp_argmax(float &v, int &i) {
   const uint32_t kmax = __reduce_max_sync(0xffffffffu, key);
   i = (int)__reduce_min_sync(0xffffffffu, key == kmax ? (uint32_t)i : 0xffffffffu);
   v = key2f(kmax);
+}
+
+// Top-k of one row of logits by one warp: lane j holds logits j, j+32, ... as order-preserving
+// keys (NaN counts as -inf); each of the k rounds takes the warp maximum of the keys (one
+// reduction), then the lowest index holding it (a second reduction), and removes that entry.
+// Lane i < k receives selection i (descending value, ties to the lower index): its index and
+// value.  The lane's running maximum is a tree of max operations, so a round is a short chain.
+template <int EC>  // entries per lane: E <= 32 * EC
+__device__ __forceinline__ void warp_topk(const float *lg, int E, int k, int &my_e, float &my_v) {
+  const int lane = threadIdx.x & 31;
+  uint32_t key[EC];
+#pragma unroll
+  for (int j = 0; j < EC; ++j) {
+    const int e = lane + 32 * j;
+    key[j] = e < E ? f2key(cand(__ldcg(lg + e))) : 0u;  // 0 sorts below every real key
+  }
+  my_e = 0;
+  my_v = 0.f;
+#pragma unroll 1
+  for (int i = 0; i < k; ++i) {
+    uint32_t m[EC];
+#pragma unroll
+    for (int j = 0; j < EC; ++j) m[j] = key[j];
+#pragma unroll
+    for (int s = 1; s < EC; s *= 2) {
+#pragma unroll
+      for (int j = 0; j < EC; j += 2 * s) m[j] = max(m[j], m[j + s]);
+    }
+    const uint32_t M = __reduce_max_sync(0xffffffffu, m[0]);
+    // the lane's lowest entry holding M: a mask of the equal entries (independent compares,
+    // OR-ed as a tree), then its lowest set bit
+    uint32_t bits[EC];
+#pragma unroll
+    for (int j = 0; j < EC; ++j) bits[j] = key[j] == M ? (1u << j) : 0u;
+#pragma unroll
+    for (int s = 1; s < EC; s *= 2) {
+#pragma unroll
+      for (int j = 0; j < EC; j += 2 * s) bits[j] |= bits[j + s];
+    }
+    const uint32_t ce = bits[0] ? (uint32_t)(lane + 32 * (__ffs(bits[0]) - 1)) : 0xffffffffu;
+    const uint32_t be = __reduce_min_sync(0xffffffffu, ce);
+    const bool mine = (int)(be & 31u) == lane;
+    const int jw = (int)(be >> 5);
+#pragma unroll
+    for (int j = 0; j < EC; ++j) key[j] = (mine && jw == j) ? 0u : key[j];
+    my_e = lane == i ? (int)be : my_e;
+    my_v = lane == i ? key2f(M) : my_v;
+  }
 }
 
 // (value, index) ordering used by every argmax / top-k: larger value first, then lower index.
