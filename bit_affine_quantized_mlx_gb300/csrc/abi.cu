@@ -61,10 +61,6 @@ static int check_layer(const lily_q4_moe_layer *L) {
   return LILY_Q4_OK;
 }
 
-static bool has_8bit_parts(const lily_q4_moe_layer &L) {
-  return L.router_bits == 8 || (L.has_shared && L.shared_bits == 8);
-}
-
 static int check_io(const uint16_t *x, uint16_t *y, int32_t *idx, float *w, void *ws) {
   if (!x || !y || !ws) return LILY_Q4_ERR_INVALID_ARG;
   if (!aligned(x, 16) || !aligned(y, 16) || !aligned(ws, kAlign)) return LILY_Q4_ERR_INVALID_ARG;
@@ -137,7 +133,7 @@ size_t lily_q4_moe_workspace_bytes(const lily_q4_moe_layer *layer, int32_t T, in
 int lily_q4_moe_launches(const lily_q4_moe_layer *layer, int32_t T, int32_t prefill) {
   if (check_layer(layer) != LILY_Q4_OK || T <= 0) return 0;
   if (prefill)
-    return !has_8bit_parts(*layer) && T <= 8192 && layer->hidden >= 128 && layer->inter >= 128 ? 8 : 0;
+    return T <= 8192 && layer->hidden >= 128 && layer->inter >= 128 ? prefill_launch_count(*layer) : 0;
   return T <= 16 ? decode_launch_count(*layer, T) : 0;
 }
 
@@ -233,7 +229,6 @@ int lily_q4_moe_prefill(const lily_q4_moe_layer *layer, const uint16_t *x, int32
                         size_t ws_bytes, lily_q4_stream_t stream) {
   int rc = check_layer(layer);
   if (rc != LILY_Q4_OK) return rc;
-  if (has_8bit_parts(*layer)) return LILY_Q4_ERR_UNSUPPORTED;
   if (T < 0 || T > 8192) return LILY_Q4_ERR_INVALID_ARG;
   if (T == 0) return LILY_Q4_OK;
   rc = check_io(x, y, topk_idx, topk_w, ws);

@@ -77,10 +77,17 @@ struct PrefillWsLayout {
   size_t off_xperm;     // bf16 [T][H] token rows in the permuted K order
   size_t off_h;         // bf16 [P][I] SwiGLU activations, sorted by expert
   size_t off_o;         // bf16 [P][H] weighted expert outputs, sorted by expert
+  // affine 8-bit parts
+  int Kr;               // reduction length of the router GEMM: H, or for an 8-bit router its
+                        // exact bf16 form (2H + 3 H/64, rounded up to whole K-split blocks)
+  size_t off_r8a;       // bf16 [E][Kr] the 8-bit router's exact bf16 form
+  size_t off_r8b;       // bf16 [T][Kr] token rows widened to match
+  size_t off_sh8;       // 8-bit shared expert as 4-bit codes of twice the width: gate, up, down
   size_t total;
   int max_items;
 };
 PrefillWsLayout prefill_ws_layout(const lily_q4_moe_layer &L, int T);
+int prefill_launch_count(const lily_q4_moe_layer &L);
 int launch_moe_prefill(const lily_q4_moe_layer &L, const uint16_t *x, int T, uint16_t *y,
                        int32_t *topk_idx, float *topk_w, void *ws, cudaStream_t st);
 

@@ -19,6 +19,20 @@
 //                 scaled by the pair's gate weight -> o (bf16)
 //   combine     : y[t] = sum over t's k slots (+ shared) of o, in slot order (deterministic)
 //
+// Layers with affine 8-bit parts (the report's checkpoint keeps its router gates at 8 bits,
+// "Hardware and software"; the fork page's q4-xl conversion keeps the shared expert at 8 bits,
+// "The model") take two preparation launches in front:
+//   8-bit router        : w = s*q + b with s*q exact in 16 bits, split exactly into bf16 hi +
+//                         lo; the bias term uses the per-group sums of x split exactly into
+//                         three bf16 parts.  The router GEMM then runs on
+//                         A = [hi | lo | b | b | b], B = [x | x | X_hi | X_mid | X_lo]: every
+//                         product exact, fp32 accumulation, logits not rounded.
+//   8-bit shared expert : q = lo + 16 hi, so s*q + b = (s*lo + b + 128 s) + (16 s*hi - 128 s)
+//                         -- each row becomes a 4-bit row of twice the width (low nibbles with
+//                         (s, b + 128 s), high nibbles with (16 s, -128 s)); the expert GEMMs run
+//                         the shared expert's tiles with K doubled, reading its token (or h)
+//                         rows twice.
+//
 // The GEMM kernel is persistent (one CTA per SM) and warp-specialised:
 //   warps 0-3  epilogue: tcgen05.ld of the fp32 accumulator (TMEM lanes 0..127)
 //   warp  4    TMEM allocation and the single-thread tcgen05.mma issue loop
@@ -97,6 +111,7 @@ struct GemmArgs {
   const int32_t *n_items_ptr;
   int n_items_static, mt_static, T;
   int ksplit;                    // router: K is split in ksplit parts (partial logits)
+  int ksh;                       // the shared expert's K is ksh * K (2: an 8-bit shared expert)
   uint16_t *h_out;
   uint16_t *o_out;
   int o_ld;                      // H
@@ -132,6 +147,12 @@ __device__ __forceinline__ int4 get_item(const GemmArgs &a, int it, const int4 *
   }
   const int i = (it - (int)blockIdx.x) / (int)gridDim.x;
   return i < kSmemItems ? s_items[i] : a.items[it];
+}
+
+// k-blocks of work item `item` (the shared expert, id E, may have a K of ksh times K).
+template <int MODE>
+__device__ __forceinline__ int item_nkb(const GemmArgs &a, const int4 &item, int nkb) {
+  return (MODE != kRouter && item.x == a.E) ? nkb * a.ksh : nkb;
 }
 
 // Position of element r inside its 8-chunk in the permuted K order (0,4,1,5,2,6,3,7).
@@ -326,7 +347,8 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) grouped_gemm_kernel(con
       const int npad = (item.z + 15) & ~15;
       const uint32_t idesc = tc::idesc_bf16_f32(kBM, npad);
       const uint32_t d0 = taddr + (uint32_t)(b * C::ACC_COLS);
-      for (int kb = 0; kb < nkb; ++kb) {
+      const int nk = item_nkb<MODE>(a, item, nkb);
+      for (int kb = 0; kb < nk; ++kb) {
         if (!__all_sync(0xffffffffu, tc::wait_bar(afull(sa), pa, &s_abort, err) &&
                                          tc::wait_bar(bfull(sb), pb, &s_abort, err))) {
           ok = false;
@@ -392,16 +414,18 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) grouped_gemm_kernel(con
         }
         dsto[i] = tc::sw128((uint32_t)n, (uint32_t)c);
       }
-      for (int kb = 0; kb < nkb; ++kb) {
+      const int nk = item_nkb<MODE>(a, item, nkb);
+      for (int kb = 0; kb < nk; ++kb) {
         if (!tc::wait_bar(bempty(sb), pb ^ 1, &s_abort, err)) {
           ok = false;
           break;
         }
         const uint32_t sB = sbase + C::OFF_B + sb * C::B_BYTES;
+        const int kbs = kb < nkb ? kb : kb - nkb;  // a doubled K reads the rows twice
 #pragma unroll
         for (int i = 0; i < QB; ++i)
           if (tb + i * kBThreads < nchunk)
-            tc::cp_async16(sB + dsto[i], srcp[i] + (nbytes[i] ? kb * 64 : 0), nbytes[i]);
+            tc::cp_async16(sB + dsto[i], srcp[i] + (nbytes[i] ? kbs * 64 : 0), nbytes[i]);
         tc::cp_async_arrive_noinc(bfull(sb));
         if (++sb == C::SB) { sb = 0; pb ^= 1; }
       }
@@ -449,23 +473,24 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) grouped_gemm_kernel(con
       // this thread's 16 TMEM columns of an A stage: lane = row (warp w writes lanes
       // 32*(w%4) .. +31, which is where its rows fall), columns mat*32 + half*16 ..
       const uint32_t t_off = ((uint32_t)(warp & 3) << 21) + (uint32_t)(C::A_COL0 + mat * 32 + half * 16);
-      const int ngrp = nkb / KG;
       struct Src {
         const uint32_t *w;
         const uint16_t *s, *b;
         bool valid;
+        int ngrp;  // register groups of the item (the rows of a doubled K are twice as long)
       };
       auto item_src = [&](int it) {
-        Src r{nullptr, nullptr, nullptr, false};
         const int4 item = get_item<MODE>(a, it, s_items);
+        const int nk = item_nkb<MODE>(a, item, nkb);
+        Src r{nullptr, nullptr, nullptr, false, nk / KG};
         const int e = item.x, m = item.w * kBM + row;
         if (m < a.a_rows) {
           const bool sh = (e == a.E);
           const lily_q4_mat &W = sh ? (mat ? a.sh1 : a.sh0) : (mat ? a.a1 : a.a0);
           const size_t rr = (sh ? 0 : (size_t)e * a.a_rows) + (size_t)m;
-          r.w = W.w + rr * (size_t)(a.K / 8) + woff;
-          r.s = W.s + rr * (size_t)G;
-          r.b = W.b + rr * (size_t)G;
+          r.w = W.w + rr * (size_t)(nk * 8) + woff;  // nk * 64 / 8 words a row
+          r.s = W.s + rr * (size_t)nk;
+          r.b = W.b + rr * (size_t)nk;
           r.valid = true;
         }
         return r;
@@ -473,7 +498,7 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) grouped_gemm_kernel(con
       uint4 raw[KG][NV];
       ScaleVec<KG> sc, bc, scn, bcn;
       int c_it = blockIdx.x, c_grp = 0;
-      Src cur{nullptr, nullptr, nullptr, false};
+      Src cur{nullptr, nullptr, nullptr, false, 0};
       if (c_it < n_items) {
         cur = item_src(c_it);
         if (cur.valid) {
@@ -489,7 +514,7 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) grouped_gemm_kernel(con
         // next group
         int n_it = c_it, n_grp = c_grp + 1;
         Src nxt = cur;
-        if (n_grp == ngrp) {
+        if (n_grp == cur.ngrp) {
           n_grp = 0;
           n_it += gridDim.x;
           if (n_it < n_items) nxt = item_src(n_it);
@@ -867,6 +892,149 @@ __global__ void combine_kernel(const uint16_t *__restrict__ o, const int32_t *__
 }
 
 // -------------------------------------------------------------------------------------
+// affine 8-bit parts
+// -------------------------------------------------------------------------------------
+
+// Row e of the 8-bit router in its exact bf16 form, A[e] = [hi | lo | b | b | b | 0...]:
+// s*q (bf16 s times a byte code) has at most 16 significant bits, so hi = bf16(s*q) and
+// lo = s*q - hi are both exact in bf16.
+__global__ void router8_prep_a_kernel(lily_q4_mat r8, int E, int H, int Kr, uint16_t *__restrict__ A) {
+  const int e = blockIdx.x;
+  if (e >= E) return;
+  const int G = H / 64;
+  const uint8_t *codes = reinterpret_cast<const uint8_t *>(r8.w) + (size_t)e * H;  // byte k = code k
+  uint16_t *row = A + (size_t)e * Kr;
+  for (int k = threadIdx.x; k < H; k += blockDim.x) {
+    const float w = bf16f(r8.s[(size_t)e * G + k / 64]) * (float)codes[k];  // exact
+    const uint16_t hi = f2bf16_rne(w);
+    row[k] = hi;
+    row[H + k] = f2bf16_rne(w - bf16f(hi));  // exact
+  }
+  for (int j = threadIdx.x; j < Kr - 2 * H; j += blockDim.x)
+    row[2 * H + j] = j < 3 * G ? r8.b[(size_t)e * G + j % G] : (uint16_t)0;
+}
+
+// Row t of the router GEMM's token operand to match, B[t] = [x | x | X_hi | X_mid | X_lo | 0...]:
+// X_g = the sum of group g of x (fp32, a fixed order), split exactly into three bf16 parts,
+// so A . B = sum_k (s*q)_k x_k + sum_g b_g X_g with every product exact.
+__global__ void router8_prep_b_kernel(const uint16_t *__restrict__ x, int H, int Kr, uint16_t *__restrict__ B) {
+  const int t = blockIdx.x;
+  const int G = H / 64;
+  const uint16_t *xr = x + (size_t)t * H;
+  uint16_t *row = B + (size_t)t * Kr;
+  for (int c = threadIdx.x; c < H / 8; c += blockDim.x) {
+    const uint4 v = __ldg(reinterpret_cast<const uint4 *>(xr) + c);
+    reinterpret_cast<uint4 *>(row)[c] = v;
+    reinterpret_cast<uint4 *>(row + H)[c] = v;
+  }
+  for (int g = threadIdx.x; g < G; g += blockDim.x) {
+    float X = 0.f;
+    for (int k = 0; k < 64; ++k) X += bf16f(xr[64 * g + k]);
+    const uint16_t h1 = f2bf16_rne(X);
+    const float r1 = X - bf16f(h1);
+    const uint16_t h2 = f2bf16_rne(r1);
+    row[2 * H + g] = h1;
+    row[2 * H + G + g] = h2;
+    row[2 * H + 2 * G + g] = f2bf16_rne(r1 - bf16f(h2));
+  }
+  for (int j = 2 * H + 3 * G + threadIdx.x; j < Kr; j += blockDim.x) row[j] = 0;
+}
+
+// An affine 8-bit matrix [N][K] (four byte codes per uint32, lowest byte first) as an affine
+// 4-bit matrix [N][2K]: q = lo + 16 hi gives
+//     s*q + b = (s*lo + (b + 128 s)) + (16 s * hi - 128 s),
+// so row n becomes the low nibbles with scales s and biases b + 128 s, then the high nibbles
+// with scales 16 s and biases -128 s (both exact in bf16).  The split is centred so that both
+// halves stay about as small as the weight itself (b is near -128 s): the tensor-core path
+// rounds each dequantised half to bf16, and uncentred halves of several times the weight's
+// size would multiply that rounding.  b + 128 s is rounded once to bf16 (it is small).
+struct Q8ToQ4x2 {
+  lily_q4_mat src;
+  int N, K;
+  uint32_t *w;  // [N][2K/8]
+  uint16_t *s;  // [N][2K/64]
+  uint16_t *b;
+};
+__global__ void q8_to_q4x2_kernel(Q8ToQ4x2 a) {
+  const int words = a.K / 8, G = a.K / 64;
+  const size_t nw = (size_t)a.N * words, ng = (size_t)a.N * G;
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < nw + ng;
+       i += (size_t)gridDim.x * blockDim.x) {
+    if (i < nw) {
+      const size_t n = i / words;
+      const int m = (int)(i % words);
+      const uint2 c = __ldg(reinterpret_cast<const uint2 *>(a.src.w + n * (a.K / 4)) + m);  // codes 8m..8m+7
+      uint32_t lo = 0, hi = 0;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        lo |= ((c.x >> (8 * j)) & 0xFu) << (4 * j);
+        hi |= ((c.x >> (8 * j + 4)) & 0xFu) << (4 * j);
+        lo |= ((c.y >> (8 * j)) & 0xFu) << (4 * j + 16);
+        hi |= ((c.y >> (8 * j + 4)) & 0xFu) << (4 * j + 16);
+      }
+      a.w[n * 2 * words + m] = lo;
+      a.w[n * 2 * words + words + m] = hi;
+    } else {
+      const size_t j = i - nw, n = j / G;
+      const int g = (int)(j % G);
+      const uint16_t sv = a.src.s[n * G + g];
+      const float sf = bf16f(sv);
+      a.s[n * 2 * G + g] = sv;
+      a.b[n * 2 * G + g] = f2bf16_rne(bf16f(a.src.b[n * G + g]) + 128.0f * sf);
+      a.s[n * 2 * G + G + g] = f2bf16_rne(16.0f * sf);
+      a.b[n * 2 * G + G + g] = f2bf16_rne(-128.0f * sf);
+    }
+  }
+}
+
+// The 4-bit form of an 8-bit shared expert in the workspace: gate, up [I][2H], down [H][2I],
+// each as codes, scales, biases.
+struct Sh8Ptrs {
+  lily_q4_mat gate, up, down;
+};
+static Sh8Ptrs sh8_ptrs(char *base, int H, int I) {
+  Sh8Ptrs p;
+  char *c = base;
+  auto mat = [&](int N, int K) {
+    lily_q4_mat m;
+    m.w = reinterpret_cast<const uint32_t *>(c);
+    c += align_up((size_t)N * (2 * K / 8) * 4);
+    m.s = reinterpret_cast<const uint16_t *>(c);
+    c += align_up((size_t)N * (2 * K / 64) * 2);
+    m.b = reinterpret_cast<const uint16_t *>(c);
+    c += align_up((size_t)N * (2 * K / 64) * 2);
+    return m;
+  };
+  p.gate = mat(I, H);
+  p.up = mat(I, H);
+  p.down = mat(H, I);
+  return p;
+}
+static size_t sh8_bytes(int H, int I) {
+  auto one = [](int N, int K) {
+    return align_up((size_t)N * (2 * K / 8) * 4) + 2 * align_up((size_t)N * (2 * K / 64) * 2);
+  };
+  return 2 * one(I, H) + one(H, I);
+}
+
+static int q8_to_q4x2(const lily_q4_mat &src, int N, int K, const lily_q4_mat &dst, cudaStream_t st) {
+  Q8ToQ4x2 a{src, N, K, const_cast<uint32_t *>(dst.w), const_cast<uint16_t *>(dst.s),
+             const_cast<uint16_t *>(dst.b)};
+  const size_t n = (size_t)N * (K / 8) + (size_t)N * (K / 64);
+  const int sms = sm_count() > 0 ? sm_count() : 1;
+  const size_t want = (n + 255) / 256;
+  q8_to_q4x2_kernel<<<(int)(want < (size_t)4 * sms ? want : (size_t)4 * sms), 256, 0, st>>>(a);
+  return check_launch();
+}
+
+static bool router8(const lily_q4_moe_layer &L) { return L.router_bits == 8; }
+static bool shared8(const lily_q4_moe_layer &L) { return L.has_shared && L.shared_bits == 8; }
+
+int prefill_launch_count(const lily_q4_moe_layer &L) {
+  return 8 + (router8(L) ? 2 : 0) + (shared8(L) ? 3 : 0);
+}
+
+// -------------------------------------------------------------------------------------
 // host side
 // -------------------------------------------------------------------------------------
 
@@ -901,6 +1069,12 @@ PrefillWsLayout prefill_ws_layout(const lily_q4_moe_layer &L, int T) {
   l.off_xperm = take(sizeof(uint16_t) * (size_t)T * l.H);
   l.off_h = take(sizeof(uint16_t) * (size_t)l.P * l.I);
   l.off_o = take(sizeof(uint16_t) * (size_t)l.P * l.H);
+  // the router GEMM's K is split into kRouterSplit(H) parts of whole 64-wide blocks
+  const int kq = 64 * kRouterSplit(l.H);
+  l.Kr = router8(L) ? (2 * l.H + 3 * (l.H / 64) + kq - 1) / kq * kq : l.H;
+  l.off_r8a = router8(L) ? take(sizeof(uint16_t) * (size_t)l.E * l.Kr) : 0;
+  l.off_r8b = router8(L) ? take(sizeof(uint16_t) * (size_t)T * l.Kr) : 0;
+  l.off_sh8 = shared8(L) ? take(sh8_bytes(l.H, l.I)) : 0;
   l.total = off;
   return l;
 }
@@ -956,15 +1130,25 @@ int launch_moe_prefill(const lily_q4_moe_layer &L, const uint16_t *x, int T, uin
   x_perm_kernel<<<(nch + 255) / 256 < 4 * sms ? (nch + 255) / 256 : 4 * sms, 256, 0, st>>>(
       reinterpret_cast<const uint4 *>(x), reinterpret_cast<uint4 *>(xperm), nch, counts, E);
 
-  // router GEMM
+  // router GEMM (an 8-bit router in its exact bf16 form, the token rows widened to match)
+  const uint16_t *ra_a = L.router, *ra_b = x;
+  if (router8(L)) {
+    uint16_t *A = reinterpret_cast<uint16_t *>(b + l.off_r8a);
+    uint16_t *B = reinterpret_cast<uint16_t *>(b + l.off_r8b);
+    router8_prep_a_kernel<<<E, 256, 0, st>>>(L.router_q8, E, H, l.Kr, A);
+    router8_prep_b_kernel<<<T, 256, 0, st>>>(x, H, l.Kr, B);
+    ra_a = A;
+    ra_b = B;
+  }
   GemmArgs ra{};
-  ra.a_bf16 = L.router;
+  ra.a_bf16 = ra_a;
   ra.a_rows = E;
-  ra.K = H;
+  ra.K = l.Kr;
   ra.E = E;
-  ra.b_src = x;
+  ra.b_src = ra_b;
   ra.mt_static = (E + kBM - 1) / kBM;
   ra.ksplit = kRouterSplit(H);
+  ra.ksh = 1;
   ra.n_items_static = ra.mt_static * ((T + kBN - 1) / kBN) * ra.ksplit;
   ra.T = T;
   ra.logits = logits;  // partial logits [ksplit][T][E]
@@ -992,11 +1176,24 @@ int launch_moe_prefill(const lily_q4_moe_layer &L, const uint16_t *x, int T, uin
     return LILY_Q4_ERR_CUDA;
   perm_kernel<<<nexp, kPermThreads, perm_smem, st>>>(pa);
 
+  // an 8-bit shared expert as 4-bit codes of twice the width (its tiles run with K doubled)
+  lily_q4_mat shg = L.sh_gate, shu = L.sh_up, shd = L.sh_down;
+  const int ksh = shared8(L) ? 2 : 1;
+  if (shared8(L)) {
+    const Sh8Ptrs sp = sh8_ptrs(b + l.off_sh8, H, I);
+    if ((rc = q8_to_q4x2(L.sh_gate, I, H, sp.gate, st)) != LILY_Q4_OK) return rc;
+    if ((rc = q8_to_q4x2(L.sh_up, I, H, sp.up, st)) != LILY_Q4_OK) return rc;
+    if ((rc = q8_to_q4x2(L.sh_down, H, I, sp.down, st)) != LILY_Q4_OK) return rc;
+    shg = sp.gate;
+    shu = sp.up;
+    shd = sp.down;
+  }
   GemmArgs ga{};
   ga.a0 = L.gate;
   ga.a1 = L.up;
-  ga.sh0 = L.sh_gate;
-  ga.sh1 = L.sh_up;
+  ga.sh0 = shg;
+  ga.sh1 = shu;
+  ga.ksh = ksh;
   ga.a_rows = I;
   ga.K = H;
   ga.E = E;
@@ -1011,7 +1208,8 @@ int launch_moe_prefill(const lily_q4_moe_layer &L, const uint16_t *x, int T, uin
 
   GemmArgs da{};
   da.a0 = L.down;
-  da.sh0 = L.sh_down;
+  da.sh0 = shd;
+  da.ksh = ksh;
   da.a_rows = H;
   da.K = I;
   da.E = E;

@@ -93,9 +93,8 @@ typedef struct {
   /* Affine 8-bit parts (the report's checkpoint keeps its router gates at 8 bits, "Hardware
    * and software"; the fork page's q4-xl conversion keeps the shared expert at 8 bits, "The
    * model").  8-bit codes: four per uint32 along K, lowest byte first, same bf16 s/b per 64.
-   * Zero-initialised fields mean the 4-bit / bf16 layout above.  The 8-bit parts are served by
-   * lily_q4_moe_decode (H <= 2048); lily_q4_moe_prefill returns LILY_Q4_ERR_UNSUPPORTED for a
-   * layer with them. */
+   * Zero-initialised fields mean the 4-bit / bf16 layout above.  Both lily_q4_moe_decode and
+   * lily_q4_moe_prefill take them (prefill prepares them in its workspace: see there). */
   int32_t shared_bits;         /* 0 or 4: sh_* as above; 8: sh_gate/sh_up [I][H/4], sh_down [H][I/4] */
   int32_t router_bits;         /* 0 or 16: bf16 router; 8: router_q8 [E][H/4] codes (router unused) */
   lily_q4_mat router_q8;       /* the 8-bit router when router_bits == 8 */
@@ -131,6 +130,11 @@ LILY_Q4_API int lily_q4_moe_decode(const lily_q4_moe_layer *layer, const uint16_
  * are multiplied with the gathered token rows, the SwiGLU and the weighted
  * combine are fused into the epilogues.  Arguments as lily_q4_moe_decode.
  * Intermediate activations h are rounded to bf16 (tensor-core operand).
+ * Affine 8-bit parts: an 8-bit router is turned, in the workspace, into an exact bf16 form
+ * (s*q split into two bf16 halves, the bias term against exact bf16 parts of the per-group
+ * sums of x), so its logits are as exact as those of a bf16 router; an 8-bit shared expert is
+ * rewritten as 4-bit codes of twice the width (q = lo + 16 hi, the halves centred) and runs on
+ * the same tensor-core path.  lily_q4_moe_workspace_bytes includes that space.
  * A bounded device-side wait that gives up is reported by lily_q4_workspace_status.
  */
 LILY_Q4_API int lily_q4_moe_prefill(const lily_q4_moe_layer *layer, const uint16_t *x, int32_t T,
@@ -224,7 +228,8 @@ LILY_Q4_API size_t lily_q4_gemv_argmax_workspace_bytes(int32_t N, int32_t K);
  * (prefill = 1) call enqueues for this layer and T; 0 when the arguments are invalid.
  * Decode uses one launch when its single-launch kernel covers the shapes and batch (one
  * block per SM, enqueued as a programmatic dependent of the previous kernel on the
- * stream), three launches otherwise (four with an 8-bit shared expert). */
+ * stream), three launches otherwise (four with an 8-bit shared expert).  Prefill uses 8
+ * launches, plus 2 that prepare an 8-bit router and 3 that prepare an 8-bit shared expert. */
 LILY_Q4_API int lily_q4_moe_launches(const lily_q4_moe_layer *layer, int32_t T, int32_t prefill);
 
 /* Zero-fill a workspace on `stream` (asynchronous). */

@@ -182,18 +182,16 @@ def test_8bit_router_and_shared_expert(torch_dev, H, E, k, I, router_bits, share
     check(torch, dev, L, _inputs(L, key, T), f"8-bit parts r{router_bits} s{shared_bits} T{T}")
 
 
-def test_8bit_parts_launch_counts_and_prefill_refused(torch_dev):
-    """Launch counts of a layer with 8-bit parts (one up to four tokens; four above: the
-    8-bit shared expert's gate/up runs as its own launch), and prefill refuses them."""
+def test_8bit_parts_launch_counts(torch_dev):
+    """Launch counts of a layer with 8-bit parts: decode one launch up to four tokens, four
+    above (the 8-bit shared expert's gate/up runs as its own launch); prefill 8 plus two
+    preparation launches for an 8-bit router and three for an 8-bit shared expert."""
     torch, dev = torch_dev
     L = synth.draw_layer(256, 16, 2, 128, shared=True, router_std=0.05, router_bias=False,
                          key=(85, 0), router_bits=8, shared_bits=8)
     dl = q4.DeviceLayer.upload(L, dev)
     assert q4.lily_q4_moe_launches(dl, 4) == 1 and q4.lily_q4_moe_launches(dl, 5) == 4
-    assert q4.lily_q4_moe_launches(dl, 64, prefill=True) == 0
-    x = q4.to_device(synth.draw_tokens(256, 5, (85, 0)), dev)
-    y = torch.empty_like(x)
-    wsp = q4.new_workspace(q4.lily_q4_moe_workspace_bytes(dl, 5, prefill=True), dev)
-    with pytest.raises(q4.Q4Error) as e:
-        q4.lily_q4_moe_prefill(dl, x, y, ws=wsp)
-    assert e.value.status == q4.ERR_UNSUPPORTED
+    assert q4.lily_q4_moe_launches(dl, 64, prefill=True) == 13
+    Lr = synth.draw_layer(256, 16, 2, 128, shared=True, router_std=0.05, router_bias=False,
+                          key=(85, 1), router_bits=8, shared_bits=4)
+    assert q4.lily_q4_moe_launches(q4.DeviceLayer.upload(Lr, dev), 64, prefill=True) == 10
