@@ -10,6 +10,12 @@ One step = one pass of the whole hot path over synthetic inputs resident in HBM:
 40 layers (18.2 GB), the LM head (175 MB) and the prefill layer (455 MB) are each larger
 than L2 (129 MB), so every timed read comes from HBM without an explicit flush.
 
+Outside the step, on the same GPU and timed the same way: the 40 layers at batch 4, the
+wide-MoE sweep (48 layers of hidden 2048, 512 experts, top-10 + shared, batch 1, 2 and 4),
+the LM head with its log-sum-exp and logprobs, the LM head at 8 bits, the decode layer in the
+q4-xl layout, and the end-to-end figures through the public API with host copies.  Every
+workspace's device-side status is checked after its timed region.
+
 `--impl reference` times the CPU oracle instead (the same metric on the same workload,
 a bounded sample per step).
 """
@@ -35,7 +41,7 @@ EXPERT_BYTES = 1769472  # gate + up + down of one expert at H=2048, I=512 (codes
 # DRAM bytes (read + write) of one single-launch decode-layer kernel at batch 1, from the ncu
 # capture summarised in profiles/moe_decode_fused_decode-layer_H2048_E256_k8.md.  Set to None
 # whenever that kernel changes until it is captured again.
-DECODE_TRAFFIC_BYTES = 17057792  # ncu dram__bytes_read+write of one moe_decode_fused launch
+DECODE_TRAFFIC_BYTES = None  # not yet captured for the current kernel
 
 
 def peaks():
@@ -60,6 +66,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true",
                     help="skip the host-copy end-to-end section (e.g. under a profiler)")
+    ap.add_argument("--no-wide", action="store_true",
+                    help="skip the wide-MoE sweep (48 layers, 43.7 GB of weights)")
     return ap.parse_args()
 
 
@@ -134,6 +142,65 @@ class Clocks:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
                 "reasons": sorted(reasons)}
+
+
+def check_status(q4, ws, stream, what):
+    """Raise if a bounded device-side wait of the workspace's last calls gave up."""
+    rc = q4.lily_q4_workspace_status(ws, stream)
+    if rc != 0:
+        raise RuntimeError(f"{what}: device-side status {rc} ({q4.status_string(rc)})")
+
+
+def layer_bytes(uniq, E, H, T, expert_bytes=EXPERT_BYTES):
+    """Bytes a decode layer must read: the unique routed experts and the shared one, the router
+    (bf16 [E][H]), g_shared, x and y."""
+    return (uniq + 1) * expert_bytes + E * H * 2 + H * 2 + 2 * T * H * 2
+
+
+def time_decode_layers(torch, q4, synth, stream, layers, wl, T, reps, warmup):
+    """Layers launched back to back on `stream` (each a programmatic dependent of the previous
+    kernel), `reps` passes timed with CUDA events; returns per-layer time and the bytes the
+    layers' routing touched."""
+    nl = len(layers)
+    xs = [q4.to_device(synth.draw_tokens(wl.H, T, wl.tokens_key(l)), torch.device(stream.device))
+          for l in range(nl)]
+    ys = [torch.empty_like(x) for x in xs]
+    idx = torch.empty((nl, T, wl.k), dtype=torch.int32, device=stream.device)
+    iv = [idx[l] for l in range(nl)]
+    ws = q4.new_workspace(q4.lily_q4_moe_workspace_bytes(layers[0], T), stream.device)
+
+    def run():
+        for l in range(nl):
+            q4.lily_q4_moe_decode(layers[l], xs[l], ys[l], topk_idx=iv[l], ws=ws, stream=stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            run()
+    stream.synchronize()
+    ms = []
+    for _ in range(reps):
+        a0 = torch.cuda.Event(enable_timing=True)
+        a1 = torch.cuda.Event(enable_timing=True)
+        a0.record(stream)
+        with torch.cuda.stream(stream):
+            run()
+        a1.record(stream)
+        a1.synchronize()
+        ms.append(a0.elapsed_time(a1))
+    check_status(q4, ws, stream, f"decode {wl.name} T{T}")
+    ih = idx.cpu().numpy()
+    uniq = [len(np.unique(ih[l])) for l in range(nl)]
+    byts = statistics.mean(layer_bytes(u, wl.E, wl.H, T) for u in uniq)
+    us = statistics.mean(ms) * 1e3 / nl
+    return us, byts, statistics.mean(uniq), q4.lily_q4_moe_launches(layers[0], T)
+
+
+def decode_entry(us, byts, uniq, T, launches, hbm_peak, what):
+    gbs = byts / (us * 1e-6) / 1e9
+    return {"us_per_layer": round(us, 3), "tok_s_per_layer": round(T / (us * 1e-6), 1),
+            "bytes_per_layer": int(byts), "unique_experts": round(uniq, 2),
+            "hbm_gbs": round(gbs, 1), "frac_of_measured_hbm": round(gbs / hbm_peak, 4),
+            "launches_per_layer": launches, "workload": what}
 
 
 # ----------------------------------------------------------------------------- GB300 arm
@@ -226,8 +293,8 @@ def run_gb300(args):
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
-    if q4.lily_q4_workspace_status(pws, stream) != 0:
-        raise RuntimeError("prefill reported a device-side timeout during warm-up")
+    check_status(q4, dws, stream, "decode (warm-up)")
+    check_status(q4, pws, stream, "prefill (warm-up)")
 
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
     clocks = Clocks(local)
@@ -252,8 +319,9 @@ def run_gb300(args):
     pf_ms = [e[2].elapsed_time(e[3]) for e in evs]
     total_ms, dec_mean, lm_mean, pf_mean = max_over_ranks(
         [total_ms, statistics.mean(dec_ms), statistics.mean(lm_ms), statistics.mean(pf_ms)], dev)
-    if q4.lily_q4_workspace_status(pws, stream) != 0:
-        raise RuntimeError("prefill reported a device-side timeout")
+    check_status(q4, dws, stream, "decode")
+    check_status(q4, lmws, stream, "LM head")
+    check_status(q4, pws, stream, "prefill")
 
     # ---- algorithmic work
     idx_h = idx_all.cpu().numpy()
@@ -269,13 +337,18 @@ def run_gb300(args):
     P = Tp * (pfw.k + 1)
     pf_flops = 6.0 * P * pfw.H * pfw.I + 2.0 * Tp * pfw.H * pfw.E
     pf_tflops = pf_flops / (pf_mean / 1e3) / 1e12
-    pf_bytes = 257 * EXPERT_BYTES + pfw.E * pfw.H * 2 + 2 * Tp * pfw.H * 2
+    # bytes the chunk must read: the experts its routing touched (and the shared one), the
+    # router, x and y
+    pf_touched = len(np.unique(idxp.cpu().numpy()))
+    pf_bytes = (pf_touched + 1) * EXPERT_BYTES + pfw.E * pfw.H * 2 + 2 * Tp * pfw.H * 2
 
     # ---- end to end through the public API: every step copies all layers' x from pinned host
     # memory in one transfer, makes one lily_q4_moe_decode call per layer, and reads every
-    # layer's y back to pinned host memory in one transfer.  Two buffer sets: step s+1's copy in
-    # (on a copy stream) overlaps step s's layers, as a serving loop would; the timer stops
-    # when the last step's y has reached the host.
+    # layer's y back to pinned host memory in one transfer.
+    #  * dependent (the e2e value): the host waits for each step's y before it copies the next
+    #    step's x in, as a greedy decode loop must (its next input depends on this output);
+    #  * overlapped (reported beside it): two buffer sets, step s+1's copy in (on a copy stream)
+    #    overlapping step s's layers -- what independent inputs would allow.
     x_host = torch.empty((nl, T, wl.H), dtype=torch.int16, pin_memory=True)
     for l in range(nl):
         x_host[l].copy_(xs[l].cpu())
@@ -288,6 +361,16 @@ def run_gb300(args):
     buf_free = [torch.cuda.Event(), torch.cuda.Event()]
     for ev in buf_free:
         ev.record(stream)
+
+    def e2e_dep_step():
+        with torch.cuda.stream(stream):
+            xdev[0].copy_(x_host, non_blocking=True)
+            for l in range(nl):
+                q4.lily_q4_moe_decode(layers[l], xdev_v[0][l], ydev_v[0][l], ws=dws, stream=stream)
+            y_host[0].copy_(ydev[0], non_blocking=True)
+            ev = torch.cuda.Event()
+            ev.record(stream)
+        ev.synchronize()  # y is on the host
 
     def e2e_step(s_):
         b = s_ % 2
@@ -383,12 +466,39 @@ def run_gb300(args):
         a1.record(stream)
         a1.synchronize()
     xl_us = max_over_ranks([a0.elapsed_time(a1) * 1e3 / 200], dev)[0]
-    if q4.lily_q4_workspace_status(xl_ws, stream) != 0:
-        raise RuntimeError("q4-xl decode reported a device-side timeout")
+    check_status(q4, xl_ws, stream, "q4-xl decode")
     del xl_layers
 
-    e2e_val = None
+    # ---- the 40 decode layers at batch 4, and the wide-MoE sweep: 48 independently seeded
+    # layers of hidden 2048, 512 experts, top-10 + shared, intermediate 512, at batch 1, 2, 4
+    # (43.7 GB of weights), each timed over `steps` passes of all its layers
+    t4 = time_decode_layers(torch, q4, synth, stream, layers, wl, 4, args.steps, args.warmup)
+    decode_t4 = decode_entry(*t4[:3], 4, t4[3], pk["hbm_gbs"],
+                             f"decode MoE H2048 E256 top-8 + shared I512, batch 4, {nl} layers")
+    wide = {}
+    if not args.no_wide:
+        ww = synth.WIDE
+        wlayers = [q4.DeviceLayer.upload(ww.layer(l), dev) for l in range(ww.layers)]
+        for Tw in ww.tokens:
+            r_ = time_decode_layers(torch, q4, synth, stream, wlayers, ww, Tw, args.steps, args.warmup)
+            wide[f"wide_t{Tw}"] = decode_entry(*r_[:3], Tw, r_[3], pk["hbm_gbs"],
+                                               f"wide MoE H2048 E512 top-10 + shared I512, batch {Tw}, "
+                                               f"{ww.layers} layers")
+        del wlayers
+        torch.cuda.empty_cache()
+
+    e2e_val = e2e_ovl = None
     if not args.no_e2e:
+        ref_y = torch.stack(ys).cpu().numpy()
+        for _ in range(2):
+            e2e_dep_step()
+        e0 = time.perf_counter()
+        for _ in range(args.steps):
+            e2e_dep_step()
+        e2e_s = max_over_ranks([(time.perf_counter() - e0) / args.steps], dev)[0]
+        e2e_val = round(replica_throughput(nl * T, e2e_s, ws_n), 1)
+        if not np.array_equal(y_host[0].numpy(), ref_y):
+            raise RuntimeError("end-to-end decode outputs differ from the device-timed ones")
         for s_ in range(2):
             e2e_step(s_)
         torch.cuda.synchronize()
@@ -396,11 +506,11 @@ def run_gb300(args):
         for s_ in range(args.steps):
             e2e_step(s_)
         torch.cuda.synchronize()
-        e2e_s = max_over_ranks([(time.perf_counter() - e0) / args.steps], dev)[0]
-        e2e_val = round(replica_throughput(nl * T, e2e_s, ws_n), 1)
-        if not np.array_equal(y_host[(args.steps - 1) % 2].numpy(),
-                              torch.stack(ys).cpu().numpy()):
+        e2e_o = max_over_ranks([(time.perf_counter() - e0) / args.steps], dev)[0]
+        e2e_ovl = round(replica_throughput(nl * T, e2e_o, ws_n), 1)
+        if not np.array_equal(y_host[(args.steps - 1) % 2].numpy(), ref_y):
             raise RuntimeError("end-to-end decode outputs differ from the device-timed ones")
+        check_status(q4, dws, stream, "decode (end to end)")
 
     launches_per_step = (sum(q4.lily_q4_moe_launches(L_, T) for L_ in layers) + 1 +
                          q4.lily_q4_moe_launches(pl, Tp, prefill=True))
@@ -435,11 +545,15 @@ def run_gb300(args):
                        "frac_of_measured_hbm": round(q8_gbs / pk["hbm_gbs"], 4)},
         "decode_q4xl": {"us_per_layer": round(xl_us, 3), "tok_s_per_layer": round(T / (xl_us * 1e-6), 1),
                         "layout": "8-bit router and shared expert, 4-bit routed experts; 8 layers cycled"},
+        "decode_t4": decode_t4,
+        **wide,
         "prefill": {"us": round(pf_mean * 1e3, 1), "gflop": round(pf_flops / 1e9, 2),
                     "tflops": round(pf_tflops, 1),
                     "frac_of_measured_bf16": round(pf_tflops / pk["bf16_tflops_sustained"], 4),
                     "tok_s": round(Tp / (pf_mean / 1e3), 1),
-                    "hbm_gbs_min_bytes": round(pf_bytes / (pf_mean / 1e3) / 1e9, 1)},
+                    "experts_touched": pf_touched, "bytes": pf_bytes,
+                    "hbm_gbs": round(pf_bytes / (pf_mean / 1e3) / 1e9, 1),
+                    "frac_of_burst_bf16": round(pf_tflops / pk["bf16_tflops"], 4)},
         "roofline": {"bound": "hbm", "kernel": "lily_q4_moe_decode (router+top-k, gate/up, down)",
                      "achieved": round(dec_gbs, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
                      "frac": round(dec_gbs / pk["hbm_gbs"], 4), "peak_source": pk["source"],
@@ -447,14 +561,17 @@ def run_gb300(args):
         "e2e": {"value": e2e_val, "unit": UNIT,
                 "h2d_bytes_per_step": nl * T * wl.H * 2, "d2h_bytes_per_step": nl * T * wl.H * 2,
                 "scope": "decode layers through lily_q4_moe_decode; per step one copy of all "
-                         "layers' x from pinned host memory and one copy of all y back, the next "
-                         "step's copy in overlapping the current step's layers"},
+                         "layers' x from pinned host memory, the layers, and one copy of all y "
+                         "back, which the host waits for before the next step's copy in",
+                "overlapped_value": e2e_ovl,
+                "overlapped_scope": "the same with two buffer sets, the next step's copy in "
+                                    "overlapping the current step's layers (independent inputs)"},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk,
         "setup_s": round(gen_s, 1),
     }
     if rank == 0 and not args.no_cpu_baseline:
-        res["cpu_baseline"] = cpu_baseline(wl, budget_s=12.0)
+        res["cpu_baseline"] = cpu_baseline(wl)
     if rank == 0:
         print(json.dumps(res), flush=True)
     if ws_n > 1:
@@ -473,20 +590,91 @@ def _oracle_layer_time(wl, l, T):
     return time.perf_counter() - t0
 
 
-def cpu_baseline(wl, budget_s=12.0, T=1):
-    """Oracle (as it stands) on this host's cores: decode layers at batch T until the budget."""
+def cpu_model():
+    """The host CPU's model name (/proc/cpuinfo or lscpu) and logical core count."""
+    name = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.split(":")[0].strip().lower() in ("model name", "vendor id") and ":" in line:
+                v = line.split(":", 1)[1].strip()
+                name = v if name is None else f"{name} {v}"
+    except Exception:
+        pass
+    if not name:
+        try:
+            for line in open("/proc/cpuinfo"):
+                if line.lower().startswith(("model name", "cpu part", "hardware")):
+                    name = line.split(":", 1)[1].strip()
+                    break
+        except Exception:
+            pass
+    return name or "unknown", os.cpu_count()
+
+
+def cpu_baseline(wl):
+    """The oracle (as it stands: OpenMP over tokens, over rows for the LM head) on this host's
+    cores, on bounded samples of the workloads:
+      * decode layer, batch 1 (the metric): one token runs on one thread;
+      * decode layer, a batch of one token per thread, all threads (tokens in parallel);
+      * LM head 151,936 x 2048 + argmax: all threads (rows in parallel) and one thread;
+      * prefill chunk of 2048 tokens: a 64-token sample on all threads, scaled to the chunk."""
+    from bit_affine_quantized_mlx_gb300 import synth
     from oracle import oracle as orc
     orc.build()
-    times, l = [], 0
-    t_start = time.perf_counter()
-    while time.perf_counter() - t_start < budget_s and l < wl.layers:
-        times.append(_oracle_layer_time(wl, l, T))
-        l += 1
-    per_layer = statistics.mean(times)
-    return {"value": round(T / per_layer, 3), "unit": UNIT, "cores": 1 if T == 1 else orc.threads(),
-            "kind": "oracle",
-            "sample": f"{len(times)} decode layers at batch {T} (of the {wl.layers}), oracle only, "
-                      "input generation excluded"}
+    n_all = orc.threads()
+    model, ncpu = cpu_model()
+    # decode, batch 1, one thread: two layers, three timings each
+    dec = []
+    for l in range(2):
+        L = wl.layer(l)
+        x = synth.draw_tokens(wl.H, 1, wl.tokens_key(l))
+        for _ in range(3):
+            t0 = time.perf_counter()
+            orc.moe(L, x)
+            dec.append(time.perf_counter() - t0)
+    per_layer = statistics.median(dec)
+    # decode, one token per thread, all threads (the last layer drawn above)
+    xb = synth.draw_tokens(wl.H, n_all, wl.tokens_key(1))
+    t0 = time.perf_counter()
+    orc.moe(L, xb)
+    batch_s = time.perf_counter() - t0
+    # LM head: all threads, then one thread
+    lmw = synth.LMHEAD
+    W = synth.draw_lm_head(lmw.V, lmw.H)
+    xl = synth.draw_lm_x(lmw.H)
+    t0 = time.perf_counter()
+    orc.lm_head(W, xl)
+    lm_all = time.perf_counter() - t0
+    orc.set_threads(1)
+    try:
+        t0 = time.perf_counter()
+        orc.lm_head(W, xl)
+        lm_one = time.perf_counter() - t0
+    finally:
+        orc.set_threads(n_all)
+    del W
+    # prefill: 64 tokens of the 2048-token chunk on all threads
+    pw = synth.PREFILL
+    Lp = pw.layer(0)
+    xp = synth.draw_tokens(pw.H, 64, pw.tokens_key(0))
+    t0 = time.perf_counter()
+    orc.moe(Lp, xp)
+    pf64 = time.perf_counter() - t0
+    Tp = pw.tokens[0]
+    return {"value": round(1 / per_layer, 3), "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": "decode MoE layer (H2048 E256 top-8 + shared I512) at batch 1: 2 of the 40 "
+                      "layers, 3 timings each, median; input generation excluded",
+            "cpu_model": model, "host_logical_cpus": ncpu, "oracle_threads": n_all,
+            "decode_ms_per_layer_1_thread": round(per_layer * 1e3, 2),
+            "decode_batch_all_threads": {"tokens": n_all, "threads": n_all,
+                                         "ms_per_layer": round(batch_s * 1e3, 1),
+                                         "tok_s_per_layer": round(n_all / batch_s, 2)},
+            "lm_head_ms": {"all_threads": round(lm_all * 1e3, 1), "threads": n_all,
+                           "one_thread": round(lm_one * 1e3, 1)},
+            "prefill_chunk_s": {"all_threads": round(pf64 * Tp / 64, 2), "threads": n_all,
+                                "sample": "64 of the 2048 tokens, scaled to the chunk",
+                                "tok_s": round(64 / pf64, 1)}}
 
 
 def run_reference(args):

@@ -585,7 +585,7 @@ constexpr long long kBarrierCycles = 2000000000LL;  // ~1 s
 // second grid barrier.
 constexpr int kFusedStaged = 4;
 constexpr int kFusedSlots = kFusedWarps * kFusedStaged;
-constexpr int kFusedMaxLoads = 6;  // 16-byte loads per thread when preparing x or h
+constexpr int kFusedMaxLoads = 7;  // 16-byte loads per thread when preparing x or h
 
 // Dynamic shared memory of the single-launch kernel (byte offsets, 16-byte aligned): x as
 // given, x prepared for the Q4 dot products (pair words + per-group sums), the staged down
