@@ -38,10 +38,10 @@ sys.path.insert(0, ROOT)
 METRIC = "Q4 MoE decode tok/s per layer & HBM GB/s vs peak; prefill chunk TFLOP/s"
 UNIT = "tok/s per layer"
 EXPERT_BYTES = 1769472  # gate + up + down of one expert at H=2048, I=512 (codes + s + b)
-# DRAM bytes (read + write) of one single-launch decode-layer kernel at batch 1, from the ncu
-# capture summarised in profiles/moe_decode_fused_decode-layer_H2048_E256_k8.md.  Set to None
-# whenever that kernel changes until it is captured again.
-DECODE_TRAFFIC_BYTES = None  # not yet captured for the current kernel
+# DRAM bytes (read + write) of one single-launch decode-layer kernel at batch 1, from one ncu
+# capture of that kernel (bench.py --layers 2, the third launch).  Set to None whenever that
+# kernel changes until it is captured again.
+DECODE_TRAFFIC_BYTES = 17064960  # dram__bytes_read.sum 17,064,960 + dram__bytes_write.sum 0
 
 
 def peaks():

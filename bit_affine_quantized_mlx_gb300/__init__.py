@@ -80,6 +80,7 @@ def load(path: Optional[str] = None):
     L.lily_q4_gemv_argmax_workspace_bytes.restype = sz
     L.lily_q4_moe_launches.argtypes = [C.POINTER(lily_q4_moe_layer), i32, i32]
     L.lily_q4_gemv_argmax_noalloc.argtypes = [C.POINTER(lily_q4_mat), i32, i32, vp, vp, vp, vp]
+    L.lily_q4_gemv_argmax_noalloc_status.argtypes = [vp]
     L.lily_q4_gemv_argmax_logprobs.argtypes = [C.POINTER(lily_q4_mat), i32, i32, vp, vp, vp, vp,
                                                vp, sz, vp]
     L.lily_q8_gemv_argmax.argtypes = L.lily_q4_gemv_argmax.argtypes
@@ -96,7 +97,8 @@ def load(path: Optional[str] = None):
     for f in ("lily_q4_moe_decode", "lily_q4_moe_prefill", "lily_q4_gemv_argmax",
               "lily_q4_workspace_init", "lily_q4_workspace_status", "lily_q4_pack",
               "lily_q4_unpack", "lily_q4_version", "lily_q4_moe_launches",
-              "lily_q4_gemv_argmax_noalloc", "lily_q4_gemv_argmax_logprobs",
+              "lily_q4_gemv_argmax_noalloc", "lily_q4_gemv_argmax_noalloc_status",
+              "lily_q4_gemv_argmax_logprobs",
               "lily_q8_gemv_argmax", "lily_q4_selftest_timeout", "lily_q8_gemv_argmax_logprobs"):
         getattr(L, f).restype = C.c_int
     _lib = L
@@ -284,9 +286,10 @@ def lily_q8_gemv_argmax(W, x, token, logits=None, ws=None, stream=None):
 
 
 def lily_q4_selftest_timeout(ws, which: int, stream=None):
-    """Enqueue a wait that runs into its bound (which 0: grid barrier, 1: mbarrier); see
-    include/lily_q4.h."""
-    return _check(load().lily_q4_selftest_timeout(_ptr(ws), ws.numel(), int(which), _stream(stream)),
+    """Enqueue a wait that runs into its bound (which 0: grid barrier, 1: mbarrier); ws=None
+    targets the fixed scratch of lily_q4_gemv_argmax_noalloc.  See include/lily_q4.h."""
+    return _check(load().lily_q4_selftest_timeout(_ptr(ws), ws.numel() if ws is not None else 0,
+                                                  int(which), _stream(stream)),
                   "lily_q4_selftest_timeout")
 
 
@@ -325,6 +328,12 @@ def lily_q4_gemv_argmax_noalloc(W: DeviceQ4, x, token, logits=None, stream=None)
     return _check(load().lily_q4_gemv_argmax_noalloc(C.byref(m), N, K, _ptr(x), _ptr(token),
                                                      _ptr(logits), _stream(stream)),
                   "lily_q4_gemv_argmax_noalloc")
+
+
+def lily_q4_gemv_argmax_noalloc_status(stream=None) -> int:
+    """0, or ERR_TIMEOUT (returned, not raised) if a bounded device wait in a call of
+    lily_q4_gemv_argmax_noalloc gave up since the last check; clears the record."""
+    return int(load().lily_q4_gemv_argmax_noalloc_status(_stream(stream)))
 
 
 def lily_q4_pack(q: np.ndarray) -> np.ndarray:

@@ -158,8 +158,13 @@ int lily_q4_workspace_status(void *ws, lily_q4_stream_t stream) {
 }
 
 int lily_q4_selftest_timeout(void *ws, size_t ws_bytes, int32_t which, lily_q4_stream_t stream) {
-  if (!ws || ws_bytes < kAlign || !aligned(ws, kAlign)) return LILY_Q4_ERR_INVALID_ARG;
   if (which != 0 && which != 1) return LILY_Q4_ERR_INVALID_ARG;
+  if (!ws && ws_bytes == 0) {  // the fixed scratch of lily_q4_gemv_argmax_noalloc
+    const int rc = noalloc_scratch(&ws);
+    if (rc != LILY_Q4_OK) return rc;
+    ws_bytes = kAlign;
+  }
+  if (!ws || ws_bytes < kAlign || !aligned(ws, kAlign)) return LILY_Q4_ERR_INVALID_ARG;
   return selftest_wait(ws, which, (cudaStream_t)stream);
 }
 

@@ -58,6 +58,9 @@ int decode_launch_count(const lily_q4_moe_layer &L, int T);
 // One block waiting on a grid barrier (which = 0) or an mbarrier (1) that never completes,
 // until the bound; records the time-out in the workspace header.
 int selftest_wait(void *ws, int which, cudaStream_t st);
+// Device address, on the current device, of the fixed scratch of lily_q4_gemv_argmax_noalloc
+// (a workspace header followed by the per-block argmax pairs).
+int noalloc_scratch(void **out);
 int launch_moe_decode(const lily_q4_moe_layer &L, const uint16_t *x, int T, uint16_t *y,
                       int32_t *topk_idx, float *topk_w, void *ws, cudaStream_t st);
 

@@ -568,7 +568,7 @@ static __device__ __align__(256) unsigned char g_gemv_argmax_scratch[kNoAllocScr
 
 // Device address of g_gemv_argmax_scratch on the current device, looked up once per device.
 // (In host code the array's name is only a host-side stand-in, never a device address.)
-static int noalloc_scratch(void **out) {
+int noalloc_scratch(void **out) {
   static std::mutex mu;
   static void *addr[64] = {nullptr};
   int dev = 0;
@@ -602,9 +602,20 @@ extern "C" int lily_q4_gemv_argmax_noalloc(const lily_q4_mat *W, int32_t N, int3
   int rc = noalloc_scratch(&scratch);
   if (rc != LILY_Q4_OK) return rc;
   cudaStream_t st = (cudaStream_t)stream;
-  // start from a zero counter even if an earlier call was cut short
-  if (cudaMemsetAsync(scratch, 0, kHdrWords * sizeof(int32_t), st) != cudaSuccess)
+  // Start from zero counters even if an earlier call was cut short.  The error word (the
+  // header's first) is left as it is: a bounded wait that gave up in an earlier call stays
+  // recorded until lily_q4_gemv_argmax_noalloc_status reads it.
+  if (cudaMemsetAsync(static_cast<int32_t *>(scratch) + kHdrCounterA, 0,
+                      (kHdrWords - kHdrCounterA) * sizeof(int32_t), st) != cudaSuccess)
     return LILY_Q4_ERR_CUDA;
   return launch_gemv_argmax(*W, N, K, x, token, logits, scratch, st);
 }
 
+
+extern "C" int lily_q4_gemv_argmax_noalloc_status(lily_q4_stream_t stream) {
+  using namespace lq4;
+  void *scratch = nullptr;
+  const int rc = noalloc_scratch(&scratch);
+  if (rc != LILY_Q4_OK) return rc;
+  return lily_q4_workspace_status(scratch, stream);
+}

@@ -985,6 +985,39 @@ __device__ __forceinline__ void load_phase_a(const FusedArgs &a, int task, int n
   }
 }
 
+// Phase timeline of the kernel, for profiling builds only (-DLILY_Q4_TRACE): thread 0 of each
+// block stamps %globaltimer at fixed points into a device array, [launch parity][block][point]
+// (the parity of the launch's index on the workspace, from its grid-barrier count):
+// 7 the previous kernel complete (griddepcontrol.wait returned), 0 x prepared, 1 phase A (router
+// rows, shared gate/up) done, 2 first grid barrier passed, 3 routed, 4 gate/up done, 5 second
+// grid barrier passed, 6 h prepared and down rows landed, 8 down done, 9 y written.
+#ifdef LILY_Q4_TRACE
+constexpr int kTracePoints = 16;
+__device__ unsigned long long g_lq4_trace[2][1024][kTracePoints];
+__device__ __forceinline__ unsigned long long lq4_now() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+#define LQ4_TRACE_AT(i, par, t)                                 \
+  do {                                                          \
+    if (threadIdx.x == 0 && blockIdx.x < 1024)                  \
+      g_lq4_trace[(par) & 1ull][blockIdx.x][(i)] = (t);         \
+  } while (0)
+#define LQ4_TRACE(i, par) LQ4_TRACE_AT(i, par, lq4_now())
+#define LQ4_TRACE_CLOCK(var) const unsigned long long var = lq4_now()
+#else
+#define LQ4_TRACE_AT(i, par, t) \
+  do {                          \
+  } while (0)
+#define LQ4_TRACE(i, par) \
+  do {                    \
+  } while (0)
+#define LQ4_TRACE_CLOCK(var) \
+  do {                       \
+  } while (0)
+#endif
+
 // Q8P: the layer has 8-bit parts (router and/or shared expert); the instantiation without
 // them carries none of their branches.
 template <int GH, int GI, int EC, bool Q8P>
@@ -1025,6 +1058,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
   uint32_t sc[4];
   if (gw < ntasks_a) load_phase_a<GH, Q8P>(a, gw, nrouter, lane, wv, sc);
   asm volatile("griddepcontrol.wait;" ::: "memory");
+  LQ4_TRACE_CLOCK(t_wait);
   // The barrier base is read by the last warp, which has no phase-A rows: the acquire load
   // holds up only that warp while the others issue their weight loads.
   if (threadIdx.x == kFusedThreads - 32) {
@@ -1044,6 +1078,9 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
   xg_stage<true>(s_xp, s_xX, a.x, T * H / 8, reinterpret_cast<uint4 *>(fsm + L0.xr));
   __syncthreads();
   const unsigned long long bbase = s_bbase;
+  [[maybe_unused]] const unsigned long long par = bbase / (2ull * gridDim.x);  // launch index
+  LQ4_TRACE_AT(7, par, t_wait);
+  LQ4_TRACE(0, par);
   for (int task = gw; task < ntasks_a; task += nw) {
     if (task != gw) load_phase_a<GH, Q8P>(a, task, nrouter, lane, wv, sc);
     if (Q8P && task < E && a.router_bits == 8) {
@@ -1115,7 +1152,9 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
       }
     }
   }
+  LQ4_TRACE(1, par);
   if (!grid_barrier(w.hdr, bbase + gridDim.x, &s_abort)) return;
+  LQ4_TRACE(2, par);
 
   // ------------------------------------------------------------------ phase B
   {
@@ -1123,6 +1162,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
                blockIdx.x == 0 ? a.out_idx : nullptr, blockIdx.x == 0 ? a.out_w : nullptr};
     route_small<EC>(w.logits, w.sigma, T, E, k, a.has_shared, d);
   }
+  LQ4_TRACE(3, par);
   const int U = s_U;
   const int Ur = a.has_shared ? U - 1 : U;  // routed unique experts
   // Down tasks (pair pr, row-step qi) -> j = pr * nq_cta + qi.  The first kFusedSlots are
@@ -1199,6 +1239,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
     }
   }
   if (!staged) stage_down();
+  LQ4_TRACE(4, par);
   if (!grid_barrier(w.hdr, bbase + 2ull * gridDim.x, &s_abort)) {
     tc::cp_async_wait_all();  // no copy may land after the block has left
     return;
@@ -1210,9 +1251,11 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
   const FusedLayout LP = fused_layout(P, T, H, I);
   uint32_t *s_hp = reinterpret_cast<uint32_t *>(fsm + LP.hp);
   float *s_hX = reinterpret_cast<float *>(fsm + LP.hX);
+  LQ4_TRACE(5, par);
   xg_stage<false>(s_hp, s_hX, h16, P * I / 8, nullptr);
   tc::cp_async_wait_all();
   __syncthreads();
+  LQ4_TRACE(6, par);
   constexpr int ROWS = kFusedMaxQ * RPS_I;  // rows of this block, at most
   __shared__ float s_part[kFusedMaxT * (kMaxK + 1)][ROWS];
   {
@@ -1284,6 +1327,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
     }
   }
   __syncthreads();
+  LQ4_TRACE(8, par);
   const int nrows_cta = nq_cta * RPS_I;
   for (int j = threadIdx.x; j < T * nrows_cta; j += kFusedThreads) {
     const int t = j / nrows_cta, rr = j % nrows_cta;
@@ -1293,7 +1337,15 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
       if (s_pair_tok[pr] == t) acc += s_part[pr][rr];
     a.y[(size_t)t * H + row] = f2bf16_rne(acc);
   }
+  LQ4_TRACE(9, par);
 }
+
+#ifdef LILY_Q4_TRACE
+extern "C" __attribute__((visibility("default"))) int lily_q4_trace_read(void *host, size_t bytes) {
+  if (bytes > sizeof(g_lq4_trace)) bytes = sizeof(g_lq4_trace);
+  return cudaMemcpyFromSymbol(host, g_lq4_trace, bytes) == cudaSuccess ? 0 : -1;
+}
+#endif
 
 static bool fused_ok(const lily_q4_moe_layer &L, int T) {
   if (T > kFusedMaxT) return false;

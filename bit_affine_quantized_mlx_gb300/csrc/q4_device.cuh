@@ -420,15 +420,12 @@ __device__ __forceinline__ void warp_argmax(float &v, int &i) {
 // reduction), then the lowest index holding it (a second reduction), and removes that entry.
 // Lane i < k receives selection i (descending value, ties to the lower index): its index and
 // value.  The lane's running maximum is a tree of max operations, so a round is a short chain.
+// warp_topk_keys is the selection on keys the lanes already hold: key[j] of lane l is entry
+// l + 32 j (f2key of the candidate value; 0 for no entry, which sorts below every real key);
+// it consumes the keys.  warp_topk loads them from a row of logits first.
 template <int EC>  // entries per lane: E <= 32 * EC
-__device__ __forceinline__ void warp_topk(const float *lg, int E, int k, int &my_e, float &my_v) {
+__device__ __forceinline__ void warp_topk_keys(uint32_t (&key)[EC], int k, int &my_e, float &my_v) {
   const int lane = threadIdx.x & 31;
-  uint32_t key[EC];
-#pragma unroll
-  for (int j = 0; j < EC; ++j) {
-    const int e = lane + 32 * j;
-    key[j] = e < E ? f2key(cand(__ldcg(lg + e))) : 0u;  // 0 sorts below every real key
-  }
   my_e = 0;
   my_v = 0.f;
 #pragma unroll 1
@@ -461,6 +458,18 @@ __device__ __forceinline__ void warp_topk(const float *lg, int E, int k, int &my
     my_e = lane == i ? (int)be : my_e;
     my_v = lane == i ? key2f(M) : my_v;
   }
+}
+
+template <int EC>
+__device__ __forceinline__ void warp_topk(const float *lg, int E, int k, int &my_e, float &my_v) {
+  const int lane = threadIdx.x & 31;
+  uint32_t key[EC];
+#pragma unroll
+  for (int j = 0; j < EC; ++j) {
+    const int e = lane + 32 * j;
+    key[j] = e < E ? f2key(cand(__ldcg(lg + e))) : 0u;
+  }
+  warp_topk_keys<EC>(key, k, my_e, my_v);
 }
 
 // (value, index) ordering used by every argmax / top-k: larger value first, then lower index.

@@ -116,6 +116,9 @@ typedef struct {
  * topk_w: fp32 [T][k] output (p, same order) or NULL.
  * An expert chosen by several tokens has its rows dequantised once per row block and
  * applied to each of those tokens.
+ * Up to 4 tokens (shapes permitting, see lily_q4_moe_launches) run as one launch of one
+ * block per SM with two grid-wide barriers; its waits are bounded, and one that gives up is
+ * reported by lily_q4_workspace_status.
  * T == 0 returns LILY_Q4_OK and enqueues nothing.
  */
 LILY_Q4_API int lily_q4_moe_decode(const lily_q4_moe_layer *layer, const uint16_t *x, int32_t T,
@@ -202,23 +205,32 @@ LILY_Q4_API size_t lily_q8_gemv_argmax_workspace_bytes(int32_t N, int32_t K);
  * and output pointers) and so have no workspace to give.  Arguments, results and errors
  * are those of lily_q4_gemv_argmax without ws/ws_bytes.
  *
- * The kernel's scratch (a counter and the per-block (max, argmax) pairs) lives in a
- * 16,640-byte __device__ array inside the library, held by every GPU that loads the
- * library until the process exits.  It covers up to 2048 blocks; when
- * lily_q4_gemv_argmax_workspace_bytes(N, K) exceeds 16,640 bytes (GPUs with more than
- * 1024 SMs) the call returns LILY_Q4_ERR_WORKSPACE_TOO_SMALL.  K must be a power of two
- * from 64 to 2048 (else LILY_Q4_ERR_UNSUPPORTED).
+ * The kernel's scratch (a 256-byte header with the counter, then the per-block (max,
+ * argmax) pairs) lives in a 16,640-byte __device__ array inside the library, held by every
+ * GPU that loads the library until the process exits.  It covers up to 2048 blocks; on GPUs
+ * with more than 1024 SMs the call returns LILY_Q4_ERR_WORKSPACE_TOO_SMALL.  K must be a
+ * power of two from 64 to 2048 (else LILY_Q4_ERR_UNSUPPORTED).
  *  - The first call on a device looks up the array's device address on that device
  *    (cudaGetSymbolAddress); make that first call before any stream capture.
  *  - Every call on a device shares the one array and it keeps the last call's contents;
- *    each call clears the counter it needs on `stream` before its kernel.  Calls whose
+ *    each call clears the counters it needs on `stream` before its kernel.  Calls whose
  *    work overlaps on the GPU (different streams without ordering) race on the array:
  *    order them.
+ *  - A bounded device-side wait of the kernel that gives up (the case that
+ *    lily_q4_workspace_status reports for a workspace) is recorded in the array's error
+ *    word.  Later calls leave that word set; lily_q4_gemv_argmax_noalloc_status reads and
+ *    clears it.
  *  - Calls no cudaMalloc, cudaFree or other allocating routine.
  */
 LILY_Q4_API int lily_q4_gemv_argmax_noalloc(const lily_q4_mat *W, int32_t N, int32_t K,
                                             const uint16_t *x, int32_t *token, float *logits,
                                             lily_q4_stream_t stream);
+
+/* Synchronises `stream`, then reads and clears the error word of the fixed scratch of
+ * lily_q4_gemv_argmax_noalloc on the current device: LILY_Q4_OK, or LILY_Q4_ERR_TIMEOUT if a
+ * bounded wait in one of its calls gave up since the last check (LILY_Q4_ERR_CUDA if the
+ * array's address cannot be looked up or the copy fails).  Allocates nothing. */
+LILY_Q4_API int lily_q4_gemv_argmax_noalloc_status(lily_q4_stream_t stream);
 
 /* Workspace sizes (bytes) for the calls above; 0 when the arguments are invalid. */
 LILY_Q4_API size_t lily_q4_moe_workspace_bytes(const lily_q4_moe_layer *layer, int32_t T, int32_t prefill);
@@ -248,7 +260,9 @@ LILY_Q4_API int lily_q4_workspace_status(void *ws, lily_q4_stream_t stream);
  * SM clock), then records the time-out in the workspace header and exits, as a stalled launch
  * of this library would.  lily_q4_workspace_status then returns LILY_Q4_ERR_TIMEOUT.
  * Afterwards the workspace's barrier count is off: re-initialise it (lily_q4_workspace_init)
- * before the next decode.  ws: any workspace of at least 256 bytes.
+ * before the next decode.  ws: any workspace of at least 256 bytes; ws = NULL with
+ * ws_bytes = 0 targets the fixed scratch of lily_q4_gemv_argmax_noalloc instead (its status
+ * is then read by lily_q4_gemv_argmax_noalloc_status; its next call resets the counters).
  */
 LILY_Q4_API int lily_q4_selftest_timeout(void *ws, size_t ws_bytes, int32_t which,
                                          lily_q4_stream_t stream);

@@ -181,6 +181,7 @@ def test_selftest_argument_errors(lib):
     assert f(FAKE + 16, 1024, 0, None) == q4.ERR_INVALID_ARG     # not 256-aligned
     assert f(FAKE, 64, 0, None) == q4.ERR_INVALID_ARG            # smaller than the header
     assert f(FAKE, 1024, 2, None) == q4.ERR_INVALID_ARG          # no such wait
+    assert f(None, 0, 2, None) == q4.ERR_INVALID_ARG             # no such wait (fixed scratch)
 
 
 def test_workspace_sizes(lib):
