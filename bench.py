@@ -157,6 +157,27 @@ def layer_bytes(uniq, E, H, T, expert_bytes=EXPERT_BYTES):
     return (uniq + 1) * expert_bytes + E * H * 2 + H * 2 + 2 * T * H * 2
 
 
+def time_isolated(torch, stream, fn, warmup, reps):
+    """Per-call device time of fn (direct launches on `stream`), each call bracketed by its own
+    pair of events.  A ~1 ms spin kernel first lets the host enqueue every call before the GPU
+    reaches them, so no interval includes host (ctypes) time; the events between calls also
+    keep each call from overlapping its neighbours."""
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            fn()
+    stream.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(reps)]
+    with torch.cuda.stream(stream):
+        torch.cuda._sleep(2_000_000)
+        for a0, a1 in evs:
+            a0.record(stream)
+            fn()
+            a1.record(stream)
+    stream.synchronize()
+    return [a0.elapsed_time(a1) for a0, a1 in evs]
+
+
 def time_decode_layers(torch, q4, synth, stream, layers, wl, T, reps, warmup):
     """Layers launched back to back on `stream` (each a programmatic dependent of the previous
     kernel), `reps` passes timed with CUDA events; returns per-layer time and the bytes the
@@ -245,13 +266,14 @@ def run_gb300(args):
     torch.cuda.synchronize()
     gen_s = time.time() - t0
 
-    # The LM head and prefill parts run as CUDA graphs (captured after a warm-up call of each
-    # part, so one-time library set-up happens outside capture); replaying them keeps the host
-    # (ctypes per call) off the critical path, as a serving loop would.  The decode layers are
-    # launched directly on the stream: each layer's kernel is enqueued as a programmatic
-    # dependent of the previous one, which lets its blocks take SMs while that kernel drains
-    # (a graph replay serialises the kernels fully, about 1 us per layer slower).  The host
-    # enqueues a layer in a few microseconds, well ahead of the ~19 us kernels.
+    # The prefill part runs as a CUDA graph (captured after a warm-up call, so one-time library
+    # set-up happens outside capture); replaying it keeps the host (ctypes per call) off the
+    # critical path, as a serving loop would.  The decode layers and the LM head are launched
+    # directly on the stream: each of their kernels is enqueued as a programmatic dependent of
+    # the previous kernel, which lets its blocks take SMs while that kernel drains (a graph
+    # replay adds its own launch latency, several us for a single-kernel graph).  The host
+    # enqueues a launch in a few microseconds, well ahead of the ~16 us kernels, so the GPU
+    # never waits for it.
     stream = torch.cuda.Stream(device=dev)
 
     idx_v = [idx_all[l] for l in range(nl)]  # views made once: slicing costs host time per call
@@ -272,14 +294,11 @@ def run_gb300(args):
         for f in parts:
             f()
     stream.synchronize()
-    graphs = []
-    for f in parts[1:]:
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=stream):
-            f()
-        graphs.append(g.replay)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        pf_part()
     stream.synchronize()
-    runs = [dec_part] + graphs
+    runs = [dec_part, lm_part, g.replay]
 
     def step(ev=None):
         with torch.cuda.stream(stream):
@@ -385,33 +404,32 @@ def run_gb300(args):
             y_host[b].copy_(ydev[b], non_blocking=True)
             buf_free[b].record(stream)
 
-    # ---- LM head with the full-vocabulary log-sum-exp and log-probabilities (one graph replay
-    # per timing; the same weights and x as the argmax-only LM head above)
+    # ---- LM head with the full-vocabulary log-sum-exp and log-probabilities (the same weights
+    # and x as the argmax-only LM head above), timed as the isolated LM heads below
     lse_d = torch.empty(1, dtype=torch.float32, device=dev)
     lp_d = torch.empty(lmw.V, dtype=torch.float32, device=dev)
 
     def lp_part():
         q4.lily_q4_gemv_argmax_logprobs(W, xl, tok, lse_d, logprobs=lp_d, ws=lmws, stream=stream)
 
-    with torch.cuda.stream(stream):
-        lp_part()
-    stream.synchronize()
-    g_lp = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g_lp, stream=stream):
-        lp_part()
-    lp_ms = []
-    with torch.cuda.stream(stream):
-        for _ in range(args.warmup):
-            g_lp.replay()
-        for _ in range(max(args.steps, 3)):
-            a0 = torch.cuda.Event(enable_timing=True)
-            a1 = torch.cuda.Event(enable_timing=True)
-            a0.record(stream)
-            g_lp.replay()
-            a1.record(stream)
-            a1.synchronize()
-            lp_ms.append(a0.elapsed_time(a1))
+    lp_ms = time_isolated(torch, stream, lp_part, args.warmup, max(args.steps, 3))
     lp_mean = max_over_ranks([statistics.mean(lp_ms)], dev)[0]
+
+    # ---- the argmax LM head in a chain of programmatic-dependent launches, timed as the decode
+    # layers are (one event pair around the chain): two independently drawn heads (350 MB,
+    # beyond L2) alternate, so no launch finds the previous one's weights in L2.  A launch's
+    # weight copies start while the previous launch drains, as they would behind the last
+    # decode layer of a step.
+    W2 = q4.DeviceQ4.upload(synth.draw_lm_head(lmw.V, lmw.H, key=(lmw.wid, 1)), dev)
+    n_chain = 8
+
+    def lm_chain():
+        for i in range(n_chain):
+            q4.lily_q4_gemv_argmax(W if i % 2 == 0 else W2, xl, tok, ws=lmws, stream=stream)
+
+    ch_ms = time_isolated(torch, stream, lm_chain, args.warmup, max(args.steps, 3))
+    ch_mean = max_over_ranks([statistics.mean(ch_ms) / n_chain], dev)[0]
+    del W2
 
     # ---- the same LM head kept at 8 bits (q4-xl), argmax only, timed the same way
     W8 = q4.DeviceQ4.upload(synth.draw_lm_head_q8(lmw.V, lmw.H), dev)
@@ -420,24 +438,7 @@ def run_gb300(args):
     def q8_part():
         q4.lily_q8_gemv_argmax(W8, xl, tok, ws=ws8, stream=stream)
 
-    with torch.cuda.stream(stream):
-        q8_part()
-    stream.synchronize()
-    g_q8 = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g_q8, stream=stream):
-        q8_part()
-    q8_ms = []
-    with torch.cuda.stream(stream):
-        for _ in range(args.warmup):
-            g_q8.replay()
-        for _ in range(max(args.steps, 3)):
-            a0 = torch.cuda.Event(enable_timing=True)
-            a1 = torch.cuda.Event(enable_timing=True)
-            a0.record(stream)
-            g_q8.replay()
-            a1.record(stream)
-            a1.synchronize()
-            q8_ms.append(a0.elapsed_time(a1))
+    q8_ms = time_isolated(torch, stream, q8_part, args.warmup, max(args.steps, 3))
     q8_mean = max_over_ranks([statistics.mean(q8_ms)], dev)[0]
     q8_bytes = lmw.V * lmw.H + lmw.V * (lmw.H // 64) * 4 + lmw.H * 2 + 4
     q8_gbs = q8_bytes / (q8_mean / 1e3) / 1e9
@@ -540,7 +541,13 @@ def run_gb300(args):
                    "frac_of_measured_hbm": round(dec_gbs / pk["hbm_gbs"], 4)},
         "lm_head": {"us": round(lm_mean * 1e3, 2), "bytes": lm_bytes,
                     "hbm_gbs": round(lm_gbs, 1), "frac_of_measured_hbm": round(lm_gbs / pk["hbm_gbs"], 4),
-                    "with_logprobs_us": round(lp_mean * 1e3, 2)},
+                    "with_logprobs_us": round(lp_mean * 1e3, 2),
+                    "chained_us": round(ch_mean * 1e3, 2),
+                    "chained_hbm_gbs": round(lm_bytes / (ch_mean / 1e3) / 1e9, 1),
+                    "chained_frac_of_measured_hbm": round(lm_bytes / (ch_mean / 1e3) / 1e9 / pk["hbm_gbs"], 4),
+                    "scope": "us: one launch between events after the step's decode layers; "
+                             "chained_us: per launch in a chain of 8 programmatic-dependent "
+                             "launches alternating two heads"},
         "lm_head_q8": {"us": round(q8_mean * 1e3, 2), "bytes": q8_bytes, "hbm_gbs": round(q8_gbs, 1),
                        "frac_of_measured_hbm": round(q8_gbs / pk["hbm_gbs"], 4)},
         "decode_q4xl": {"us_per_layer": round(xl_us, 3), "tok_s_per_layer": round(T / (xl_us * 1e-6), 1),

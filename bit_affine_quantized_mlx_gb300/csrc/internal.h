@@ -18,6 +18,7 @@ enum HeaderWord : int {
   kHdrCounterB = 2,
   kHdrCounterC = 3,
   kHdrBarrier64 = 4,  // words 4-5: 64-bit grid-barrier arrival count
+  kHdrArgmax64 = 6,   // words 6-7: the LM head's running (value, row) maximum, packed (self-resetting)
   kHdrWords = 64,
 };
 

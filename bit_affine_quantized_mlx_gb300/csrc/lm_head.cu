@@ -125,9 +125,12 @@ __global__ void sub_lse_kernel(float *__restrict__ v, int N, const float *__rest
     v[i] -= l;
 }
 
-// Block-wide then grid-wide argmax of the threads' (value, row) pairs: every block publishes
-// its best pair, and the last block to finish (ticket on header counter A) reduces the pairs
-// into *token and re-arms the counter for the next call.
+// Block-wide then grid-wide argmax of the threads' (value, row) pairs.  Argmax only: every
+// block folds its best pair into one 64-bit maximum in the header (the order-preserving key
+// of the value above the complement of the row, so a larger value wins and equal values go to
+// the lower row), and the last block to finish (ticket on header counter A) reads it into
+// *token and re-arms maximum and counter for the next call.  With the log-sum-exp, every
+// block publishes its best pair and partials and the last block reduces them.
 // With LSE, the threads' (m, s) log-sum-exp partials are reduced alongside, in a fixed order
 // (deterministic), into *lse = m + log(s).
 struct LseOut {
@@ -144,6 +147,30 @@ __device__ __forceinline__ void block_argmax_finish(float best_v, int best_i, in
   warp_argmax(best_v, best_i);
   __shared__ float sv_[NW];
   __shared__ int si_[NW];
+  if constexpr (!LSE) {
+    if (lane == 0) {
+      sv_[warp] = best_v;
+      si_[warp] = best_i;
+    }
+    __syncthreads();
+    if (warp == 0) {
+      float v = lane < NW ? sv_[lane] : -INFINITY;
+      int i = lane < NW ? si_[lane] : INT_MAX;
+      warp_argmax(v, i);
+      if (lane == 0) {
+        unsigned long long *mx = reinterpret_cast<unsigned long long *>(hdr + kHdrArgmax64);
+        atomicMax(mx, ((unsigned long long)f2key(v) << 32) | (0xFFFFFFFFu - (uint32_t)i));
+        __threadfence();
+        if (atomicAdd(hdr + kHdrCounterA, 1) == (int)gridDim.x - 1) {
+          __threadfence();
+          const unsigned long long k = atomicExch(mx, 0ull);  // read, and re-arm
+          *token = (int32_t)(0xFFFFFFFFu - (uint32_t)k);
+          hdr[kHdrCounterA] = 0;
+        }
+      }
+    }
+    return;
+  }
   __shared__ float sm_[LSE ? NW : 1], ss_[LSE ? NW : 1];
   __shared__ int is_last;
   if (LSE) lse_warp(lm, ls);
@@ -297,6 +324,30 @@ __global__ void __launch_bounds__(kLmThreads, kLmBlocksPerSm)
 }
 
 // ---------------------------------------------------------------------------------------
+// Timeline of the streaming kernel's last launch, for profiling builds only (-DLILY_Q4_TRACE):
+// %globaltimer stamps by thread 0 of each block ([block][point]: 0 block set up, 1 x prepared,
+// 2 first stage landed, 3 last stage computed, 4 the block's argmax folded in, 5 block done)
+// and by the copy thread (6 last copy issued).
+#ifdef LILY_Q4_TRACE
+__device__ unsigned long long g_lm_trace[1024][8];
+#define LM_TRACE(i, cond)                                                  \
+  do {                                                                     \
+    if ((cond) && blockIdx.x < 1024) {                                     \
+      unsigned long long t_;                                               \
+      asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t_));               \
+      g_lm_trace[blockIdx.x][(i)] = t_;                                    \
+    }                                                                      \
+  } while (0)
+extern "C" __attribute__((visibility("default"))) int lily_q4_lm_trace_read(void *host, size_t bytes) {
+  if (bytes > sizeof(g_lm_trace)) bytes = sizeof(g_lm_trace);
+  return cudaMemcpyFromSymbol(host, g_lm_trace, bytes) == cudaSuccess ? 0 : -1;
+}
+#else
+#define LM_TRACE(i, cond) \
+  do {                    \
+  } while (0)
+#endif
+
 // Streaming variant for rows of at least 8 groups (K >= 512), the LM-head shapes.
 //
 // Each block owns a contiguous range of rows -- one contiguous range of codes, of scales and
@@ -333,6 +384,11 @@ __global__ void __launch_bounds__(kLsThreads, 1)
   const uint32_t bar0 = sbase + C::OFF_BAR;
   auto full = [&](int i) { return bar0 + 8u * i; };
   auto empty = [&](int i) { return bar0 + 8u * (kLsStages + i); };
+  // Launched as a programmatic dependent of the previous kernel on the stream: let the next
+  // kernel be scheduled early too.  The copy thread streams the weights (which no kernel
+  // writes) at once; every other thread waits for the previous kernel before it reads x, the
+  // workspace or the outputs.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   int32_t *err = hdr + kHdrError;
   const int r_begin = min(N, (int)blockIdx.x * rows_per_block);
@@ -347,6 +403,7 @@ __global__ void __launch_bounds__(kLsThreads, 1)
     tc::mbar_init_fence();
   }
   __syncthreads();
+  LM_TRACE(0, threadIdx.x == 0);
 
   float best_v = -INFINITY;
   int best_i = INT_MAX;
@@ -367,6 +424,7 @@ __global__ void __launch_bounds__(kLsThreads, 1)
         tc::bulk_g2s(dst + kLsStageCodes, s + (size_t)r0 * G, sb, full(slot));
         tc::bulk_g2s(dst + kLsStageCodes + C::SC, b + (size_t)r0 * G, sb, full(slot));
       }
+      LM_TRACE(6, true);
       if (s_abort) {
         // after a time-out: let the copies still in flight land before the block exits
         for (int j = st > kLsStages ? st - kLsStages : 0; j < st; ++j) {
@@ -380,6 +438,9 @@ __global__ void __launch_bounds__(kLsThreads, 1)
   } else {
     // ---------------------------------------------------------------- compute warps
     const int g = lane % G, rsub = lane / G;
+    // x is the previous kernel's output: wait for it (the copy thread streams weights, which
+    // do not depend on it, from the start)
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     // x pairs in the order the codes unpack in (4-bit: (x_j, x_j+4); 8-bit: (x_j, x_j+2))
     std::conditional_t<BITS == 8, XGroup8, XGroupB> xg;
     {
@@ -392,29 +453,41 @@ __global__ void __launch_bounds__(kLsThreads, 1)
       else
         xgroupb_from_bf16(xg, c);
     }
+    LM_TRACE(1, threadIdx.x == 0);
+    constexpr int NV = C::CB / 16;          // 16-byte code vectors of a lane's group
+    constexpr int ROW_B = C::CB * G;        // code bytes of a row
+    // The warp's rows of a stage are lr = row0 + u * RPS (u < WR); the lane's code and scale
+    // offsets inside a stage are fixed, so the per-row addressing is a constant per u.
+    const int row0 = warp * C::WR * C::RPS + rsub;
+    const int code_off = row0 * ROW_B + C::CB * g;
+    const int sc_off = row0 * G + g;
+    // Two rows of 32 groups per warp-step pair (the LM-head shape): their sums are reduced
+    // together -- lanes 0-15 finish the first row, 16-31 the second -- and lanes 0 and 16
+    // each keep their row's argmax candidate.
+    constexpr bool PAIR = (G == 32 && C::WR == 2);
 #pragma unroll 1
     for (int st = 0; st < nst; ++st) {
       const int slot = st % kLsStages;
       if (!__all_sync(0xffffffffu,
                       tc::wait_bar(full(slot), (st / kLsStages) & 1, &s_abort, err)))
         break;
+      LM_TRACE(2, threadIdx.x == 0 && st == 0);
       const int r0 = r_begin + st * C::SR;
       const int rows = min(C::SR, r_end - r0);
+      const bool full_stage = rows == C::SR;
       const uint8_t *cs = ls_smem + slot * C::STAGE;
       const uint16_t *ss = reinterpret_cast<const uint16_t *>(cs + kLsStageCodes);
       const uint16_t *bs = reinterpret_cast<const uint16_t *>(cs + kLsStageCodes + C::SC);
-      constexpr int NV = C::CB / 16;  // 16-byte code vectors of a lane's group
       uint4 wc[C::WR][NV];
       float sv[C::WR], bv[C::WR];
 #pragma unroll
       for (int u = 0; u < C::WR; ++u) {
-        const int lr = (warp * C::WR + u) * C::RPS + rsub;
-        if (lr < rows) {
-          const uint4 *p = reinterpret_cast<const uint4 *>(cs + lr * C::CB * G + C::CB * g);
+        if (full_stage || row0 + u * C::RPS < rows) {
+          const uint4 *p = reinterpret_cast<const uint4 *>(cs + code_off + u * C::RPS * ROW_B);
 #pragma unroll
           for (int v = 0; v < NV; ++v) wc[u][v] = p[v];
-          sv[u] = bf16f(ss[lr * G + g]);
-          bv[u] = bf16f(bs[lr * G + g]);
+          sv[u] = bf16f(ss[sc_off + u * C::RPS * G]);
+          bv[u] = bf16f(bs[sc_off + u * C::RPS * G]);
         } else {
 #pragma unroll
           for (int v = 0; v < NV; ++v) wc[u][v] = make_uint4(0, 0, 0, 0);
@@ -424,26 +497,45 @@ __global__ void __launch_bounds__(kLsThreads, 1)
       // the warp's rows are in registers: hand the stage back before computing
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(empty(slot));
+      float part[C::WR];
 #pragma unroll
       for (int u = 0; u < C::WR; ++u) {
-        float d;
         if constexpr (BITS == 8)
-          d = seg_sum<G>(q8_group_dot_b(wc[u], xg, sv[u], bv[u]));
+          part[u] = q8_group_dot_b(wc[u], xg, sv[u], bv[u]);
         else
-          d = seg_sum<G>(q4_group_dot_b(wc[u][0], wc[u][1], xg, sv[u], bv[u]));
-        const int lr = (warp * C::WR + u) * C::RPS + rsub;
-        if (g == 0 && lr < rows) {
+          part[u] = q4_group_dot_b(wc[u][0], wc[u][1], xg, sv[u], bv[u]);
+      }
+      if constexpr (PAIR) {
+        const bool hi = lane >= 16;
+        float keep = hi ? part[1] : part[0];
+        keep += __shfl_xor_sync(0xffffffffu, hi ? part[0] : part[1], 16);
+        keep = seg_sum<16>(keep);
+        const int lr = row0 + (hi ? 1 : 0);
+        const bool owner = (lane & 15) == 0 && (full_stage || lr < rows);
+        const int row = r0 + lr;
+        if (owner && logits) logits[row] = keep;
+        const float dc = cand(keep);
+        const bool take = owner && better(dc, row, best_v, best_i);
+        best_v = take ? dc : best_v;
+        best_i = take ? row : best_i;
+      } else {
+#pragma unroll
+        for (int u = 0; u < C::WR; ++u) {
+          const float d = seg_sum<G>(part[u]);
+          const int lr = row0 + u * C::RPS;
+          const bool owner = g == 0 && (full_stage || lr < rows);
           const int row = r0 + lr;
-          if (logits) logits[row] = d;
+          if (owner && logits) logits[row] = d;
           const float dc = cand(d);
-          if (better(dc, row, best_v, best_i)) {
-            best_v = dc;
-            best_i = row;
-          }
+          const bool take = owner && better(dc, row, best_v, best_i);
+          best_v = take ? dc : best_v;
+          best_i = take ? row : best_i;
         }
       }
     }
+    LM_TRACE(3, threadIdx.x == 0);
   }
+  if (warp == kLsWarps) asm volatile("griddepcontrol.wait;" ::: "memory");
   if (LSE) {
     // the block's rows have their logits in `logits` (global, just written): every thread
     // folds a strided share of them into its partial, off the streaming loop
@@ -451,7 +543,33 @@ __global__ void __launch_bounds__(kLsThreads, 1)
     if (!s_abort)
       for (int r = r_begin + (int)threadIdx.x; r < r_end; r += kLsThreads) lse_add(lm, ls, __ldcg(logits + r));
   }
+  LM_TRACE(4, threadIdx.x == 0);
   block_argmax_finish<kLsWarps + 1, LSE>(best_v, best_i, token, hdr, part_v, part_i, lm, ls, lo);
+  LM_TRACE(5, threadIdx.x == 0);
+}
+
+// The streaming kernel is launched as a programmatic dependent of the previous kernel on the
+// stream (its weight copies start while that kernel drains; see the kernel).
+template <int G, bool LSE, int BITS>
+static void launch_stream(const LmWsLayout &l, cudaStream_t st, const uint32_t *w,
+                          const uint16_t *s, const uint16_t *b, int N, const uint16_t *x,
+                          float *logits, int32_t *token, int32_t *hdr, float *pv, int32_t *pi,
+                          LseOut lo) {
+  using C = LsCfg<G, BITS>;
+  auto fn = gemv_argmax_stream_kernel<G, LSE, BITS>;
+  // set on every call: cheap, and correct for whichever device is current
+  cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, C::BYTES);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(l.grid);
+  cfg.blockDim = dim3(kLsThreads);
+  cfg.dynamicSmemBytes = C::BYTES;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaLaunchKernelEx(&cfg, fn, w, s, b, N, l.rows_per_block, x, logits, token, hdr, pv, pi, lo);
 }
 
 template <int G, bool LSE>
@@ -465,14 +583,9 @@ static void launch_g(const lily_q4_mat &W, int N, const uint16_t *x, int32_t *to
                                  reinterpret_cast<float *>(base + l.off_partial_s), lse}
                         : LseOut{};
   if constexpr (G >= 8) {
-    using C = LsCfg<G>;
     // the log-sum-exp pass reads the logits back: into the workspace when not requested
     if (LSE && !logits) logits = reinterpret_cast<float *>(base + l.off_logits);
-    // set on every call: cheap, and correct for whichever device is current
-    cudaFuncSetAttribute(gemv_argmax_stream_kernel<G, LSE>,
-                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::BYTES);
-    gemv_argmax_stream_kernel<G, LSE><<<l.grid, kLsThreads, C::BYTES, st>>>(
-        W.w, W.s, W.b, N, l.rows_per_block, x, logits, token, hdr, pv, pi, lo);
+    launch_stream<G, LSE, 4>(l, st, W.w, W.s, W.b, N, x, logits, token, hdr, pv, pi, lo);
   } else {
     gemv_argmax_kernel<G, (G >= 16 ? 8 : 4), LSE><<<l.grid, kLmThreads, 0, st>>>(
         W.w, W.s, W.b, N, x, logits, token, hdr, pv, pi, lo);
@@ -498,17 +611,14 @@ template <int G, bool LSE>
 static void launch_q8_g(const lily_q4_mat &W, int N, const uint16_t *x, int32_t *token,
                         float *logits, void *ws, const LmWsLayout &l, cudaStream_t st, float *lse) {
   char *base = static_cast<char *>(ws);
-  using C = LsCfg<G, 8>;
   const LseOut lo = LSE ? LseOut{reinterpret_cast<float *>(base + l.off_partial_m),
                                  reinterpret_cast<float *>(base + l.off_partial_s), lse}
                         : LseOut{};
   if (LSE && !logits) logits = reinterpret_cast<float *>(base + l.off_logits);
-  cudaFuncSetAttribute(gemv_argmax_stream_kernel<G, LSE, 8>,
-                       cudaFuncAttributeMaxDynamicSharedMemorySize, C::BYTES);
-  gemv_argmax_stream_kernel<G, LSE, 8><<<l.grid, kLsThreads, C::BYTES, st>>>(
-      W.w, W.s, W.b, N, l.rows_per_block, x, logits, token, reinterpret_cast<int32_t *>(base),
-      reinterpret_cast<float *>(base + l.off_partial_v),
-      reinterpret_cast<int32_t *>(base + l.off_partial_i), lo);
+  launch_stream<G, LSE, 8>(l, st, W.w, W.s, W.b, N, x, logits, token,
+                           reinterpret_cast<int32_t *>(base),
+                           reinterpret_cast<float *>(base + l.off_partial_v),
+                           reinterpret_cast<int32_t *>(base + l.off_partial_i), lo);
 }
 
 template <bool LSE>
