@@ -30,6 +30,7 @@ def _run(torch, dev, W, x_bits, with_logits=True):
     ws = q4.new_workspace(q4.lily_q4_gemv_argmax_workspace_bytes(N, K), dev)
     q4.lily_q4_gemv_argmax(dW, xd, tok, logits=lg, ws=ws)
     torch.cuda.synchronize()
+    assert q4.lily_q4_workspace_status(ws) == q4.OK, "a bounded device-side wait timed out"
     return int(tok.item()), (lg.cpu().numpy().astype(np.float64) if with_logits else None)
 
 
@@ -266,3 +267,35 @@ def test_q8_logprobs_full_size(torch_dev):
     _check_lp(a, tok, lg, "full 8-bit LM head")
     b = _run_q8_lp(torch, dev, W, x)
     assert a[0] == b[0] and a[1] == b[1] and np.array_equal(a[2], b[2])
+
+
+def test_back_to_back_calls_share_a_workspace(torch_dev):
+    """Calls enqueued back to back on one stream with one workspace (each a programmatic
+    dependent of the previous one, its weight copies starting while that one drains) alternate
+    two heads; every token matches the oracle, so the packed grid maximum and the block counter
+    are re-armed by each call before the next one folds into them."""
+    torch, dev = torch_dev
+    N, K = 50001, 2048
+    heads = [synth.draw_q4(N, K, 61, h, 0) for h in range(2)]
+    xs, wants = [], []
+    for c in range(4):
+        for attempt in range(20):  # a token row whose top-2 logits are not a near tie
+            x = synth.draw_x(K, (61, c), 0, attempt)
+            tok, lg = orc.lm_head(heads[c % 2], x)
+            top2 = np.sort(lg)[-2:]
+            if top2[1] - top2[0] >= 1e-3:
+                break
+        xs.append(x)
+        wants.append(tok)
+    dWs = [q4.DeviceQ4.upload(W, dev) for W in heads]
+    ws = q4.new_workspace(q4.lily_q4_gemv_argmax_workspace_bytes(N, K), dev)
+    toks = [torch.full((1,), -7, dtype=torch.int32, device=dev) for _ in xs]
+    xds = [q4.to_device(x, dev) for x in xs]
+    st = torch.cuda.Stream(device=dev)
+    with torch.cuda.stream(st):
+        for c in range(len(xs)):
+            q4.lily_q4_gemv_argmax(dWs[c % 2], xds[c], toks[c], ws=ws, stream=st)
+    st.synchronize()
+    assert q4.lily_q4_workspace_status(ws, st) == q4.OK
+    for c in range(len(xs)):
+        assert int(toks[c].item()) == wants[c], f"call {c}"

@@ -36,6 +36,7 @@ def run_decode(torch, dev, dl, x_bits, ws=None):
         ws = q4.new_workspace(q4.lily_q4_moe_workspace_bytes(dl, T), dev)
     q4.lily_q4_moe_decode(dl, xd, y, topk_idx=idx, topk_w=w, ws=ws)
     torch.cuda.synchronize()
+    assert q4.lily_q4_workspace_status(ws) == q4.OK, "a bounded device-side wait timed out"
     return bf16_bits_to_f64(y), idx.cpu().numpy(), w.cpu().numpy()
 
 
