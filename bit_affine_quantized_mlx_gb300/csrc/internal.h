@@ -98,4 +98,23 @@ int launch_moe_prefill(const lily_q4_moe_layer &L, const uint16_t *x, int T, uin
 int sm_count();
 int check_launch();
 
+// Launch `fn` as a programmatic dependent of the previous kernel on `st`: its blocks may be
+// scheduled while that kernel drains, and they wait (griddepcontrol.wait) for its completion
+// before touching anything it wrote or reads.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*fn)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t st, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, fn, args...);
+}
+
 }  // namespace lq4

@@ -28,6 +28,8 @@ constexpr int kLsWarps = 24;                     // compute warps
 constexpr int kLsThreads = (kLsWarps + 1) * 32;  // + the copy warp
 constexpr int kLsStages = 4;
 constexpr int kLsStageCodes = 49152;             // code bytes per stage
+// stage waits suspend the waiting thread (time hint) instead of spinning
+constexpr uint32_t kLsSleepNs = 1000;
 // code bytes of a 64-group: 32 for 4-bit codes, 64 for 8-bit codes
 __host__ __device__ constexpr int ls_rows_per_stage(int G, int bits = 4) {
   return kLsStageCodes / (8 * bits * G);
@@ -414,7 +416,7 @@ __global__ void __launch_bounds__(kLsThreads, 1)
       int st = 0;
       for (; st < nst; ++st) {
         const int slot = st % kLsStages;
-        if (!tc::wait_bar(empty(slot), ((st / kLsStages) & 1) ^ 1, &s_abort, err)) break;
+        if (!tc::wait_bar(empty(slot), ((st / kLsStages) & 1) ^ 1, &s_abort, err, kLsSleepNs)) break;
         const int r0 = r_begin + st * C::SR;
         const int rows = min(C::SR, r_end - r0);
         const uint32_t cb = (uint32_t)rows * (uint32_t)C::CB * G, sb = (uint32_t)rows * 2u * G;
@@ -469,7 +471,7 @@ __global__ void __launch_bounds__(kLsThreads, 1)
     for (int st = 0; st < nst; ++st) {
       const int slot = st % kLsStages;
       if (!__all_sync(0xffffffffu,
-                      tc::wait_bar(full(slot), (st / kLsStages) & 1, &s_abort, err)))
+                      tc::wait_bar(full(slot), (st / kLsStages) & 1, &s_abort, err, kLsSleepNs)))
         break;
       LM_TRACE(2, threadIdx.x == 0 && st == 0);
       const int r0 = r_begin + st * C::SR;

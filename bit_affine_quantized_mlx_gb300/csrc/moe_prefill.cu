@@ -11,8 +11,9 @@
 //                 operands are permuted alike)
 //   router GEMM : logits[T][E] = x Wr^T (+ offsets), bf16 x bf16 -> fp32 on tcgen05
 //   topk        : top-k per token, softmax over the k, shared gate sigmoid(x . g)
-//   scan        : per-expert offsets of the token-sorted pairs, GEMM work lists
-//   perm        : stable bucketing (token order inside an expert)
+//   scan        : per-expert offsets of the expert-sorted pairs, GEMM work lists
+//   place       : bucketing, one thread per selection (atomic cursor per expert; the order
+//                 inside an expert is free, no result depends on it)
 //   gate/up GEMM: per (expert, 128 intermediate rows, <=128 tokens): dequantised Q4
 //                 gate and up tiles x gathered token rows, SwiGLU in the epilogue -> h (bf16)
 //   down GEMM   : per (expert, 128 output rows, <=128 tokens): Q4 down tile x h rows,
@@ -40,7 +41,10 @@
 //   warps 8-   weight producers: Q4 codes prefetched into registers a group of k-blocks
 //              ahead, dequantised (bf16x2 FMA: s*q + b, one rounding) and written with
 //              tcgen05.st straight into tensor memory as the MMA's A operand (row i of the
-//              tile in lane i); the router GEMM's bf16 A tile is cp.async'd to shared memory
+//              tile in lane i); the router GEMM's bf16 A tile is cp.async'd to shared memory.
+//              A row's k-block (32 bytes of codes) is taken by one thread with one 256-bit
+//              load when the weights are 32-byte aligned (every code sector is requested
+//              once), else by two threads with 128-bit loads
 // Stages are handed over with mbarriers; the down and router accumulators are
 // double-buffered in TMEM so the epilogue of one tile overlaps the main loop of the next
 // (gate/up keeps one accumulator pair: its A stages take the other half of TMEM).  Every
@@ -60,8 +64,12 @@ constexpr int kBM = 128;  // weight rows per tile (MMA M)
 constexpr int kBN = 128;  // tokens per tile (MMA N, padded to a multiple of 16)
 constexpr int kMmaWarp = 4;
 constexpr int kBWarp0 = 5, kBThreads = 96;
-constexpr int kAWarp0 = 8;  // weight producers: warps 8.. (256 threads per A matrix)
+constexpr int kAWarp0 = 8;  // weight producers: warps 8.. (128 * RT threads per A matrix)
 constexpr int kHdrItemsGU = 8, kHdrItemsDN = 9;
+// Waiting threads are suspended by the hardware (mbarrier.try_wait with a time hint) instead of
+// spinning, so the warps that wait leave the issue slots to the weight producers, which pace
+// the pipeline; the bounded-wait checks run between suspensions.
+constexpr uint32_t kSleepNs = 1000;
 
 // The router GEMM splits K so that more SMs share its few tiles; the partial logits are
 // summed in a fixed order by the top-k kernel.
@@ -72,22 +80,31 @@ enum { kRouter = 0, kGateUp = 1, kDown = 2 };
 // Tile memory.  The router's A operand (bf16 weights) is copied into shared memory; the
 // dequantised Q4 tiles of the expert GEMMs are written by the producer threads straight into
 // tensor memory (row i in lane i), so shared-memory bandwidth is left to the token tiles.
-// TMEM columns: accumulators first (NACC buffers of ACC_COLS), then SA A stages of 32*NA.
-template <int MODE>
+// TMEM columns: accumulators first (NACC buffers of ACC_COLS), then SA A stages of 32*NA*KS.
+// RT = producer threads per weight row (1: the row's whole k-block, 8 code words; 2: 4 each).
+// KS = k-blocks (64 of K) per pipeline stage: gate/up hands over two k-blocks at a time, so
+// the MMA thread's per-stage waits, fences and commits are paid once per 16 MMAs (measured
+// faster there, slower for down).  A stage's A columns are [matrix][k-block][32]; its B tile
+// is KS 128-byte-swizzled [kBN][64] sub-tiles.
+template <int MODE, int RT = 2>
 struct Cfg {
   static constexpr bool TMEM_A = MODE != kRouter;
   static constexpr int NA = MODE == kGateUp ? 2 : 1;  // A tiles per k-block
-  static constexpr int SA = MODE == kGateUp ? 4 : (MODE == kDown ? 8 : 4);  // A stages
-  static constexpr int SB = TMEM_A ? 8 : 6;                                 // B (token) stages
-  static constexpr int AT = NA * 256;                 // weight-producer threads (4 words each)
-  static constexpr int THREADS = kAWarp0 * 32 + AT;
+  static constexpr int KS = MODE == kGateUp ? 2 : 1;  // k-blocks per stage
+  static constexpr int SA = MODE == kGateUp ? 2 : (MODE == kDown ? 8 : 4);  // A stages
+  static constexpr int SB = MODE == kGateUp ? 4 : (MODE == kDown ? 8 : 6);  // B (token) stages
+  static constexpr int AT = NA * kBM * RT;            // weight-producer threads
+  static constexpr int XB = 0;                        // gather warps after the producers
+  static constexpr int BT = kBThreads + 32 * XB;      // token-row gather threads
+  static constexpr int THREADS = kAWarp0 * 32 + AT + 32 * XB;
   static constexpr int A_BYTES = kBM * 128;
-  static constexpr int B_BYTES = kBN * 128;
+  static constexpr int B_SUB = kBN * 128;              // one k-block of a B stage
+  static constexpr int B_BYTES = KS * B_SUB;
   static constexpr int A_STAGE = NA * A_BYTES;        // shared-memory A stage (router)
   static constexpr int ACC_COLS = NA * kBN;
   static constexpr int NACC = MODE == kGateUp ? 1 : 2;  // accumulator buffers
   static constexpr int A_COL0 = NACC * ACC_COLS;        // first TMEM column of the A stages
-  static constexpr int A_COLS = 32 * NA;                // TMEM columns of one A stage
+  static constexpr int A_COLS = 32 * NA * KS;           // TMEM columns of one A stage
   static constexpr int TMEM_COLS = TMEM_A ? A_COL0 + SA * A_COLS : NACC * ACC_COLS;
   static constexpr int OFF_B = TMEM_A ? 0 : SA * A_STAGE;
   // epilogue staging of one bf16 output tile [kBN tokens][kBM rows] (expert GEMMs)
@@ -201,9 +218,20 @@ struct ScaleVec {
   }
 };
 
-template <int MODE, int KG>
-__global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) grouped_gemm_kernel(const GemmArgs a) {
-  using C = Cfg<MODE>;
+// The code words of one row's k-block that a producer thread takes: NV 16-byte vectors
+// (NV = 2: the whole 32-byte k-block in one 256-bit load; the address is 32-byte aligned).
+template <int NV>
+__device__ __forceinline__ void ld_codes(const uint32_t *p, uint4 (&r)[NV]) {
+  if constexpr (NV == 2)
+    ld_stream32(p, r[0], r[1]);
+  else
+    r[0] = ld_stream(p);
+}
+
+template <int MODE, int KG, int RT>
+__global__ void __launch_bounds__(Cfg<MODE, RT>::THREADS, 1) grouped_gemm_kernel(const GemmArgs a) {
+  using C = Cfg<MODE, RT>;
+  static_assert(MODE != kRouter || RT == 2, "the router's A copy takes two threads a row");
   extern __shared__ uint8_t smem_dyn[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(((uintptr_t)smem_dyn + 1023) & ~(uintptr_t)1023);
   const uint32_t sbase = tc::smem_u32(smem);
@@ -220,13 +248,7 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) grouped_gemm_kernel(con
   __shared__ volatile int s_abort;
   __shared__ int4 s_items[MODE == kRouter ? 1 : kSmemItems];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int n_items = MODE == kRouter ? a.n_items_static : *(volatile const int32_t *)a.n_items_ptr;
-  if (MODE != kRouter) {
-    for (int i = threadIdx.x; i < kSmemItems; i += C::THREADS) {
-      const int it = (int)blockIdx.x + i * (int)gridDim.x;
-      if (it < n_items) s_items[i] = a.items[it];
-    }
-  }
+  pdl_allow_next();
   const int G = a.K / 64;  // groups per row
   const int nkb = MODE == kRouter ? G / a.ksplit : G;  // k-blocks per item
 
@@ -237,7 +259,7 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) grouped_gemm_kernel(con
       tc::mbar_init(aempty(s), 1);
     }
     for (int s = 0; s < C::SB; ++s) {
-      tc::mbar_init(bfull(s), kBThreads);
+      tc::mbar_init(bfull(s), C::BT);
       tc::mbar_init(bempty(s), 1);
     }
     for (int b = 0; b < 2; ++b) {
@@ -250,6 +272,16 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) grouped_gemm_kernel(con
   if (warp == kMmaWarp) {
     tc::tmem_alloc(tc::smem_u32(&s_taddr), C::TMEM_COLS);
     tc::tmem_relinquish();
+  }
+  // Set-up above overlaps the previous kernel's tail; the work list (and every operand) is
+  // read only after that kernel has completed.
+  pdl_wait_prev();
+  const int n_items = MODE == kRouter ? a.n_items_static : *(volatile const int32_t *)a.n_items_ptr;
+  if (MODE != kRouter) {
+    for (int i = threadIdx.x; i < kSmemItems; i += C::THREADS) {
+      const int it = (int)blockIdx.x + i * (int)gridDim.x;
+      if (it < n_items) s_items[i] = a.items[it];
+    }
   }
   tc::tc_fence_before();
   __syncthreads();
@@ -274,7 +306,7 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) grouped_gemm_kernel(con
       }
       // all four warps take the same decision, so the epilogue's own barriers never wait for
       // a warp that left
-      if (epilogue_any(!tc::wait_bar(accf_bar(b), (j / C::NACC) & 1, &s_abort, err))) break;
+      if (epilogue_any(!tc::wait_bar(accf_bar(b), (j / C::NACC) & 1, &s_abort, err, kSleepNs))) break;
       tc::tc_fence_after();
       const int ntok = item.z, npad = (ntok + 15) & ~15;
       const int m = item.w * kBM + r;
@@ -341,16 +373,16 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) grouped_gemm_kernel(con
       const int4 item = get_item<MODE>(a, it, s_items);
       const int b = j % C::NACC;
       if (!__all_sync(0xffffffffu,
-                      tc::wait_bar(acce_bar(b), ((j / C::NACC) & 1) ^ 1, &s_abort, err)))
+                      tc::wait_bar(acce_bar(b), ((j / C::NACC) & 1) ^ 1, &s_abort, err, kSleepNs)))
         break;
       tc::tc_fence_after();
       const int npad = (item.z + 15) & ~15;
       const uint32_t idesc = tc::idesc_bf16_f32(kBM, npad);
       const uint32_t d0 = taddr + (uint32_t)(b * C::ACC_COLS);
-      const int nk = item_nkb<MODE>(a, item, nkb);
-      for (int kb = 0; kb < nk; ++kb) {
-        if (!__all_sync(0xffffffffu, tc::wait_bar(afull(sa), pa, &s_abort, err) &&
-                                         tc::wait_bar(bfull(sb), pb, &s_abort, err))) {
+      const int nk = item_nkb<MODE>(a, item, nkb);  // a multiple of KS
+      for (int kb = 0; kb < nk; kb += C::KS) {
+        if (!__all_sync(0xffffffffu, tc::wait_bar(afull(sa), pa, &s_abort, err, kSleepNs) &&
+                                         tc::wait_bar(bfull(sb), pb, &s_abort, err, kSleepNs))) {
           ok = false;
           break;
         }
@@ -359,13 +391,17 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) grouped_gemm_kernel(con
         const uint32_t sB = sbase + C::OFF_B + sb * C::B_BYTES;
         if constexpr (C::TMEM_A) {
           // A stage in TMEM: 8 columns (16 bf16 of K) per MMA
-          const uint32_t tA = taddr + (uint32_t)(C::A_COL0 + sa * C::A_COLS);
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            const uint64_t bd = tc::desc_k128_sw128(sB + 32 * kk);
-            const uint32_t acc = (kb | kk) ? 1u : 0u;
-            tc::mma_bf16_ts_warp(d0, tA + 8 * kk, bd, idesc, acc);
-            if (MODE == kGateUp) tc::mma_bf16_ts_warp(d0 + kBN, tA + 32 + 8 * kk, bd, idesc, acc);
+          for (int ks = 0; ks < C::KS; ++ks) {
+            const uint32_t tA = taddr + (uint32_t)(C::A_COL0 + sa * C::A_COLS + 32 * ks);
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+              const uint64_t bd = tc::desc_k128_sw128(sB + ks * C::B_SUB + 32 * kk);
+              const uint32_t acc = (kb | ks | kk) ? 1u : 0u;
+              tc::mma_bf16_ts_warp(d0, tA + 8 * kk, bd, idesc, acc);
+              if (MODE == kGateUp)
+                tc::mma_bf16_ts_warp(d0 + kBN, tA + 32 * C::KS + 8 * kk, bd, idesc, acc);
+            }
           }
         } else {
           const uint32_t sA = sbase + sa * C::A_STAGE;
@@ -386,12 +422,13 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) grouped_gemm_kernel(con
     }
     // drain: all issued MMAs complete before TMEM is released
     tc::mma_commit_warp(done_bar);
-    tc::wait_bar(done_bar, 0, &s_abort, err);
+    tc::wait_bar(done_bar, 0, &s_abort, err, kSleepNs);
     __syncwarp();
-  } else if (warp >= kBWarp0 && warp < kAWarp0) {
+  } else if ((warp >= kBWarp0 && warp < kAWarp0) || warp >= kAWarp0 + C::AT / 32) {
     // ------------------------------------------------------------------ token-row gather
-    constexpr int QB = (kBN * 8 + kBThreads - 1) / kBThreads;  // 16-byte chunks per thread
-    const int tb = threadIdx.x - kBWarp0 * 32;
+    constexpr int QB = (kBN * 8 + C::BT - 1) / C::BT;  // 16-byte chunks per thread
+    const int tb = warp < kAWarp0 ? (int)threadIdx.x - kBWarp0 * 32
+                                  : kBThreads + (int)threadIdx.x - (kAWarp0 * 32 + C::AT);
     int sb = 0;
     uint32_t pb = 0;
     bool ok = true;
@@ -403,7 +440,7 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) grouped_gemm_kernel(con
       uint32_t dsto[QB], nbytes[QB];
 #pragma unroll
       for (int i = 0; i < QB; ++i) {
-        const int q = tb + i * kBThreads;
+        const int q = tb + i * C::BT;
         const int n = q >> 3, c = q & 7;
         srcp[i] = a.b_src;
         nbytes[i] = 0;
@@ -415,17 +452,20 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) grouped_gemm_kernel(con
         dsto[i] = tc::sw128((uint32_t)n, (uint32_t)c);
       }
       const int nk = item_nkb<MODE>(a, item, nkb);
-      for (int kb = 0; kb < nk; ++kb) {
-        if (!tc::wait_bar(bempty(sb), pb ^ 1, &s_abort, err)) {
+      for (int kb = 0; kb < nk; kb += C::KS) {
+        if (!tc::wait_bar(bempty(sb), pb ^ 1, &s_abort, err, kSleepNs)) {
           ok = false;
           break;
         }
-        const uint32_t sB = sbase + C::OFF_B + sb * C::B_BYTES;
-        const int kbs = kb < nkb ? kb : kb - nkb;  // a doubled K reads the rows twice
 #pragma unroll
-        for (int i = 0; i < QB; ++i)
-          if (tb + i * kBThreads < nchunk)
-            tc::cp_async16(sB + dsto[i], srcp[i] + (nbytes[i] ? kbs * 64 : 0), nbytes[i]);
+        for (int ks = 0; ks < C::KS; ++ks) {
+          const uint32_t sB = sbase + C::OFF_B + sb * C::B_BYTES + ks * C::B_SUB;
+          const int kbs = kb + ks < nkb ? kb + ks : kb + ks - nkb;  // a doubled K reads the rows twice
+#pragma unroll
+          for (int i = 0; i < QB; ++i)
+            if (tb + i * C::BT < nchunk)
+              tc::cp_async16(sB + dsto[i], srcp[i] + (nbytes[i] ? kbs * 64 : 0), nbytes[i]);
+        }
         tc::cp_async_arrive_noinc(bfull(sb));
         if (++sb == C::SB) { sb = 0; pb ^= 1; }
       }
@@ -436,8 +476,8 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) grouped_gemm_kernel(con
     const int ta = threadIdx.x - kAWarp0 * 32;  // 0 .. C::AT-1
     const int row = ta & (kBM - 1);
     const int sub = ta >> 7;
-    const int mat = C::NA == 2 ? sub >> 1 : 0;  // GateUp: gate or up
-    const int half = sub & 1;                   // which half of the row's k-block
+    const int mat = C::NA == 2 ? (RT == 2 ? sub >> 1 : sub) : 0;  // GateUp: gate or up
+    const int half = RT == 2 ? (sub & 1) : 0;  // which half of the row's k-block (RT = 2)
     int sa = 0;
     uint32_t pa = 0;
     bool ok = true;
@@ -447,7 +487,7 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) grouped_gemm_kernel(con
         const int m = item.w * kBM + row;
         const bool valid = m < a.a_rows;
         for (int kb = 0; kb < nkb; ++kb) {
-          if (!tc::wait_bar(aempty(sa), pa ^ 1, &s_abort, err)) {
+          if (!tc::wait_bar(aempty(sa), pa ^ 1, &s_abort, err, kSleepNs)) {
             ok = false;
             break;
           }
@@ -468,11 +508,13 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) grouped_gemm_kernel(con
       // Codes of the next group of KG k-blocks are loaded into registers while the current
       // group is dequantised (prefetch distance KG k-blocks); per-item addressing is done
       // once per item.
-      constexpr int NV = 1;  // one 16-byte code vector (4 words) per thread per k-block
+      constexpr int NV = 2 / RT;  // 16-byte code vectors (4 words) per thread per k-block
       const int woff = 4 * half;
       // this thread's 16 TMEM columns of an A stage: lane = row (warp w writes lanes
       // 32*(w%4) .. +31, which is where its rows fall), columns mat*32 + half*16 ..
-      const uint32_t t_off = ((uint32_t)(warp & 3) << 21) + (uint32_t)(C::A_COL0 + mat * 32 + half * 16);
+      const uint32_t t_off =
+          ((uint32_t)(warp & 3) << 21) + (uint32_t)(C::A_COL0 + mat * 32 * C::KS + half * 16);
+      static_assert(KG % C::KS == 0, "register groups hold whole stages");
       struct Src {
         const uint32_t *w;
         const uint16_t *s, *b;
@@ -503,9 +545,7 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) grouped_gemm_kernel(con
         cur = item_src(c_it);
         if (cur.valid) {
 #pragma unroll
-          for (int i = 0; i < KG; ++i)
-#pragma unroll
-            for (int v = 0; v < NV; ++v) raw[i][v] = ld_stream(cur.w + i * 8 + 4 * v);
+          for (int i = 0; i < KG; ++i) ld_codes<NV>(cur.w + i * 8, raw[i]);
           sc.load(cur.s);
           bc.load(cur.b);
         }
@@ -540,35 +580,37 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) grouped_gemm_kernel(con
 #pragma unroll
             for (int q = 0; q < NV * 4; ++q) outv[q] = make_uint4(0, 0, 0, 0);
           }
-          if (have_next) {
-#pragma unroll
-            for (int v = 0; v < NV; ++v)
-              raw[i][v] = ld_stream(nxt.w + (n_grp * KG + i) * 8 + 4 * v);
-          }
+          if (have_next) ld_codes<NV>(nxt.w + (n_grp * KG + i) * 8, raw[i]);
           // The decision to go on is warp-uniform, so the warp-wide hand-over below never
-          // waits for a lane that left.
-          if (!__all_sync(0xffffffffu, tc::wait_bar(aempty(sa), pa ^ 1, &s_abort, err))) {
-            ok = false;
-            break;
+          // waits for a lane that left.  A stage is claimed at its first k-block.
+          const int ks = i % C::KS;
+          if (ks == 0) {
+            if (!__all_sync(0xffffffffu, tc::wait_bar(aempty(sa), pa ^ 1, &s_abort, err, kSleepNs))) {
+              ok = false;
+              break;
+            }
+            tc::tc_fence_after();
           }
-          tc::tc_fence_after();
           {
-            uint32_t r[16];
+            uint32_t r[16 * NV];
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
+            for (int q = 0; q < 4 * NV; ++q) {
               r[4 * q + 0] = outv[q].x;
               r[4 * q + 1] = outv[q].y;
               r[4 * q + 2] = outv[q].z;
               r[4 * q + 3] = outv[q].w;
             }
-            tc::tmem_st16(taddr + t_off + (uint32_t)(sa * C::A_COLS), r);
+            tc::tmem_st(taddr + t_off + (uint32_t)(sa * C::A_COLS + 32 * ks), r);
           }
           // The stores are complete (tcgen05.wait::st); one arrival per warp (the barrier
-          // expects one per producer warp) after the warp has converged.
-          tc::tc_fence_before();
-          __syncwarp();
-          if (lane == 0) tc::mbar_arrive(afull(sa));
-          if (++sa == C::SA) { sa = 0; pa ^= 1; }
+          // expects one per producer warp) after the warp has converged, once the stage's
+          // last k-block is in.
+          if (ks == C::KS - 1) {
+            tc::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(afull(sa));
+            if (++sa == C::SA) { sa = 0; pa ^= 1; }
+          }
         }
         c_it = n_it;
         c_grp = n_grp;
@@ -595,6 +637,7 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) grouped_gemm_kernel(con
 // kernel accumulates (the workspace layout depends on T, so nothing is assumed about them).
 __global__ void x_perm_kernel(const uint4 *__restrict__ x, uint4 *__restrict__ xp, int nchunks,
                               int32_t *__restrict__ counts, int ncounts) {
+  pdl_enter();
   for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < ncounts; i += gridDim.x * blockDim.x)
     counts[i] = 0;
   for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < nchunks; i += gridDim.x * blockDim.x) {
@@ -628,6 +671,7 @@ struct TopkArgs {
 // (logit desc, index asc); softmax over the k; shared gate sigmoid(x . g).
 template <int EC>
 __global__ void __launch_bounds__(256) topk_prefill_kernel(TopkArgs a) {
+  pdl_enter();
   const int lane = threadIdx.x & 31;
   const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
   if (t >= a.T) return;
@@ -723,6 +767,7 @@ struct ScanArgs {
 
 // Single block: per-expert offsets and the GEMM work lists.
 __global__ void __launch_bounds__(1024) scan_items_kernel(ScanArgs a) {
+  pdl_enter();
   __shared__ int s_cnt[1025];
   __shared__ int s_off[1026];
   __shared__ int s_nt[1025];
@@ -787,95 +832,63 @@ struct PermArgs {
   const float *p;
   const float *sigma;
   const int32_t *offsets;
+  int32_t *counts;  // per-expert selection counts; used up as cursors (left at zero)
   int32_t *perm;
   float *pw;
   int32_t *inv;
-  int T, E, k;
+  int T, E, k, has_shared;
 };
 
-// Block e: the pairs choosing expert e, in token order (stable bucketing).  Each of the
-// 32 warps owns a contiguous slice of the (token, slot) entries: it counts its matches with
-// ballots, the warps' counts are scanned, then each warp places its matches in order.
-constexpr int kPermThreads = 1024;
-constexpr int kPermStaged = 48 * 1024;  // selections staged in shared memory, at most
-__global__ void __launch_bounds__(kPermThreads) perm_kernel(PermArgs a) {
-  const int e = blockIdx.x;
-  const int kk = a.k + 1;
-  if (e == a.E) {  // shared expert: every token, in order
-    for (int t = threadIdx.x; t < a.T; t += blockDim.x) {
+// Pair rows: one thread per selection (t, i) takes a row of its expert's range from an atomic
+// cursor on the expert's count; then the shared expert's rows, every token in order.  The
+// order of an expert's pairs is therefore not fixed, and no result depends on it: every
+// output element of the expert GEMMs is one dot product of a weight row with one pair's
+// token (or h) row, accumulated in a fixed k-block order, and combine sums a token's slots
+// in slot order.
+__global__ void place_kernel(PermArgs a) {
+  pdl_enter();
+  const int n = a.T * a.k, kk = a.k + 1;
+  const int total = n + (a.has_shared ? a.T : 0);
+  for (int j = blockIdx.x * blockDim.x + threadIdx.x; j < total; j += gridDim.x * blockDim.x) {
+    if (j < n) {
+      const int e = a.idx[j];
+      const int t = j / a.k, i = j - t * a.k;
+      const int pos = a.offsets[e] + atomicSub(a.counts + e, 1) - 1;
+      a.perm[pos] = t;
+      a.pw[pos] = a.p[j];
+      a.inv[t * kk + i] = pos;
+    } else {
+      const int t = j - n;
       const int pos = a.offsets[a.E] + t;
       a.perm[pos] = t;
       a.pw[pos] = a.sigma[t];
       a.inv[t * kk + a.k] = pos;
     }
-    return;
-  }
-  __shared__ int s_cnt[32];
-  extern __shared__ int s_idx[];  // the whole [T][k] selection, staged once when it fits
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int n = a.T * a.k;
-  const bool staged = n <= kPermStaged;
-  if (staged) {
-    // eight loads in flight per thread before any store
-    for (int j0 = threadIdx.x; j0 < n; j0 += kPermThreads * 8) {
-      int v[8];
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const int j = j0 + u * kPermThreads;
-        v[u] = j < n ? __ldg(a.idx + j) : 0;
-      }
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const int j = j0 + u * kPermThreads;
-        if (j < n) s_idx[j] = v[u];
-      }
-    }
-    __syncthreads();
-  }
-  const int32_t *idx = staged ? s_idx : a.idx;
-  const int slice = ((n + 31) / 32 + 31) & ~31;  // entries per warp, a multiple of 32
-  const int lo = warp * slice, hi = min(n, lo + slice);
-  int cnt = 0;
-  for (int j0 = lo; j0 < hi; j0 += 32) {
-    const int j = j0 + lane;
-    cnt += __popc(__ballot_sync(0xffffffffu, j < hi && idx[j] == e));
-  }
-  if (lane == 0) s_cnt[warp] = cnt;
-  __syncthreads();
-  if (warp == 0) {
-    int tot;
-    const int ex = warp_excl_scan(s_cnt[lane], &tot);
-    __syncwarp();
-    s_cnt[lane] = ex;
-  }
-  __syncthreads();
-  int pos0 = a.offsets[e] + s_cnt[warp];
-  for (int j0 = lo; j0 < hi; j0 += 32) {
-    const int j = j0 + lane;
-    const bool f = j < hi && idx[j] == e;
-    const unsigned bal = __ballot_sync(0xffffffffu, f);
-    if (f) {
-      const int pos = pos0 + __popc(bal & ((1u << lane) - 1));
-      const int t = j / a.k, i = j % a.k;
-      a.perm[pos] = t;
-      a.pw[pos] = a.p[j];
-      a.inv[t * kk + i] = pos;
-    }
-    pos0 += __popc(bal);
   }
 }
 
-// y[t][8c..8c+7] = sum over t's slots of o[inv[t][slot]] (fixed slot order).
+// y[t][8c..8c+7] = sum over t's slots of o[inv[t][slot]] (fixed slot order).  All of a
+// chunk's slot rows are requested before any is summed (NS >= the slot count).
+template <int NS>
 __global__ void combine_kernel(const uint16_t *__restrict__ o, const int32_t *__restrict__ inv,
                                uint16_t *__restrict__ y, int T, int H, int nslots, int kk) {
+  pdl_enter();
   const int cpr = H / 8;
   for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < T * cpr; i += gridDim.x * blockDim.x) {
     const int t = i / cpr, c = i % cpr;
+    int pos[NS];
+#pragma unroll
+    for (int s = 0; s < NS; ++s) pos[s] = s < nslots ? __ldg(inv + t * kk + s) : 0;
+    uint4 v[NS];
+#pragma unroll
+    for (int s = 0; s < NS; ++s)
+      v[s] = s < nslots ? __ldcg(reinterpret_cast<const uint4 *>(o + (size_t)pos[s] * H) + c)
+                        : make_uint4(0, 0, 0, 0);
     float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-    for (int s = 0; s < nslots; ++s) {
-      const int pos = __ldg(inv + t * kk + s);
-      const uint4 v = __ldcg(reinterpret_cast<const uint4 *>(o + (size_t)pos * H) + c);
-      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int s = 0; s < NS; ++s) {
+      if (s >= nslots) break;
+      const uint32_t w[4] = {v[s].x, v[s].y, v[s].z, v[s].w};
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         acc[2 * q] += __uint_as_float(w[q] << 16);
@@ -899,6 +912,7 @@ __global__ void combine_kernel(const uint16_t *__restrict__ o, const int32_t *__
 // s*q (bf16 s times a byte code) has at most 16 significant bits, so hi = bf16(s*q) and
 // lo = s*q - hi are both exact in bf16.
 __global__ void router8_prep_a_kernel(lily_q4_mat r8, int E, int H, int Kr, uint16_t *__restrict__ A) {
+  pdl_enter();
   const int e = blockIdx.x;
   if (e >= E) return;
   const int G = H / 64;
@@ -918,6 +932,7 @@ __global__ void router8_prep_a_kernel(lily_q4_mat r8, int E, int H, int Kr, uint
 // X_g = the sum of group g of x (fp32, a fixed order), split exactly into three bf16 parts,
 // so A . B = sum_k (s*q)_k x_k + sum_g b_g X_g with every product exact.
 __global__ void router8_prep_b_kernel(const uint16_t *__restrict__ x, int H, int Kr, uint16_t *__restrict__ B) {
+  pdl_enter();
   const int t = blockIdx.x;
   const int G = H / 64;
   const uint16_t *xr = x + (size_t)t * H;
@@ -956,6 +971,7 @@ struct Q8ToQ4x2 {
   uint16_t *b;
 };
 __global__ void q8_to_q4x2_kernel(Q8ToQ4x2 a) {
+  pdl_enter();
   const int words = a.K / 8, G = a.K / 64;
   const size_t nw = (size_t)a.N * words, ng = (size_t)a.N * G;
   for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < nw + ng;
@@ -1023,7 +1039,9 @@ static int q8_to_q4x2(const lily_q4_mat &src, int N, int K, const lily_q4_mat &d
   const size_t n = (size_t)N * (K / 8) + (size_t)N * (K / 64);
   const int sms = sm_count() > 0 ? sm_count() : 1;
   const size_t want = (n + 255) / 256;
-  q8_to_q4x2_kernel<<<(int)(want < (size_t)4 * sms ? want : (size_t)4 * sms), 256, 0, st>>>(a);
+  if (launch_pdl(q8_to_q4x2_kernel, dim3((unsigned)(want < (size_t)4 * sms ? want : (size_t)4 * sms)),
+                 dim3(256), 0, st, a) != cudaSuccess)
+    return LILY_Q4_ERR_CUDA;
   return check_launch();
 }
 
@@ -1079,24 +1097,43 @@ PrefillWsLayout prefill_ws_layout(const lily_q4_moe_layer &L, int T) {
   return l;
 }
 
-template <int MODE, int KG>
+template <int MODE, int KG, int RT = 2>
 static int launch_gemm_kg(const GemmArgs &a, int grid, cudaStream_t st) {
-  const int bytes = Cfg<MODE>::BYTES;
+  const int bytes = Cfg<MODE, RT>::BYTES;
   // set on every call: cheap, and correct for whichever device is current
-  if (cudaFuncSetAttribute(grouped_gemm_kernel<MODE, KG>,
+  if (cudaFuncSetAttribute(grouped_gemm_kernel<MODE, KG, RT>,
                            cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess)
     return LILY_Q4_ERR_CUDA;
-  grouped_gemm_kernel<MODE, KG><<<grid, Cfg<MODE>::THREADS, bytes, st>>>(a);
+  if (launch_pdl(grouped_gemm_kernel<MODE, KG, RT>, dim3(grid), dim3(Cfg<MODE, RT>::THREADS),
+                 (size_t)bytes, st, a) != cudaSuccess)
+    return LILY_Q4_ERR_CUDA;
   return check_launch();
 }
 
-// KG = k-blocks per register group of the weight producers: min(8, K/64).
+static bool aligned32(const void *p) { return ((uintptr_t)p & 31) == 0; }
+
+// KG = k-blocks per register group of the weight producers (K/64 is a power of two >= 2):
+// 8 for down; 4 for gate/up, whose producers hold both matrices' rows (a group of 8 k-blocks
+// there does not fit the register budget).  Gate/up takes one producer thread per row when
+// all four of its code arrays are 32-byte aligned (row and expert strides are multiples of
+// 32 bytes, so every row's k-block is then too).
 template <int MODE>
 static int launch_gemm(const GemmArgs &a, int grid, cudaStream_t st) {
   const int G = a.K / 64;
-  if (MODE == kRouter || G >= 8) return launch_gemm_kg<MODE, 8>(a, grid, st);
-  if (G == 4) return launch_gemm_kg<MODE, 4>(a, grid, st);
-  return launch_gemm_kg<MODE, 2>(a, grid, st);
+  if constexpr (MODE == kRouter) {
+    return launch_gemm_kg<MODE, 8>(a, grid, st);
+  } else if constexpr (MODE == kGateUp) {
+    if (G >= 4) {
+      const bool al = aligned32(a.a0.w) && aligned32(a.a1.w) &&
+                      (!a.sh0.w || (aligned32(a.sh0.w) && aligned32(a.sh1.w)));
+      return al ? launch_gemm_kg<MODE, 4, 1>(a, grid, st) : launch_gemm_kg<MODE, 4, 2>(a, grid, st);
+    }
+    return launch_gemm_kg<MODE, 2>(a, grid, st);
+  } else {
+    if (G >= 8) return launch_gemm_kg<MODE, 8>(a, grid, st);
+    if (G == 4) return launch_gemm_kg<MODE, 4>(a, grid, st);
+    return launch_gemm_kg<MODE, 2>(a, grid, st);
+  }
 }
 
 int launch_moe_prefill(const lily_q4_moe_layer &L, const uint16_t *x, int T, uint16_t *y,
@@ -1126,17 +1163,25 @@ int launch_moe_prefill(const lily_q4_moe_layer &L, const uint16_t *x, int T, uin
   int4 *items_gu = items;
   int4 *items_dn = items + (size_t)tiles * mt_gu;
 
+  // Every launch below is a programmatic dependent of the one before it (launch_pdl): set-up
+  // overlaps the previous kernel's tail, and each kernel waits for that kernel's completion
+  // before it reads or writes anything the chain shares.
   const int nch = T * H / 8;
-  x_perm_kernel<<<(nch + 255) / 256 < 4 * sms ? (nch + 255) / 256 : 4 * sms, 256, 0, st>>>(
-      reinterpret_cast<const uint4 *>(x), reinterpret_cast<uint4 *>(xperm), nch, counts, E);
+  if (launch_pdl(x_perm_kernel, dim3((nch + 255) / 256 < 4 * sms ? (nch + 255) / 256 : 4 * sms),
+                 dim3(256), 0, st, reinterpret_cast<const uint4 *>(x), reinterpret_cast<uint4 *>(xperm),
+                 nch, counts, E) != cudaSuccess)
+    return LILY_Q4_ERR_CUDA;
 
   // router GEMM (an 8-bit router in its exact bf16 form, the token rows widened to match)
   const uint16_t *ra_a = L.router, *ra_b = x;
   if (router8(L)) {
     uint16_t *A = reinterpret_cast<uint16_t *>(b + l.off_r8a);
     uint16_t *B = reinterpret_cast<uint16_t *>(b + l.off_r8b);
-    router8_prep_a_kernel<<<E, 256, 0, st>>>(L.router_q8, E, H, l.Kr, A);
-    router8_prep_b_kernel<<<T, 256, 0, st>>>(x, H, l.Kr, B);
+    if (launch_pdl(router8_prep_a_kernel, dim3(E), dim3(256), 0, st, L.router_q8, E, H, l.Kr, A) !=
+            cudaSuccess ||
+        launch_pdl(router8_prep_b_kernel, dim3(T), dim3(256), 0, st, static_cast<const uint16_t *>(x),
+                   H, l.Kr, B) != cudaSuccess)
+      return LILY_Q4_ERR_CUDA;
     ra_a = A;
     ra_b = B;
   }
@@ -1158,23 +1203,20 @@ int launch_moe_prefill(const lily_q4_moe_layer &L, const uint16_t *x, int T, uin
 
   TopkArgs ta{logits, L.router_bias, ra.ksplit, x, L.shared_gate, T, E, H, k, L.has_shared,
               idx, p, sigma, counts, topk_idx, topk_w};
-  if (E <= 256)
-    topk_prefill_kernel<8><<<(T + 7) / 8, 256, 0, st>>>(ta);
-  else if (E <= 512)
-    topk_prefill_kernel<16><<<(T + 7) / 8, 256, 0, st>>>(ta);
-  else
-    topk_prefill_kernel<32><<<(T + 7) / 8, 256, 0, st>>>(ta);
+  const dim3 tk_grid((T + 7) / 8), tk_block(256);
+  cudaError_t ce = E <= 256   ? launch_pdl(topk_prefill_kernel<8>, tk_grid, tk_block, 0, st, ta)
+                   : E <= 512 ? launch_pdl(topk_prefill_kernel<16>, tk_grid, tk_block, 0, st, ta)
+                              : launch_pdl(topk_prefill_kernel<32>, tk_grid, tk_block, 0, st, ta);
+  if (ce != cudaSuccess) return LILY_Q4_ERR_CUDA;
 
   ScanArgs sa{counts, offsets, items_gu, items_dn, hdr, T, E, k, L.has_shared, mt_gu, mt_dn};
-  scan_items_kernel<<<1, 1024, 0, st>>>(sa);
-
-  PermArgs pa{idx, p, sigma, offsets, perm, pw, inv, T, E, k};
-  const int nsel = T * k;
-  const size_t perm_smem = nsel <= kPermStaged ? (size_t)nsel * sizeof(int32_t) : 0;
-  if (cudaFuncSetAttribute(perm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           kPermStaged * (int)sizeof(int32_t)) != cudaSuccess)
+  if (launch_pdl(scan_items_kernel, dim3(1), dim3(1024), 0, st, sa) != cudaSuccess)
     return LILY_Q4_ERR_CUDA;
-  perm_kernel<<<nexp, kPermThreads, perm_smem, st>>>(pa);
+
+  PermArgs pa{idx, p, sigma, offsets, counts, perm, pw, inv, T, E, k, L.has_shared};
+  const int nplace = T * k + (L.has_shared ? T : 0);
+  if (launch_pdl(place_kernel, dim3((nplace + 255) / 256), dim3(256), 0, st, pa) != cudaSuccess)
+    return LILY_Q4_ERR_CUDA;
 
   // an 8-bit shared expert as 4-bit codes of twice the width (its tiles run with K doubled)
   lily_q4_mat shg = L.sh_gate, shu = L.sh_up, shd = L.sh_down;
@@ -1224,8 +1266,13 @@ int launch_moe_prefill(const lily_q4_moe_layer &L, const uint16_t *x, int T, uin
   if (rc != LILY_Q4_OK) return rc;
 
   const int cch = T * H / 8;
-  combine_kernel<<<(cch + 255) / 256 < 8 * sms ? (cch + 255) / 256 : 8 * sms, 256, 0, st>>>(
-      o, inv, y, T, H, k + L.has_shared, k + 1);
+  const dim3 cb_grid((cch + 255) / 256 < 8 * sms ? (cch + 255) / 256 : 8 * sms), cb_block(256);
+  const int nslots = k + L.has_shared;
+  const uint16_t *oc = o;
+  if ((nslots <= 9 ? launch_pdl(combine_kernel<9>, cb_grid, cb_block, 0, st, oc, inv, y, T, H, nslots, k + 1)
+                   : launch_pdl(combine_kernel<17>, cb_grid, cb_block, 0, st, oc, inv, y, T, H, nslots,
+                                k + 1)) != cudaSuccess)
+    return LILY_Q4_ERR_CUDA;
   return check_launch();
 }
 

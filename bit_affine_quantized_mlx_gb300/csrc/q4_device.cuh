@@ -53,6 +53,27 @@ __device__ __forceinline__ uint4 ld_stream(const void *p) {
   return r;
 }
 
+// Programmatic dependent launch: let the next kernel on the stream be scheduled, and wait
+// until the previous one has completed with its writes visible (a no-op for a kernel that
+// was not launched as a programmatic dependent).
+__device__ __forceinline__ void pdl_allow_next() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait_prev() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_enter() {
+  pdl_allow_next();
+  pdl_wait_prev();
+}
+
+// 32 bytes (one 256-bit load; p 32-byte aligned), streamed like ld_stream.
+__device__ __forceinline__ void ld_stream32(const void *p, uint4 &lo, uint4 &hi) {
+  asm volatile(
+      "ld.global.nc.L1::no_allocate.L2::cache_hint.v8.u32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8], %9;"
+      : "=r"(lo.x), "=r"(lo.y), "=r"(lo.z), "=r"(lo.w), "=r"(hi.x), "=r"(hi.y), "=r"(hi.z),
+        "=r"(hi.w)
+      : "l"(p), "l"(l2_evict_first()));
+}
+
 __device__ __forceinline__ uint16_t ld_u16(const uint16_t *p) {
   uint16_t r;
   asm volatile("ld.global.nc.L2::cache_hint.u16 %0, [%1], %2;" : "=h"(r) : "l"(p), "l"(l2_evict_first()));
