@@ -129,6 +129,7 @@ struct GemmArgs {
   int n_items_static, mt_static, T;
   int ksplit;                    // router: K is split in ksplit parts (partial logits)
   int ksh;                       // the shared expert's K is ksh * K (2: an 8-bit shared expert)
+  int P;                         // pair rows (h is [I/64][P][64], k-block-major)
   uint16_t *h_out;
   uint16_t *o_out;
   int o_ld;                      // H
@@ -259,7 +260,7 @@ __global__ void __launch_bounds__(Cfg<MODE, RT>::THREADS, 1) grouped_gemm_kernel
       tc::mbar_init(aempty(s), 1);
     }
     for (int s = 0; s < C::SB; ++s) {
-      tc::mbar_init(bfull(s), C::BT);
+      tc::mbar_init(bfull(s), MODE == kDown ? 1 : C::BT);
       tc::mbar_init(bempty(s), 1);
     }
     for (int b = 0; b < 2; ++b) {
@@ -296,10 +297,10 @@ __global__ void __launch_bounds__(Cfg<MODE, RT>::THREADS, 1) grouped_gemm_kernel
     for (int it = blockIdx.x; it < n_items; it += gridDim.x, ++j) {
       const int4 item = get_item<MODE>(a, it, s_items);
       const int b = j % C::NACC;
-      // down: the pairs' gate weights of this tile (token n in lane n % 32 of pwv[n / 32]),
+      // gate/up: the pairs' gate weights of this tile (token n in lane n % 32 of pwv[n / 32]),
       // fetched before the accumulator is ready
       float pwv[kBN / 32] = {};
-      if (MODE == kDown) {
+      if (MODE == kGateUp) {
 #pragma unroll
         for (int q = 0; q < kBN / 32; ++q)
           if (lane + 32 * q < item.z) pwv[q] = __ldg(a.pw + item.y + lane + 32 * q);
@@ -323,28 +324,34 @@ __global__ void __launch_bounds__(Cfg<MODE, RT>::THREADS, 1) grouped_gemm_kernel
           if (MODE == kGateUp) {
             float u[16];
             tc::tmem_ld16x2(tcol + c0, d, tcol + kBN + c0, u);
-#pragma unroll
-            for (int i = 0; i < 16; ++i) stg[(c0 + i) * kBM + pos] = f2bf16_rne(silu_mul(d[i], u[i]));
-          } else {
-            tc::tmem_ld16(tcol + c0, d);
             const float pwc = c0 < 32 ? pwv[0] : c0 < 64 ? pwv[1] : c0 < 96 ? pwv[2] : pwv[3];
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
               const float w = __shfl_sync(0xffffffffu, pwc, (c0 & 31) + i);
-              stg[(c0 + i) * kBM + pos] = f2bf16_rne(w * d[i]);
+              stg[(c0 + i) * kBM + pos] = f2bf16_rne(w * silu_mul(d[i], u[i]));
             }
+          } else {
+            tc::tmem_ld16(tcol + c0, d);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) stg[(c0 + i) * kBM + pos] = f2bf16_rne(d[i]);
           }
         }
         tc::tc_fence_before();
         tc::mbar_arrive(acce_bar(b));
         epilogue_sync();  // the whole tile is staged
-        uint16_t *dst = MODE == kGateUp ? a.h_out : a.o_out;
-        const size_t ld = MODE == kGateUp ? (size_t)a.a_rows : (size_t)a.o_ld;
-        const int col0 = item.w * kBM;
         for (int q = r; q < ntok * (kBM / 8); q += 128) {
           const int n = q / (kBM / 8), c = q % (kBM / 8);
-          *reinterpret_cast<uint4 *>(dst + (size_t)(item.y + n) * ld + col0 + 8 * c) =
-              *reinterpret_cast<const uint4 *>(stg + n * kBM + 8 * c);
+          uint16_t *dst;
+          if (MODE == kGateUp) {
+            // h in k-block-major order, [I/64][P][64], each 128-byte row slice with its 16-byte
+            // chunks in the 128-byte-swizzle order of the row's place n in its tile (the down
+            // GEMM's tiles cover the same pair rows), so a down B stage is one bulk copy
+            const int kbg = item.w * (kBM / 64) + (c >> 3);
+            dst = a.h_out + ((size_t)kbg * a.P + item.y + n) * 64 + 8 * ((c & 7) ^ (n & 7));
+          } else {
+            dst = a.o_out + (size_t)(item.y + n) * a.o_ld + item.w * kBM + 8 * c;
+          }
+          *reinterpret_cast<uint4 *>(dst) = *reinterpret_cast<const uint4 *>(stg + n * kBM + 8 * c);
         }
         epilogue_sync();  // the staging buffer is free for the next tile
       } else {
@@ -424,6 +431,39 @@ __global__ void __launch_bounds__(Cfg<MODE, RT>::THREADS, 1) grouped_gemm_kernel
     tc::mma_commit_warp(done_bar);
     tc::wait_bar(done_bar, 0, &s_abort, err, kSleepNs);
     __syncwarp();
+  } else if (MODE == kDown && warp >= kBWarp0 && warp < kAWarp0) {
+    // ------------------------------------------------------------------ h rows (down)
+    // An item's h rows are consecutive pair rows, stored k-block-major and pre-swizzled by the
+    // gate/up epilogue: a B stage is one bulk copy of the item's ntok rows of one k-block
+    // (rows past ntok keep stale data; they only feed accumulator columns that are not stored).
+    if (warp == kBWarp0 && lane == 0) {
+      int sb = 0;
+      uint32_t pb = 0;
+      bool ok = true;
+      long long issued = 0;
+      for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
+        const int4 item = get_item<MODE>(a, it, s_items);
+        const uint32_t bytes = (uint32_t)item.z * 128u;
+        const int nk = item_nkb<MODE>(a, item, nkb);
+        for (int kb = 0; kb < nk; ++kb) {
+          if (!tc::wait_bar(bempty(sb), pb ^ 1, &s_abort, err, kSleepNs)) {
+            ok = false;
+            break;
+          }
+          const int kbs = kb < nkb ? kb : kb - nkb;  // a doubled K reads the rows twice
+          const uint32_t sB = sbase + C::OFF_B + sb * C::B_BYTES;
+          tc::mbar_arrive_expect_tx(bfull(sb), bytes);
+          tc::bulk_g2s(sB, a.b_src + ((size_t)kbs * a.P + item.y) * 64, bytes, bfull(sb));
+          ++issued;
+          if (++sb == C::SB) { sb = 0; pb ^= 1; }
+        }
+      }
+      // No copy may still be landing when the block exits (after an abort the MMA thread
+      // stops consuming): wait, bounded, for the last stages issued.
+      volatile int no_abort = 0;
+      for (long long q = issued - 1; q >= 0 && q >= issued - C::SB; --q)
+        tc::wait_bar(bfull((int)(q % C::SB)), (uint32_t)((q / C::SB) & 1), &no_abort, err, kSleepNs);
+    }
   } else if ((warp >= kBWarp0 && warp < kAWarp0) || warp >= kAWarp0 + C::AT / 32) {
     // ------------------------------------------------------------------ token-row gather
     constexpr int QB = (kBN * 8 + C::BT - 1) / C::BT;  // 16-byte chunks per thread
@@ -667,14 +707,21 @@ struct TopkArgs {
 };
 
 // One warp per token: logits = fixed-order sum of the router GEMM's K-split partials plus
-// the per-expert offsets, held in registers (EC per lane); k rounds of a warp argmax
-// (logit desc, index asc); softmax over the k; shared gate sigmoid(x . g).
+// the per-expert offsets, held in registers (EC per lane); the k largest (logit desc, index
+// asc); softmax over the k; shared gate sigmoid(x . g).  The block's selections are counted
+// per expert in shared memory first and added to the global counts once per (block, expert):
+// a skewed router sends most tokens to the same experts, and one global atomic per selection
+// would serialise on those counters.
+constexpr int kTopkTokens = 16;  // tokens (warps) per block
 template <int EC>
-__global__ void __launch_bounds__(256) topk_prefill_kernel(TopkArgs a) {
+__global__ void __launch_bounds__(32 * kTopkTokens) topk_prefill_kernel(TopkArgs a) {
   pdl_enter();
+  __shared__ int s_cnt[32 * EC];
+  for (int e = threadIdx.x; e < a.E; e += blockDim.x) s_cnt[e] = 0;
+  __syncthreads();
   const int lane = threadIdx.x & 31;
-  const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
-  if (t >= a.T) return;
+  const int t = blockIdx.x * kTopkTokens + (threadIdx.x >> 5);
+  if (t < a.T) {
   // every partial logit of the lane is loaded before any is summed (the split count is at most
   // kRouterSplit(H) = 4), then the partials are summed in split order
   float lv[EC];
@@ -696,27 +743,12 @@ __global__ void __launch_bounds__(256) topk_prefill_kernel(TopkArgs a) {
     }
     lv[j] = v;
   }
-  uint32_t taken = 0;
-  float myv = -INFINITY;  // lane i < k keeps selection i
-  int mye = 0;
-  for (int i = 0; i < a.k; ++i) {
-    float bv = -INFINITY;
-    int be = INT_MAX;
+  uint32_t key[EC];
 #pragma unroll
-    for (int j = 0; j < EC; ++j) {
-      const int e = lane + 32 * j;
-      if (e < a.E && !(taken & (1u << j)) && better(lv[j], e, bv, be)) {
-        bv = lv[j];
-        be = e;
-      }
-    }
-    warp_argmax(bv, be);
-    if ((be & 31) == lane) taken |= 1u << (be >> 5);
-    if (lane == i) {
-      myv = bv;
-      mye = be;
-    }
-  }
+  for (int j = 0; j < EC; ++j) key[j] = lane + 32 * j < a.E ? f2key(lv[j]) : 0u;
+  float myv;  // lane i < k keeps selection i
+  int mye;
+  warp_topk_keys<EC>(key, a.k, mye, myv);
   float sig = 0.f;
   if (a.has_shared) {
     const uint16_t *xt = a.x + (size_t)t * a.H;
@@ -752,9 +784,13 @@ __global__ void __launch_bounds__(256) topk_prefill_kernel(TopkArgs a) {
     a.p[t * a.k + lane] = pi;
     if (a.out_idx) a.out_idx[t * a.k + lane] = mye;
     if (a.out_w) a.out_w[t * a.k + lane] = pi;
-    atomicAdd(a.counts + mye, 1);
+    atomicAdd(s_cnt + mye, 1);
   }
   if (lane == 0) a.sigma[t] = sig;
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < a.E; e += blockDim.x)
+    if (s_cnt[e]) atomicAdd(a.counts + e, s_cnt[e]);
 }
 
 struct ScanArgs {
@@ -839,31 +875,46 @@ struct PermArgs {
   int T, E, k, has_shared;
 };
 
-// Pair rows: one thread per selection (t, i) takes a row of its expert's range from an atomic
-// cursor on the expert's count; then the shared expert's rows, every token in order.  The
-// order of an expert's pairs is therefore not fixed, and no result depends on it: every
-// output element of the expert GEMMs is one dot product of a weight row with one pair's
-// token (or h) row, accumulated in a fixed k-block order, and combine sums a token's slots
-// in slot order.
-__global__ void place_kernel(PermArgs a) {
+// Pair rows: one thread per selection (t, i).  A block ranks its selections per expert in
+// shared memory, reserves one range per (block, expert) from an atomic cursor on the expert's
+// count (counting it down to zero), and each selection takes base + rank; the blocks past the
+// selections write the shared expert's rows, every token in order.  The order of an expert's
+// pairs is therefore not fixed, and no result depends on it: every output element of the
+// expert GEMMs is one dot product of a weight row with one pair's token (or h) row,
+// accumulated in a fixed k-block order, and combine sums a token's slots in slot order.
+constexpr int kPlaceThreads = 256;
+__global__ void __launch_bounds__(kPlaceThreads) place_kernel(PermArgs a) {
   pdl_enter();
+  __shared__ int s_cnt[1024];  // E <= 1024
   const int n = a.T * a.k, kk = a.k + 1;
-  const int total = n + (a.has_shared ? a.T : 0);
-  for (int j = blockIdx.x * blockDim.x + threadIdx.x; j < total; j += gridDim.x * blockDim.x) {
-    if (j < n) {
-      const int e = a.idx[j];
-      const int t = j / a.k, i = j - t * a.k;
-      const int pos = a.offsets[e] + atomicSub(a.counts + e, 1) - 1;
-      a.perm[pos] = t;
-      a.pw[pos] = a.p[j];
-      a.inv[t * kk + i] = pos;
-    } else {
-      const int t = j - n;
+  const int nsel_blocks = (n + kPlaceThreads - 1) / kPlaceThreads;
+  if ((int)blockIdx.x >= nsel_blocks) {  // shared expert
+    const int t = ((int)blockIdx.x - nsel_blocks) * kPlaceThreads + (int)threadIdx.x;
+    if (t < a.T) {
       const int pos = a.offsets[a.E] + t;
       a.perm[pos] = t;
       a.pw[pos] = a.sigma[t];
       a.inv[t * kk + a.k] = pos;
     }
+    return;
+  }
+  for (int e = threadIdx.x; e < a.E; e += blockDim.x) s_cnt[e] = 0;
+  __syncthreads();
+  const int j = blockIdx.x * kPlaceThreads + threadIdx.x;
+  const int e = j < n ? a.idx[j] : 0;
+  const int rank = j < n ? atomicAdd(s_cnt + e, 1) : 0;
+  __syncthreads();
+  for (int q = threadIdx.x; q < a.E; q += blockDim.x) {
+    const int c = s_cnt[q];
+    if (c) s_cnt[q] = atomicSub(a.counts + q, c) - c;  // the block's range: [old - c, old)
+  }
+  __syncthreads();
+  if (j < n) {
+    const int t = j / a.k, i = j - t * a.k;
+    const int pos = a.offsets[e] + s_cnt[e] + rank;
+    a.perm[pos] = t;
+    a.pw[pos] = a.p[j];
+    a.inv[t * kk + i] = pos;
   }
 }
 
@@ -1203,7 +1254,7 @@ int launch_moe_prefill(const lily_q4_moe_layer &L, const uint16_t *x, int T, uin
 
   TopkArgs ta{logits, L.router_bias, ra.ksplit, x, L.shared_gate, T, E, H, k, L.has_shared,
               idx, p, sigma, counts, topk_idx, topk_w};
-  const dim3 tk_grid((T + 7) / 8), tk_block(256);
+  const dim3 tk_grid((T + kTopkTokens - 1) / kTopkTokens), tk_block(32 * kTopkTokens);
   cudaError_t ce = E <= 256   ? launch_pdl(topk_prefill_kernel<8>, tk_grid, tk_block, 0, st, ta)
                    : E <= 512 ? launch_pdl(topk_prefill_kernel<16>, tk_grid, tk_block, 0, st, ta)
                               : launch_pdl(topk_prefill_kernel<32>, tk_grid, tk_block, 0, st, ta);
@@ -1214,8 +1265,9 @@ int launch_moe_prefill(const lily_q4_moe_layer &L, const uint16_t *x, int T, uin
     return LILY_Q4_ERR_CUDA;
 
   PermArgs pa{idx, p, sigma, offsets, counts, perm, pw, inv, T, E, k, L.has_shared};
-  const int nplace = T * k + (L.has_shared ? T : 0);
-  if (launch_pdl(place_kernel, dim3((nplace + 255) / 256), dim3(256), 0, st, pa) != cudaSuccess)
+  const int nplace = (T * k + kPlaceThreads - 1) / kPlaceThreads +
+                     (L.has_shared ? (T + kPlaceThreads - 1) / kPlaceThreads : 0);
+  if (launch_pdl(place_kernel, dim3(nplace), dim3(kPlaceThreads), 0, st, pa) != cudaSuccess)
     return LILY_Q4_ERR_CUDA;
 
   // an 8-bit shared expert as 4-bit codes of twice the width (its tiles run with K doubled)
@@ -1244,6 +1296,8 @@ int launch_moe_prefill(const lily_q4_moe_layer &L, const uint16_t *x, int T, uin
   ga.items = items_gu;
   ga.n_items_ptr = hdr + kHdrItemsGU;
   ga.h_out = h;
+  ga.pw = pw;
+  ga.P = l.P;
   ga.hdr = hdr;
   rc = launch_gemm<kGateUp>(ga, sms, st);
   if (rc != LILY_Q4_OK) return rc;
@@ -1256,11 +1310,11 @@ int launch_moe_prefill(const lily_q4_moe_layer &L, const uint16_t *x, int T, uin
   da.K = I;
   da.E = E;
   da.b_src = h;
+  da.P = l.P;
   da.items = items_dn;
   da.n_items_ptr = hdr + kHdrItemsDN;
   da.o_out = o;
   da.o_ld = H;
-  da.pw = pw;
   da.hdr = hdr;
   rc = launch_gemm<kDown>(da, sms, st);
   if (rc != LILY_Q4_OK) return rc;
