@@ -12,8 +12,8 @@
 //   router GEMM : logits[T][E] = x Wr^T (+ offsets), bf16 x bf16 -> fp32 on tcgen05
 //   topk        : top-k per token, softmax over the k, shared gate sigmoid(x . g)
 //   scan        : per-expert offsets of the expert-sorted pairs, GEMM work lists
-//   place       : bucketing, one thread per selection (atomic cursor per expert; the order
-//                 inside an expert is free, no result depends on it)
+//   place       : stable bucketing (token order inside an expert) from the top-k blocks'
+//                 per-expert counts and their prefixes over the blocks
 //   gate/up GEMM: per (expert, 128 intermediate rows, <=128 tokens): dequantised Q4
 //                 gate and up tiles x gathered token rows, SwiGLU in the epilogue -> h (bf16)
 //   down GEMM   : per (expert, 128 output rows, <=128 tokens): Q4 down tile x h rows,
@@ -673,13 +673,9 @@ __global__ void __launch_bounds__(Cfg<MODE, RT>::THREADS, 1) grouped_gemm_kernel
 // small kernels around the GEMMs
 // -------------------------------------------------------------------------------------
 
-// x_perm[t][8c + pos(i)] = x[t][8c + i]; also clears the per-expert counts that the top-k
-// kernel accumulates (the workspace layout depends on T, so nothing is assumed about them).
-__global__ void x_perm_kernel(const uint4 *__restrict__ x, uint4 *__restrict__ xp, int nchunks,
-                              int32_t *__restrict__ counts, int ncounts) {
+// x_perm[t][8c + pos(i)] = x[t][8c + i].
+__global__ void x_perm_kernel(const uint4 *__restrict__ x, uint4 *__restrict__ xp, int nchunks) {
   pdl_enter();
-  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < ncounts; i += gridDim.x * blockDim.x)
-    counts[i] = 0;
   for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < nchunks; i += gridDim.x * blockDim.x) {
     const uint4 v = __ldg(x + i);
     uint4 o;
@@ -701,7 +697,7 @@ struct TopkArgs {
   int32_t *idx;
   float *p;
   float *sigma;
-  int32_t *counts;
+  int32_t *ctab;  // [gridDim.x][E]: the block's selection count per expert
   int32_t *out_idx;
   float *out_w;
 };
@@ -709,10 +705,11 @@ struct TopkArgs {
 // One warp per token: logits = fixed-order sum of the router GEMM's K-split partials plus
 // the per-expert offsets, held in registers (EC per lane); the k largest (logit desc, index
 // asc); softmax over the k; shared gate sigmoid(x . g).  The block's selections are counted
-// per expert in shared memory first and added to the global counts once per (block, expert):
-// a skewed router sends most tokens to the same experts, and one global atomic per selection
-// would serialise on those counters.
+// per expert in shared memory and written to the count table (every expert, zeros included):
+// the scan turns each expert's row into block prefixes, so the bucketing is stable without a
+// global atomic per selection (a skewed router sends most tokens to the same experts).
 constexpr int kTopkTokens = 16;  // tokens (warps) per block
+constexpr int kMaxTopK = 16;     // the API's top-k limit
 template <int EC>
 __global__ void __launch_bounds__(32 * kTopkTokens) topk_prefill_kernel(TopkArgs a) {
   pdl_enter();
@@ -790,18 +787,21 @@ __global__ void __launch_bounds__(32 * kTopkTokens) topk_prefill_kernel(TopkArgs
   }
   __syncthreads();
   for (int e = threadIdx.x; e < a.E; e += blockDim.x)
-    if (s_cnt[e]) atomicAdd(a.counts + e, s_cnt[e]);
+    a.ctab[(size_t)blockIdx.x * a.E + e] = s_cnt[e];
 }
 
 struct ScanArgs {
-  const int32_t *counts;  // [E]
+  int32_t *ctab;     // [nb][E] block counts -> exclusive prefixes over the blocks
+  int nb;            // top-k blocks
   int32_t *offsets;  // [E+2]
   int4 *items_gu, *items_dn;
   int32_t *hdr;
   int T, E, k, has_shared, mt_gu, mt_dn;
 };
 
-// Single block: per-expert offsets and the GEMM work lists.
+// Single block: each expert's row of the count table becomes the exclusive prefix over the
+// top-k blocks (one warp per expert, rows of 32 blocks at a time), the expert totals give the
+// per-expert offsets, then the GEMM work lists.
 __global__ void __launch_bounds__(1024) scan_items_kernel(ScanArgs a) {
   pdl_enter();
   __shared__ int s_cnt[1025];
@@ -809,11 +809,76 @@ __global__ void __launch_bounds__(1024) scan_items_kernel(ScanArgs a) {
   __shared__ int s_nt[1025];
   __shared__ int s_ibase[1026];
   const int nexp = a.E + a.has_shared;
-  for (int e = threadIdx.x; e < nexp; e += blockDim.x) {
-    const int c = e < a.E ? min(max(a.counts[e], 0), a.T) : a.T;
-    s_cnt[e] = c;
-    s_nt[e] = (c + kBN - 1) / kBN;
+  // G = blockDim / E thread groups; group g takes the blocks [g*seg, g*seg + seg) of every
+  // expert (thread e of the group: expert e, so a warp reads consecutive experts of a block
+  // row): the group's sums meet in shared memory, then each group rewrites its blocks as
+  // prefixes.  E > blockDim takes several passes with one group.
+  __shared__ int s_gsum[1024];
+  const int G = max(1, (int)blockDim.x / a.E);
+  const int seg = (a.nb + G - 1) / G;
+  for (int e0 = 0; e0 < a.E; e0 += (int)blockDim.x / G) {
+    const int g = (int)threadIdx.x / (a.E < (int)blockDim.x ? a.E : (int)blockDim.x);
+    const int e = e0 + (int)threadIdx.x % (a.E < (int)blockDim.x ? a.E : (int)blockDim.x);
+    const bool live = g < G && e < a.E;
+    const int b0 = min(a.nb, g * seg), b1 = min(a.nb, b0 + seg);
+    // a segment of at most kSegV blocks is read once and kept in registers; a longer one is
+    // read twice, eight loads in flight at a time
+    constexpr int kSegV = 32;
+    int v[kSegV];
+    int sum = 0;
+    if (live) {
+      if (seg <= kSegV) {
+#pragma unroll
+        for (int q = 0; q < kSegV; ++q) v[q] = b0 + q < b1 ? a.ctab[(size_t)(b0 + q) * a.E + e] : 0;
+#pragma unroll
+        for (int q = 0; q < kSegV; ++q) sum += v[q];
+      } else {
+        for (int c = b0; c < b1; c += 8) {
+          int u[8];
+#pragma unroll
+          for (int q = 0; q < 8; ++q) u[q] = c + q < b1 ? a.ctab[(size_t)(c + q) * a.E + e] : 0;
+#pragma unroll
+          for (int q = 0; q < 8; ++q) sum += u[q];
+        }
+      }
+      s_gsum[g * (a.E < (int)blockDim.x ? a.E : (int)blockDim.x) + (e - e0)] = sum;
+    }
+    __syncthreads();
+    if (live) {
+      const int w = a.E < (int)blockDim.x ? a.E : (int)blockDim.x;
+      int run = 0, tot = 0;
+      for (int h = 0; h < G; ++h) {
+        const int gs = s_gsum[h * w + (e - e0)];
+        if (h < g) run += gs;
+        tot += gs;
+      }
+      if (seg <= kSegV) {
+#pragma unroll
+        for (int q = 0; q < kSegV; ++q)
+          if (b0 + q < b1) {
+            a.ctab[(size_t)(b0 + q) * a.E + e] = run;
+            run += v[q];
+          }
+      } else {
+        for (int c = b0; c < b1; c += 8) {
+          int u[8];
+#pragma unroll
+          for (int q = 0; q < 8; ++q) u[q] = c + q < b1 ? a.ctab[(size_t)(c + q) * a.E + e] : 0;
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+            if (c + q < b1) {
+              a.ctab[(size_t)(c + q) * a.E + e] = run;
+              run += u[q];
+            }
+        }
+      }
+      if (g == 0) s_cnt[e] = min(tot, a.T);
+    }
+    __syncthreads();
   }
+  if (a.has_shared && threadIdx.x == 0) s_cnt[a.E] = a.T;
+  __syncthreads();
+  for (int e = threadIdx.x; e < nexp; e += blockDim.x) s_nt[e] = (s_cnt[e] + kBN - 1) / kBN;
   __syncthreads();
   if (threadIdx.x < 32) {
     const int lane = threadIdx.x;
@@ -868,28 +933,26 @@ struct PermArgs {
   const float *p;
   const float *sigma;
   const int32_t *offsets;
-  int32_t *counts;  // per-expert selection counts; used up as cursors (left at zero)
+  const int32_t *ctab;  // [nb][E] exclusive prefixes over the top-k blocks
+  int nb;
   int32_t *perm;
   float *pw;
   int32_t *inv;
   int T, E, k, has_shared;
 };
 
-// Pair rows: one thread per selection (t, i).  A block ranks its selections per expert in
-// shared memory, reserves one range per (block, expert) from an atomic cursor on the expert's
-// count (counting it down to zero), and each selection takes base + rank; the blocks past the
-// selections write the shared expert's rows, every token in order.  The order of an expert's
-// pairs is therefore not fixed, and no result depends on it: every output element of the
-// expert GEMMs is one dot product of a weight row with one pair's token (or h) row,
-// accumulated in a fixed k-block order, and combine sums a token's slots in slot order.
-constexpr int kPlaceThreads = 256;
+// Stable bucketing (token order within an expert): block b places the selections of the
+// tokens of top-k block b; a selection's row is its expert's offset, plus the selections of
+// that expert in earlier blocks (the scanned count table, [block][expert]), plus its rank
+// among the block's earlier selections of the expert.  The blocks past them write the shared expert's rows,
+// every token in order.
+constexpr int kPlaceThreads = kTopkTokens * kMaxTopK;
 __global__ void __launch_bounds__(kPlaceThreads) place_kernel(PermArgs a) {
   pdl_enter();
-  __shared__ int s_cnt[1024];  // E <= 1024
-  const int n = a.T * a.k, kk = a.k + 1;
-  const int nsel_blocks = (n + kPlaceThreads - 1) / kPlaceThreads;
-  if ((int)blockIdx.x >= nsel_blocks) {  // shared expert
-    const int t = ((int)blockIdx.x - nsel_blocks) * kPlaceThreads + (int)threadIdx.x;
+  __shared__ int s_e[kPlaceThreads];
+  const int kk = a.k + 1;
+  if ((int)blockIdx.x >= a.nb) {  // shared expert
+    const int t = ((int)blockIdx.x - a.nb) * kPlaceThreads + (int)threadIdx.x;
     if (t < a.T) {
       const int pos = a.offsets[a.E] + t;
       a.perm[pos] = t;
@@ -898,20 +961,17 @@ __global__ void __launch_bounds__(kPlaceThreads) place_kernel(PermArgs a) {
     }
     return;
   }
-  for (int e = threadIdx.x; e < a.E; e += blockDim.x) s_cnt[e] = 0;
+  const int n = a.T * a.k, j0 = blockIdx.x * kTopkTokens * a.k;
+  const int nb_sel = min(n - j0, kTopkTokens * a.k);
+  const int q = threadIdx.x;
+  const int e = q < nb_sel ? a.idx[j0 + q] : -1;
+  s_e[q] = e;
   __syncthreads();
-  const int j = blockIdx.x * kPlaceThreads + threadIdx.x;
-  const int e = j < n ? a.idx[j] : 0;
-  const int rank = j < n ? atomicAdd(s_cnt + e, 1) : 0;
-  __syncthreads();
-  for (int q = threadIdx.x; q < a.E; q += blockDim.x) {
-    const int c = s_cnt[q];
-    if (c) s_cnt[q] = atomicSub(a.counts + q, c) - c;  // the block's range: [old - c, old)
-  }
-  __syncthreads();
-  if (j < n) {
-    const int t = j / a.k, i = j - t * a.k;
-    const int pos = a.offsets[e] + s_cnt[e] + rank;
+  if (q < nb_sel) {
+    int rank = 0;
+    for (int r = 0; r < q; ++r) rank += s_e[r] == e;
+    const int j = j0 + q, t = j / a.k, i = j - t * a.k;
+    const int pos = a.offsets[e] + a.ctab[(size_t)blockIdx.x * a.E + e] + rank;
     a.perm[pos] = t;
     a.pw[pos] = a.p[j];
     a.inv[t * kk + i] = pos;
@@ -1129,7 +1189,7 @@ PrefillWsLayout prefill_ws_layout(const lily_q4_moe_layer &L, int T) {
   l.off_idx = take(sizeof(int32_t) * (size_t)T * l.k);
   l.off_p = take(sizeof(float) * (size_t)T * l.k);
   l.off_sigma = take(sizeof(float) * (size_t)T);
-  l.off_counts = take(sizeof(int32_t) * (size_t)(l.E + 1));
+  l.off_ctab = take(sizeof(int32_t) * (size_t)l.E * (size_t)((T + kTopkTokens - 1) / kTopkTokens));
   l.off_offsets = take(sizeof(int32_t) * (size_t)(l.E + 2));
   l.off_perm = take(sizeof(int32_t) * (size_t)l.P);
   l.off_pw = take(sizeof(float) * (size_t)l.P);
@@ -1197,7 +1257,8 @@ int launch_moe_prefill(const lily_q4_moe_layer &L, const uint16_t *x, int T, uin
   int32_t *idx = reinterpret_cast<int32_t *>(b + l.off_idx);
   float *p = reinterpret_cast<float *>(b + l.off_p);
   float *sigma = reinterpret_cast<float *>(b + l.off_sigma);
-  int32_t *counts = reinterpret_cast<int32_t *>(b + l.off_counts);
+  int32_t *ctab = reinterpret_cast<int32_t *>(b + l.off_ctab);
+  const int nbk = (T + kTopkTokens - 1) / kTopkTokens;  // top-k blocks
   int32_t *offsets = reinterpret_cast<int32_t *>(b + l.off_offsets);
   int32_t *perm = reinterpret_cast<int32_t *>(b + l.off_perm);
   float *pw = reinterpret_cast<float *>(b + l.off_pw);
@@ -1220,7 +1281,7 @@ int launch_moe_prefill(const lily_q4_moe_layer &L, const uint16_t *x, int T, uin
   const int nch = T * H / 8;
   if (launch_pdl(x_perm_kernel, dim3((nch + 255) / 256 < 4 * sms ? (nch + 255) / 256 : 4 * sms),
                  dim3(256), 0, st, reinterpret_cast<const uint4 *>(x), reinterpret_cast<uint4 *>(xperm),
-                 nch, counts, E) != cudaSuccess)
+                 nch) != cudaSuccess)
     return LILY_Q4_ERR_CUDA;
 
   // router GEMM (an 8-bit router in its exact bf16 form, the token rows widened to match)
@@ -1253,20 +1314,19 @@ int launch_moe_prefill(const lily_q4_moe_layer &L, const uint16_t *x, int T, uin
   if (rc != LILY_Q4_OK) return rc;
 
   TopkArgs ta{logits, L.router_bias, ra.ksplit, x, L.shared_gate, T, E, H, k, L.has_shared,
-              idx, p, sigma, counts, topk_idx, topk_w};
-  const dim3 tk_grid((T + kTopkTokens - 1) / kTopkTokens), tk_block(32 * kTopkTokens);
+              idx, p, sigma, ctab, topk_idx, topk_w};
+  const dim3 tk_grid(nbk), tk_block(32 * kTopkTokens);
   cudaError_t ce = E <= 256   ? launch_pdl(topk_prefill_kernel<8>, tk_grid, tk_block, 0, st, ta)
                    : E <= 512 ? launch_pdl(topk_prefill_kernel<16>, tk_grid, tk_block, 0, st, ta)
                               : launch_pdl(topk_prefill_kernel<32>, tk_grid, tk_block, 0, st, ta);
   if (ce != cudaSuccess) return LILY_Q4_ERR_CUDA;
 
-  ScanArgs sa{counts, offsets, items_gu, items_dn, hdr, T, E, k, L.has_shared, mt_gu, mt_dn};
+  ScanArgs sa{ctab, nbk, offsets, items_gu, items_dn, hdr, T, E, k, L.has_shared, mt_gu, mt_dn};
   if (launch_pdl(scan_items_kernel, dim3(1), dim3(1024), 0, st, sa) != cudaSuccess)
     return LILY_Q4_ERR_CUDA;
 
-  PermArgs pa{idx, p, sigma, offsets, counts, perm, pw, inv, T, E, k, L.has_shared};
-  const int nplace = (T * k + kPlaceThreads - 1) / kPlaceThreads +
-                     (L.has_shared ? (T + kPlaceThreads - 1) / kPlaceThreads : 0);
+  PermArgs pa{idx, p, sigma, offsets, ctab, nbk, perm, pw, inv, T, E, k, L.has_shared};
+  const int nplace = nbk + (L.has_shared ? (T + kPlaceThreads - 1) / kPlaceThreads : 0);
   if (launch_pdl(place_kernel, dim3(nplace), dim3(kPlaceThreads), 0, st, pa) != cudaSuccess)
     return LILY_Q4_ERR_CUDA;
 

@@ -65,13 +65,15 @@ __device__ __forceinline__ void pdl_enter() {
   pdl_wait_prev();
 }
 
-// 32 bytes (one 256-bit load; p 32-byte aligned), streamed like ld_stream.
+// 32 bytes (one 256-bit load; p 32-byte aligned) of a weight row that is read k-block by
+// k-block: L2 fetches the surrounding 256 bytes (the row's next k-blocks) with it, at normal
+// priority (the expert GEMMs re-read a tile's rows for each of its token tiles).
 __device__ __forceinline__ void ld_stream32(const void *p, uint4 &lo, uint4 &hi) {
   asm volatile(
-      "ld.global.nc.L1::no_allocate.L2::cache_hint.v8.u32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8], %9;"
+      "ld.global.nc.L1::no_allocate.L2::256B.v8.u32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
       : "=r"(lo.x), "=r"(lo.y), "=r"(lo.z), "=r"(lo.w), "=r"(hi.x), "=r"(hi.y), "=r"(hi.z),
         "=r"(hi.w)
-      : "l"(p), "l"(l2_evict_first()));
+      : "l"(p));
 }
 
 __device__ __forceinline__ uint16_t ld_u16(const uint16_t *p) {
