@@ -160,12 +160,21 @@ __device__ __forceinline__ void block_argmax_finish(float best_v, int best_i, in
       int i = lane < NW ? si_[lane] : INT_MAX;
       warp_argmax(v, i);
       if (lane == 0) {
+        // The block's (value, row) folds into the packed maximum with a fire-and-forget
+        // reduction; the ticket is an acquire-release add, so the reduction is ordered before
+        // it and the last block, acquiring, sees every block's.  No round trip but the ticket.
         unsigned long long *mx = reinterpret_cast<unsigned long long *>(hdr + kHdrArgmax64);
-        atomicMax(mx, ((unsigned long long)f2key(v) << 32) | (0xFFFFFFFFu - (uint32_t)i));
-        __threadfence();
-        if (atomicAdd(hdr + kHdrCounterA, 1) == (int)gridDim.x - 1) {
-          __threadfence();
-          const unsigned long long k = atomicExch(mx, 0ull);  // read, and re-arm
+        const unsigned long long key =
+            ((unsigned long long)f2key(v) << 32) | (0xFFFFFFFFu - (uint32_t)i);
+        asm volatile("red.relaxed.gpu.global.max.u64 [%0], %1;" ::"l"(mx), "l"(key) : "memory");
+        int ticket;
+        asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;"
+                     : "=r"(ticket)
+                     : "l"(hdr + kHdrCounterA)
+                     : "memory");
+        if (ticket == (int)gridDim.x - 1) {
+          unsigned long long k;  // read, and re-arm
+          asm volatile("atom.acquire.gpu.global.exch.b64 %0, [%1], 0;" : "=l"(k) : "l"(mx) : "memory");
           *token = (int32_t)(0xFFFFFFFFu - (uint32_t)k);
           hdr[kHdrCounterA] = 0;
         }
