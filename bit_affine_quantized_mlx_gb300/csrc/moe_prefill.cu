@@ -8,9 +8,9 @@
 //   x_perm      : token rows with K permuted inside every 8-element chunk to the order
 //                 the Q4 unpack produces (0,4,1,5,2,6,3,7), so dequantised weight words
 //                 are stored without a shuffle (a dot product is unchanged when both
-//                 operands are permuted alike)
+//                 operands are permuted alike); the shared gate sigmoid(x . g) per token
 //   router GEMM : logits[T][E] = x Wr^T (+ offsets), bf16 x bf16 -> fp32 on tcgen05
-//   topk        : top-k per token, softmax over the k, shared gate sigmoid(x . g)
+//   topk        : top-k per token, softmax over the k
 //   scan        : per-expert offsets of the expert-sorted pairs, GEMM work lists
 //   place       : stable bucketing (token order inside an expert) from the top-k blocks'
 //                 per-expert counts and their prefixes over the blocks
@@ -673,17 +673,49 @@ __global__ void __launch_bounds__(Cfg<MODE, RT>::THREADS, 1) grouped_gemm_kernel
 // small kernels around the GEMMs
 // -------------------------------------------------------------------------------------
 
-// x_perm[t][8c + pos(i)] = x[t][8c + i].
-__global__ void x_perm_kernel(const uint4 *__restrict__ x, uint4 *__restrict__ xp, int nchunks) {
+// x_perm[t][8c + pos(i)] = x[t][8c + i], one warp per token row; with a shared expert the
+// same warp forms its gate sigmoid(x . g) from the chunks it reads (sigma[t]).  Lane l takes
+// chunks l, l + 32, ... (8 bf16 each) and accumulates them in that order; the lanes' sums
+// meet in a fixed-order warp sum.
+__global__ void x_perm_kernel(const uint16_t *__restrict__ x, uint16_t *__restrict__ xp, int T,
+                              int H, const uint16_t *__restrict__ g, float *__restrict__ sigma) {
   pdl_enter();
-  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < nchunks; i += gridDim.x * blockDim.x) {
-    const uint4 v = __ldg(x + i);
+  const int lane = threadIdx.x & 31;
+  const int t = blockIdx.x * ((int)blockDim.x / 32) + ((int)threadIdx.x >> 5);
+  if (t >= T) return;
+  const uint4 *xr = reinterpret_cast<const uint4 *>(x + (size_t)t * H);
+  const uint4 *gr = reinterpret_cast<const uint4 *>(g);
+  uint4 *pr = reinterpret_cast<uint4 *>(xp + (size_t)t * H);
+  const int cpr = H / 8;  // <= 256
+  uint4 xv[8], gv[8];
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    const int ch = lane + 32 * c;
+    xv[c] = ch < cpr ? __ldg(xr + ch) : make_uint4(0, 0, 0, 0);
+    gv[c] = (g && ch < cpr) ? __ldg(gr + ch) : make_uint4(0, 0, 0, 0);
+  }
+  float acc = 0.f;
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    const int ch = lane + 32 * c;
+    if (ch >= cpr) break;
+    const uint4 v = xv[c];
     uint4 o;
     o.x = __byte_perm(v.x, v.z, 0x5410);
     o.y = __byte_perm(v.x, v.z, 0x7632);
     o.z = __byte_perm(v.y, v.w, 0x5410);
     o.w = __byte_perm(v.y, v.w, 0x7632);
-    xp[i] = o;
+    pr[ch] = o;
+    const uint32_t xx[4] = {v.x, v.y, v.z, v.w}, gg[4] = {gv[c].x, gv[c].y, gv[c].z, gv[c].w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      acc = fmaf(__uint_as_float(xx[i] << 16), __uint_as_float(gg[i] << 16), acc);
+      acc = fmaf(__uint_as_float(xx[i] & 0xFFFF0000u), __uint_as_float(gg[i] & 0xFFFF0000u), acc);
+    }
+  }
+  if (g) {
+    acc = seg_sum<32>(acc);
+    if (lane == 0) sigma[t] = 1.0f / (1.0f + expf(-acc));
   }
 }
 
@@ -691,12 +723,9 @@ struct TopkArgs {
   const float *logits;  // [nsplit][T][E] partials
   const float *bias;    // [E] or NULL
   int nsplit;
-  const uint16_t *x;
-  const uint16_t *shared_gate;
-  int T, E, H, k, has_shared;
+  int T, E, k;
   int32_t *idx;
   float *p;
-  float *sigma;
   int32_t *ctab;  // [gridDim.x][E]: the block's selection count per expert
   int32_t *out_idx;
   float *out_w;
@@ -704,7 +733,7 @@ struct TopkArgs {
 
 // One warp per token: logits = fixed-order sum of the router GEMM's K-split partials plus
 // the per-expert offsets, held in registers (EC per lane); the k largest (logit desc, index
-// asc); softmax over the k; shared gate sigmoid(x . g).  The block's selections are counted
+// asc); softmax over the k.  The block's selections are counted
 // per expert in shared memory and written to the count table (every expert, zeros included):
 // the scan turns each expert's row into block prefixes, so the bucketing is stable without a
 // global atomic per selection (a skewed router sends most tokens to the same experts).
@@ -746,31 +775,6 @@ __global__ void __launch_bounds__(32 * kTopkTokens) topk_prefill_kernel(TopkArgs
   float myv;  // lane i < k keeps selection i
   int mye;
   warp_topk_keys<EC>(key, a.k, mye, myv);
-  float sig = 0.f;
-  if (a.has_shared) {
-    const uint16_t *xt = a.x + (size_t)t * a.H;
-    float acc = 0.f;
-    // H <= 2048: at most 8 chunks per lane, all loaded before the dot products
-    uint4 xv[8], gv[8];
-#pragma unroll
-    for (int c = 0; c < 8; ++c) {
-      const int h = lane * 8 + 256 * c;
-      xv[c] = h < a.H ? __ldg(reinterpret_cast<const uint4 *>(xt + h)) : make_uint4(0, 0, 0, 0);
-      gv[c] = h < a.H ? __ldg(reinterpret_cast<const uint4 *>(a.shared_gate + h)) : make_uint4(0, 0, 0, 0);
-    }
-#pragma unroll
-    for (int c = 0; c < 8; ++c) {
-      if (lane * 8 + 256 * c >= a.H) break;
-      const uint32_t xx[4] = {xv[c].x, xv[c].y, xv[c].z, xv[c].w}, gg[4] = {gv[c].x, gv[c].y, gv[c].z, gv[c].w};
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        acc = fmaf(__uint_as_float(xx[i] << 16), __uint_as_float(gg[i] << 16), acc);
-        acc = fmaf(__uint_as_float(xx[i] & 0xFFFF0000u), __uint_as_float(gg[i] & 0xFFFF0000u), acc);
-      }
-    }
-    acc = seg_sum<32>(acc);
-    sig = 1.0f / (1.0f + expf(-acc));
-  }
   // softmax over the k selected logits, one selection per lane
   const float v0 = __shfl_sync(0xffffffffu, myv, 0);
   const float ex = lane < a.k ? expf(myv - v0) : 0.f;
@@ -783,7 +787,6 @@ __global__ void __launch_bounds__(32 * kTopkTokens) topk_prefill_kernel(TopkArgs
     if (a.out_w) a.out_w[t * a.k + lane] = pi;
     atomicAdd(s_cnt + mye, 1);
   }
-  if (lane == 0) a.sigma[t] = sig;
   }
   __syncthreads();
   for (int e = threadIdx.x; e < a.E; e += blockDim.x)
@@ -1299,10 +1302,10 @@ int launch_moe_prefill(const lily_q4_moe_layer &L, const uint16_t *x, int T, uin
   // Every launch below is a programmatic dependent of the one before it (launch_pdl): set-up
   // overlaps the previous kernel's tail, and each kernel waits for that kernel's completion
   // before it reads or writes anything the chain shares.
-  const int nch = T * H / 8;
-  if (launch_pdl(x_perm_kernel, dim3((nch + 255) / 256 < 4 * sms ? (nch + 255) / 256 : 4 * sms),
-                 dim3(256), 0, st, reinterpret_cast<const uint4 *>(x), reinterpret_cast<uint4 *>(xperm),
-                 nch) != cudaSuccess)
+  // token permutation, and the shared expert's gate (one warp per token)
+  const uint16_t *sgate = L.has_shared ? L.shared_gate : nullptr;
+  if (launch_pdl(x_perm_kernel, dim3((T + 7) / 8), dim3(256), 0, st, x, xperm, T, H, sgate, sigma) !=
+      cudaSuccess)
     return LILY_Q4_ERR_CUDA;
 
   // router GEMM (an 8-bit router in its exact bf16 form, the token rows widened to match)
@@ -1334,8 +1337,7 @@ int launch_moe_prefill(const lily_q4_moe_layer &L, const uint16_t *x, int T, uin
   int rc = launch_gemm<kRouter>(ra, ra.n_items_static < sms ? ra.n_items_static : sms, st);
   if (rc != LILY_Q4_OK) return rc;
 
-  TopkArgs ta{logits, L.router_bias, ra.ksplit, x, L.shared_gate, T, E, H, k, L.has_shared,
-              idx, p, sigma, ctab, topk_idx, topk_w};
+  TopkArgs ta{logits, L.router_bias, ra.ksplit, T, E, k, idx, p, ctab, topk_idx, topk_w};
   const dim3 tk_grid(nbk), tk_block(32 * kTopkTokens);
   cudaError_t ce = E <= 256   ? launch_pdl(topk_prefill_kernel<8>, tk_grid, tk_block, 0, st, ta)
                    : E <= 512 ? launch_pdl(topk_prefill_kernel<16>, tk_grid, tk_block, 0, st, ta)
