@@ -186,3 +186,36 @@ def test_prefill_q4xl_layout_full_size(torch_dev):
     ref = orc.moe(L, x)
     assert_topk_equal(idx, w, ref, "q4-xl prefill 2048 tokens")
     assert_close(y, ref["y"], "q4-xl prefill 2048 tokens, every token")
+
+
+def test_prefill_weights_16_byte_aligned(torch_dev):
+    """The API promises 16-byte aligned code arrays.  When a gate/up code array is not 32-byte
+    aligned, the gate/up GEMM takes each row's k-block with two threads (128-bit loads)
+    instead of one (a 256-bit load): same values, so y is bit-identical to the aligned run,
+    and within the tolerance of the oracle."""
+    torch, dev = torch_dev
+    H, E, k, I, T = 512, 8, 2, 256, 150
+    key = (83, 0)
+    L = synth.draw_layer(H, E, k, I, shared=True, router_std=0.05, router_bias=False, key=key)
+    x = _inputs(L, key, T)
+    dl = q4.DeviceLayer.upload(L, dev)
+    ya, ia, _ = run_prefill(torch, dev, dl, x)
+
+    def shifted(t):
+        # the same words 16 bytes into a fresh buffer: 16-byte but not 32-byte aligned
+        buf = torch.zeros(t.numel() + 4, dtype=t.dtype, device=dev)
+        buf[4:].copy_(t.reshape(-1))
+        view = buf[4:].view(t.shape)
+        assert view.data_ptr() % 32 == 16
+        return view, buf
+
+    keep = []
+    for m in (dl.gate, dl.up, dl.sh_gate, dl.sh_up):
+        m.w, b = shifted(m.w)
+        keep.append(b)
+    dl._c = None
+    yb, ib, _ = run_prefill(torch, dev, dl, x)
+    assert (ia == ib).all()
+    assert np.array_equal(ya, yb), "two-threads-per-row gate/up differs from the one-thread form"
+    ref = orc.moe(L, x)
+    assert_close(yb, ref["y"], "16-byte aligned weights")
