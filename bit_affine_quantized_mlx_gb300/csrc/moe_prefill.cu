@@ -82,17 +82,17 @@ enum { kRouter = 0, kGateUp = 1, kDown = 2 };
 // tensor memory (row i in lane i), so shared-memory bandwidth is left to the token tiles.
 // TMEM columns: accumulators first (NACC buffers of ACC_COLS), then SA A stages of 32*NA*KS.
 // RT = producer threads per weight row (1: the row's whole k-block, 8 code words; 2: 4 each).
-// KS = k-blocks (64 of K) per pipeline stage: gate/up hands over two k-blocks at a time, so
-// the MMA thread's per-stage waits, fences and commits are paid once per 16 MMAs (measured
-// faster there, slower for down).  A stage's A columns are [matrix][k-block][32]; its B tile
-// is KS 128-byte-swizzled [kBN][64] sub-tiles.
+// KS = k-blocks (64 of K) per pipeline stage: the expert GEMMs hand over two k-blocks at a
+// time, so the MMA thread's per-stage waits, fences and commits are paid once per 16 (gate/up)
+// or 8 (down) MMAs; that loop, not the tensor pipe, bounds the small token tiles.  A stage's A
+// columns are [matrix][k-block][32]; its B tile is KS 128-byte-swizzled [kBN][64] sub-tiles.
 template <int MODE, int RT = 2>
 struct Cfg {
   static constexpr bool TMEM_A = MODE != kRouter;
   static constexpr int NA = MODE == kGateUp ? 2 : 1;  // A tiles per k-block
-  static constexpr int KS = MODE == kGateUp ? 2 : 1;  // k-blocks per stage
-  static constexpr int SA = MODE == kGateUp ? 2 : (MODE == kDown ? 8 : 4);  // A stages
-  static constexpr int SB = MODE == kGateUp ? 4 : (MODE == kDown ? 8 : 6);  // B (token) stages
+  static constexpr int KS = MODE == kRouter ? 1 : 2;  // k-blocks per stage
+  static constexpr int SA = MODE == kGateUp ? 2 : 4;  // A stages
+  static constexpr int SB = MODE == kGateUp ? 4 : (MODE == kDown ? 4 : 6);  // B (token) stages
   static constexpr int AT = NA * kBM * RT;            // weight-producer threads
   static constexpr int XB = 0;                        // gather warps after the producers
   static constexpr int BT = kBThreads + 32 * XB;      // token-row gather threads
@@ -434,7 +434,7 @@ __global__ void __launch_bounds__(Cfg<MODE, RT>::THREADS, 1) grouped_gemm_kernel
   } else if (MODE == kDown && warp >= kBWarp0 && warp < kAWarp0) {
     // ------------------------------------------------------------------ h rows (down)
     // An item's h rows are consecutive pair rows, stored k-block-major and pre-swizzled by the
-    // gate/up epilogue: a B stage is one bulk copy of the item's ntok rows of one k-block
+    // gate/up epilogue: each k-block of a B stage is one bulk copy of the item's ntok rows
     // (rows past ntok keep stale data; they only feed accumulator columns that are not stored).
     if (warp == kBWarp0 && lane == 0) {
       int sb = 0;
@@ -445,15 +445,18 @@ __global__ void __launch_bounds__(Cfg<MODE, RT>::THREADS, 1) grouped_gemm_kernel
         const int4 item = get_item<MODE>(a, it, s_items);
         const uint32_t bytes = (uint32_t)item.z * 128u;
         const int nk = item_nkb<MODE>(a, item, nkb);
-        for (int kb = 0; kb < nk; ++kb) {
+        for (int kb = 0; kb < nk; kb += C::KS) {
           if (!tc::wait_bar(bempty(sb), pb ^ 1, &s_abort, err, kSleepNs)) {
             ok = false;
             break;
           }
-          const int kbs = kb < nkb ? kb : kb - nkb;  // a doubled K reads the rows twice
           const uint32_t sB = sbase + C::OFF_B + sb * C::B_BYTES;
-          tc::mbar_arrive_expect_tx(bfull(sb), bytes);
-          tc::bulk_g2s(sB, a.b_src + ((size_t)kbs * a.P + item.y) * 64, bytes, bfull(sb));
+          tc::mbar_arrive_expect_tx(bfull(sb), bytes * C::KS);
+#pragma unroll
+          for (int ks = 0; ks < C::KS; ++ks) {
+            const int kbs = kb + ks < nkb ? kb + ks : kb + ks - nkb;  // a doubled K reads the rows twice
+            tc::bulk_g2s(sB + ks * C::B_SUB, a.b_src + ((size_t)kbs * a.P + item.y) * 64, bytes, bfull(sb));
+          }
           ++issued;
           if (++sb == C::SB) { sb = 0; pb ^= 1; }
         }
