@@ -72,8 +72,8 @@ struct PrefillWsLayout {
   size_t off_idx;       // i32 [T][k]
   size_t off_p;         // f32 [T][k]
   size_t off_sigma;     // f32 [T]
-  size_t off_ctab;      // i32 [T/16 blocks][E]: each top-k block's count per expert, then
-                        // (after the scan) the exclusive prefix over blocks
+  size_t off_ctab;      // i32 [T/16 blocks][E]: each top-k block's count per expert
+  size_t off_cpre;      // i32 [T/128][E]: exclusive prefix over the blocks before every 8th
   size_t off_offsets;   // i32 [E+2] exclusive prefix of counts
   size_t off_perm;      // i32 [P] token of each sorted pair
   size_t off_pw;        // f32 [P] combine weight of each sorted pair

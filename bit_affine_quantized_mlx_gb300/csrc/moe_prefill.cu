@@ -796,18 +796,27 @@ __global__ void __launch_bounds__(32 * kTopkTokens) topk_prefill_kernel(TopkArgs
     a.ctab[(size_t)blockIdx.x * a.E + e] = s_cnt[e];
 }
 
+// Rows of the block-prefix table the scan writes: every kPrefixStride-th top-k block; the
+// placement adds the counts of the (< kPrefixStride) blocks between.
+constexpr int kPrefixStride = 8;
+// Tiles whose expert the scan looks up in a shared-memory table (more: binary search).
+constexpr int kTileTable = 4096;
+
 struct ScanArgs {
-  int32_t *ctab;     // [nb][E] block counts -> exclusive prefixes over the blocks
-  int nb;            // top-k blocks
+  const int32_t *ctab;  // [nb][E] block counts
+  int32_t *cpre;        // [ceil(nb / kPrefixStride)][E] exclusive prefix over the blocks before
+                        // every kPrefixStride-th block
+  int nb;               // top-k blocks
   int32_t *offsets;  // [E+2]
   int4 *items_gu, *items_dn;
   int32_t *hdr;
   int T, E, k, has_shared, mt_gu, mt_dn;
 };
 
-// Single block: each expert's row of the count table becomes the exclusive prefix over the
-// top-k blocks (one warp per expert, rows of 32 blocks at a time), the expert totals give the
-// per-expert offsets, then the GEMM work lists.
+// Single block: the expert totals and, at every kPrefixStride-th top-k block, each expert's
+// exclusive prefix over the blocks before it (the placement finishes the prefix of the blocks
+// between); the totals give the per-expert offsets, then the GEMM work lists (each tile's
+// expert from a table in shared memory).
 __global__ void __launch_bounds__(1024) scan_items_kernel(ScanArgs a) {
   pdl_enter();
   __shared__ int s_cnt[1025];
@@ -817,34 +826,41 @@ __global__ void __launch_bounds__(1024) scan_items_kernel(ScanArgs a) {
   const int nexp = a.E + a.has_shared;
   // G = blockDim / E thread groups; group g takes the blocks [g*seg, g*seg + seg) of every
   // expert (thread e of the group: expert e, so a warp reads consecutive experts of a block
-  // row): the group's sums meet in shared memory, then each group rewrites its blocks as
-  // prefixes.  E > blockDim takes several passes with one group.
+  // row): the group's sums meet in shared memory, then each group writes the prefixes of its
+  // segment's every kPrefixStride-th block.  E > blockDim takes several passes with one group.
   __shared__ int s_gsum[1024];
   const int G = max(1, (int)blockDim.x / a.E);
-  const int seg = (a.nb + G - 1) / G;
+  const int seg = ((a.nb + G - 1) / G + kPrefixStride - 1) / kPrefixStride * kPrefixStride;
   for (int e0 = 0; e0 < a.E; e0 += (int)blockDim.x / G) {
     const int g = (int)threadIdx.x / (a.E < (int)blockDim.x ? a.E : (int)blockDim.x);
     const int e = e0 + (int)threadIdx.x % (a.E < (int)blockDim.x ? a.E : (int)blockDim.x);
     const bool live = g < G && e < a.E;
     const int b0 = min(a.nb, g * seg), b1 = min(a.nb, b0 + seg);
-    // a segment of at most kSegV blocks is read once and kept in registers; a longer one is
-    // read twice, eight loads in flight at a time
+    // A segment (a multiple of kPrefixStride blocks, so its prefix rows sit at fixed offsets)
+    // is read once: its sum, and the partial sums before its prefix rows -- in registers for a
+    // segment of at most kSegV blocks, else written to the prefix table and completed after
+    // the groups' sums are known.
     constexpr int kSegV = 32;
-    int v[kSegV];
+    int ploc[kSegV / kPrefixStride];
     int sum = 0;
     if (live) {
       if (seg <= kSegV) {
+        int v[kSegV];
 #pragma unroll
         for (int q = 0; q < kSegV; ++q) v[q] = b0 + q < b1 ? a.ctab[(size_t)(b0 + q) * a.E + e] : 0;
 #pragma unroll
-        for (int q = 0; q < kSegV; ++q) sum += v[q];
+        for (int q = 0; q < kSegV; ++q) {
+          if (q % kPrefixStride == 0) ploc[q / kPrefixStride] = sum;
+          sum += v[q];
+        }
       } else {
-        for (int c = b0; c < b1; c += 8) {
-          int u[8];
+        for (int c = b0; c < b1; c += kPrefixStride) {
+          int u[kPrefixStride];
 #pragma unroll
-          for (int q = 0; q < 8; ++q) u[q] = c + q < b1 ? a.ctab[(size_t)(c + q) * a.E + e] : 0;
+          for (int q = 0; q < kPrefixStride; ++q) u[q] = c + q < b1 ? a.ctab[(size_t)(c + q) * a.E + e] : 0;
+          a.cpre[(size_t)(c / kPrefixStride) * a.E + e] = sum;
 #pragma unroll
-          for (int q = 0; q < 8; ++q) sum += u[q];
+          for (int q = 0; q < kPrefixStride; ++q) sum += u[q];
         }
       }
       s_gsum[g * (a.E < (int)blockDim.x ? a.E : (int)blockDim.x) + (e - e0)] = sum;
@@ -860,23 +876,11 @@ __global__ void __launch_bounds__(1024) scan_items_kernel(ScanArgs a) {
       }
       if (seg <= kSegV) {
 #pragma unroll
-        for (int q = 0; q < kSegV; ++q)
-          if (b0 + q < b1) {
-            a.ctab[(size_t)(b0 + q) * a.E + e] = run;
-            run += v[q];
-          }
+        for (int m = 0; m < kSegV / kPrefixStride; ++m)
+          if (b0 + m * kPrefixStride < b1)
+            a.cpre[(size_t)(b0 / kPrefixStride + m) * a.E + e] = run + ploc[m];
       } else {
-        for (int c = b0; c < b1; c += 8) {
-          int u[8];
-#pragma unroll
-          for (int q = 0; q < 8; ++q) u[q] = c + q < b1 ? a.ctab[(size_t)(c + q) * a.E + e] : 0;
-#pragma unroll
-          for (int q = 0; q < 8; ++q)
-            if (c + q < b1) {
-              a.ctab[(size_t)(c + q) * a.E + e] = run;
-              run += u[q];
-            }
-        }
+        for (int c = b0; c < b1; c += kPrefixStride) a.cpre[(size_t)(c / kPrefixStride) * a.E + e] += run;
       }
       if (g == 0) s_cnt[e] = min(tot, a.T);
     }
@@ -912,16 +916,29 @@ __global__ void __launch_bounds__(1024) scan_items_kernel(ScanArgs a) {
   __syncthreads();
   const int ntiles = s_ibase[nexp];
   for (int e = threadIdx.x; e < nexp; e += blockDim.x) a.offsets[e] = s_off[e];
-  // one thread per work item: its tile's expert is found by binary search of the tile bases
+  // one thread per work item: its tile's expert from the table (each expert writes its tiles'
+  // entries), or by binary search of the tile bases when the tiles outnumber the table
+  __shared__ int16_t s_t2e[kTileTable];
+  const bool table = ntiles <= kTileTable;
+  if (table) {
+    for (int e = threadIdx.x; e < nexp; e += blockDim.x)
+      for (int t = s_ibase[e]; t < s_ibase[e + 1]; ++t) s_t2e[t] = (int16_t)e;
+  }
+  __syncthreads();
   const int ngu = ntiles * a.mt_gu, nitems = ngu + ntiles * a.mt_dn;
   for (int q = threadIdx.x; q < nitems; q += blockDim.x) {
     const bool gu = q < ngu;
     const int mts = gu ? a.mt_gu : a.mt_dn, qi = gu ? q : q - ngu;
     const int tile = qi / mts, mt = qi % mts;
-    int lo = 0, hi = nexp - 1;  // last e with s_ibase[e] <= tile
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (s_ibase[mid] <= tile) lo = mid; else hi = mid - 1;
+    int lo = 0;  // last e with s_ibase[e] <= tile
+    if (table) {
+      lo = s_t2e[tile];
+    } else {
+      int hi = nexp - 1;
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (s_ibase[mid] <= tile) lo = mid; else hi = mid - 1;
+      }
     }
     const int e = lo, nt = tile - s_ibase[e];
     const int4 item = make_int4(e, s_off[e] + nt * kBN, min(kBN, s_cnt[e] - nt * kBN), mt);
@@ -939,7 +956,8 @@ struct PermArgs {
   const float *p;
   const float *sigma;
   const int32_t *offsets;
-  const int32_t *ctab;  // [nb][E] exclusive prefixes over the top-k blocks
+  const int32_t *ctab;  // [nb][E] block counts
+  const int32_t *cpre;  // [ceil(nb / kPrefixStride)][E] prefixes at every kPrefixStride-th block
   int nb;
   int32_t *perm;
   float *pw;
@@ -949,8 +967,9 @@ struct PermArgs {
 
 // Stable bucketing (token order within an expert): block b places the selections of the
 // tokens of top-k block b; a selection's row is its expert's offset, plus the selections of
-// that expert in earlier blocks (the scanned count table, [block][expert]), plus its rank
-// among the block's earlier selections of the expert.  The blocks past them write the shared expert's rows,
+// that expert in earlier blocks (the scan's prefix at the last kPrefixStride-th block, plus the
+// counts of the blocks from there to b), plus its rank among the block's earlier selections
+// of the expert.  The blocks past them write the shared expert's rows,
 // every token in order.
 constexpr int kPlaceThreads = kTopkTokens * kMaxTopK;
 __global__ void __launch_bounds__(kPlaceThreads) place_kernel(PermArgs a) {
@@ -977,7 +996,12 @@ __global__ void __launch_bounds__(kPlaceThreads) place_kernel(PermArgs a) {
     int rank = 0;
     for (int r = 0; r < q; ++r) rank += s_e[r] == e;
     const int j = j0 + q, t = j / a.k, i = j - t * a.k;
-    const int pos = a.offsets[e] + a.ctab[(size_t)blockIdx.x * a.E + e] + rank;
+    const int b = blockIdx.x, bc = b - b % kPrefixStride;
+    int before = a.cpre[(size_t)(b / kPrefixStride) * a.E + e];
+#pragma unroll
+    for (int i = 0; i < kPrefixStride - 1; ++i)  // all loads in flight together
+      if (bc + i < b) before += a.ctab[(size_t)(bc + i) * a.E + e];
+    const int pos = a.offsets[e] + before + rank;
     a.perm[pos] = t;
     a.pw[pos] = a.p[j];
     a.inv[t * kk + i] = pos;
@@ -1216,7 +1240,9 @@ PrefillWsLayout prefill_ws_layout(const lily_q4_moe_layer &L, int T) {
   l.off_idx = take(sizeof(int32_t) * (size_t)T * l.k);
   l.off_p = take(sizeof(float) * (size_t)T * l.k);
   l.off_sigma = take(sizeof(float) * (size_t)T);
-  l.off_ctab = take(sizeof(int32_t) * (size_t)l.E * (size_t)((T + kTopkTokens - 1) / kTopkTokens));
+  const size_t nbk = (size_t)((T + kTopkTokens - 1) / kTopkTokens);
+  l.off_ctab = take(sizeof(int32_t) * (size_t)l.E * nbk);
+  l.off_cpre = take(sizeof(int32_t) * (size_t)l.E * ((nbk + kPrefixStride - 1) / kPrefixStride));
   l.off_offsets = take(sizeof(int32_t) * (size_t)(l.E + 2));
   l.off_perm = take(sizeof(int32_t) * (size_t)l.P);
   l.off_pw = take(sizeof(float) * (size_t)l.P);
@@ -1285,6 +1311,7 @@ int launch_moe_prefill(const lily_q4_moe_layer &L, const uint16_t *x, int T, uin
   float *p = reinterpret_cast<float *>(b + l.off_p);
   float *sigma = reinterpret_cast<float *>(b + l.off_sigma);
   int32_t *ctab = reinterpret_cast<int32_t *>(b + l.off_ctab);
+  int32_t *cpre = reinterpret_cast<int32_t *>(b + l.off_cpre);
   const int nbk = (T + kTopkTokens - 1) / kTopkTokens;  // top-k blocks
   int32_t *offsets = reinterpret_cast<int32_t *>(b + l.off_offsets);
   int32_t *perm = reinterpret_cast<int32_t *>(b + l.off_perm);
@@ -1347,11 +1374,11 @@ int launch_moe_prefill(const lily_q4_moe_layer &L, const uint16_t *x, int T, uin
                               : launch_pdl(topk_prefill_kernel<32>, tk_grid, tk_block, 0, st, ta);
   if (ce != cudaSuccess) return LILY_Q4_ERR_CUDA;
 
-  ScanArgs sa{ctab, nbk, offsets, items_gu, items_dn, hdr, T, E, k, L.has_shared, mt_gu, mt_dn};
+  ScanArgs sa{ctab, cpre, nbk, offsets, items_gu, items_dn, hdr, T, E, k, L.has_shared, mt_gu, mt_dn};
   if (launch_pdl(scan_items_kernel, dim3(1), dim3(1024), 0, st, sa) != cudaSuccess)
     return LILY_Q4_ERR_CUDA;
 
-  PermArgs pa{idx, p, sigma, offsets, ctab, nbk, perm, pw, inv, T, E, k, L.has_shared};
+  PermArgs pa{idx, p, sigma, offsets, ctab, cpre, nbk, perm, pw, inv, T, E, k, L.has_shared};
   const int nplace = nbk + (L.has_shared ? (T + kPlaceThreads - 1) / kPlaceThreads : 0);
   if (launch_pdl(place_kernel, dim3(nplace), dim3(kPlaceThreads), 0, st, pa) != cudaSuccess)
     return LILY_Q4_ERR_CUDA;
