@@ -74,6 +74,8 @@ constexpr uint32_t kSleepNs = 1000;
 // The router GEMM splits K so that more SMs share its few tiles; the partial logits are
 // summed in a fixed order by the top-k kernel.
 __host__ __device__ constexpr int kRouterSplit(int H) { return H >= 1024 ? 4 : 1; }
+static_assert(kRouterSplit(1 << 30) <= 4 && kRouterSplit(128) <= 4,
+              "the top-k kernel sums at most four partial logits per token");
 
 enum { kRouter = 0, kGateUp = 1, kDown = 2 };
 
