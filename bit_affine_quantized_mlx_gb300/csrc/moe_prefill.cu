@@ -921,17 +921,60 @@ __global__ void __launch_bounds__(1024) scan_items_kernel(ScanArgs a) {
   // one thread per work item: its tile's expert from the table (each expert writes its tiles'
   // entries), or by binary search of the tile bases when the tiles outnumber the table
   __shared__ int16_t s_t2e[kTileTable];
-  const bool table = ntiles <= kTileTable;
+  const bool table = ntiles <= kTileTable && blockDim.x * 4 >= kTileTable;
   if (table) {
     for (int e = threadIdx.x; e < nexp; e += blockDim.x)
       for (int t = s_ibase[e]; t < s_ibase[e + 1]; ++t) s_t2e[t] = (int16_t)e;
+  }
+  __syncthreads();
+  // Work order: the tiles of more than 16 tokens first, then those of at most 16 (tile order
+  // within each part), so that the last, partial round of the round-robin hand-out of items
+  // (item i to block i mod grid) holds small tiles.  Thread j takes tiles 4j .. 4j+3; a block
+  // scan of the large-tile counts gives every tile its place.
+  __shared__ int16_t s_ord[kTileTable];
+  __shared__ int s_wbig[33];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  bool big[4] = {false, false, false, false};
+  int nbig = 0, pre = 0;
+  if (table) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int t = 4 * (int)threadIdx.x + i;
+      if (t < ntiles) {
+        const int e = s_t2e[t], nt = t - s_ibase[e];
+        big[i] = s_cnt[e] - nt * kBN > 16;
+      }
+      nbig += big[i];
+    }
+    int wt;
+    pre = warp_excl_scan(nbig, &wt);
+    if (lane == 0) s_wbig[warp] = wt;
+  }
+  __syncthreads();
+  if (table && warp == 0) {
+    int tot;
+    const int v = lane < (int)blockDim.x / 32 ? s_wbig[lane] : 0;
+    const int ex = warp_excl_scan(v, &tot);
+    s_wbig[lane] = ex;
+    if (lane == 0) s_wbig[32] = tot;
+  }
+  __syncthreads();
+  if (table) {
+    int pb = s_wbig[warp] + pre;  // large tiles before this thread's first tile
+    const int nbig_all = s_wbig[32];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int t = 4 * (int)threadIdx.x + i;
+      if (t < ntiles) s_ord[big[i] ? pb : nbig_all + t - pb] = (int16_t)t;
+      pb += big[i];
+    }
   }
   __syncthreads();
   const int ngu = ntiles * a.mt_gu, nitems = ngu + ntiles * a.mt_dn;
   for (int q = threadIdx.x; q < nitems; q += blockDim.x) {
     const bool gu = q < ngu;
     const int mts = gu ? a.mt_gu : a.mt_dn, qi = gu ? q : q - ngu;
-    const int tile = qi / mts, mt = qi % mts;
+    const int tile = table ? s_ord[qi / mts] : qi / mts, mt = qi % mts;
     int lo = 0;  // last e with s_ibase[e] <= tile
     if (table) {
       lo = s_t2e[tile];
