@@ -5,12 +5,12 @@
 // achieved"; prompt chunks of 2,048 tokens, Lily-vs-MLX report, "Measurement
 // contract").  Launch sequence on the caller's stream:
 //
-//   x_perm      : token rows with K permuted inside every 8-element chunk to the order
-//                 the Q4 unpack produces (0,4,1,5,2,6,3,7), so dequantised weight words
-//                 are stored without a shuffle (a dot product is unchanged when both
-//                 operands are permuted alike); the shared gate sigmoid(x . g) per token
 //   router GEMM : logits[T][E] = x Wr^T (+ offsets), bf16 x bf16 -> fp32 on tcgen05
-//   topk        : top-k per token, softmax over the k
+//   topk        : top-k per token, softmax over the k; the same warp writes the token's row
+//                 with K permuted inside every 8-element chunk to the order the Q4 unpack
+//                 produces (0,4,1,5,2,6,3,7), so dequantised weight words are stored without
+//                 a shuffle (a dot product is unchanged when both operands are permuted
+//                 alike), and the shared gate sigmoid(x . g)
 //   scan        : per-expert offsets of the expert-sorted pairs, GEMM work lists
 //   place       : stable bucketing (token order inside an expert) from the top-k blocks'
 //                 per-expert counts and their prefixes over the blocks
@@ -124,7 +124,7 @@ struct GemmArgs {
   int a_rows;                    // rows of one expert matrix (or E for the router)
   int K;                         // reduction length
   int E;
-  const uint16_t *b_src;         // x_perm / h / x
+  const uint16_t *b_src;         // permuted token rows / h / x
   const int32_t *perm;
   const int4 *items;
   const int32_t *n_items_ptr;
@@ -678,16 +678,14 @@ __global__ void __launch_bounds__(Cfg<MODE, RT>::THREADS, 1) grouped_gemm_kernel
 // small kernels around the GEMMs
 // -------------------------------------------------------------------------------------
 
-// x_perm[t][8c + pos(i)] = x[t][8c + i], one warp per token row; with a shared expert the
+// xp[t][8c + pos(i)] = x[t][8c + i] for one token row, by one warp; with a shared expert the
 // same warp forms its gate sigmoid(x . g) from the chunks it reads (sigma[t]).  Lane l takes
 // chunks l, l + 32, ... (8 bf16 each) and accumulates them in that order; the lanes' sums
 // meet in a fixed-order warp sum.
-__global__ void x_perm_kernel(const uint16_t *__restrict__ x, uint16_t *__restrict__ xp, int T,
-                              int H, const uint16_t *__restrict__ g, float *__restrict__ sigma) {
-  pdl_enter();
+__device__ __forceinline__ void permute_token_row(const uint16_t *__restrict__ x, uint16_t *__restrict__ xp,
+                                                  int t, int H, const uint16_t *__restrict__ g,
+                                                  float *__restrict__ sigma) {
   const int lane = threadIdx.x & 31;
-  const int t = blockIdx.x * ((int)blockDim.x / 32) + ((int)threadIdx.x >> 5);
-  if (t >= T) return;
   const uint4 *xr = reinterpret_cast<const uint4 *>(x + (size_t)t * H);
   const uint4 *gr = reinterpret_cast<const uint4 *>(g);
   uint4 *pr = reinterpret_cast<uint4 *>(xp + (size_t)t * H);
@@ -734,14 +732,21 @@ struct TopkArgs {
   int32_t *ctab;  // [gridDim.x][E]: the block's selection count per expert
   int32_t *out_idx;
   float *out_w;
+  // the token rows in the permuted K order, and the shared gate (g NULL: no shared expert)
+  const uint16_t *x;
+  uint16_t *xp;
+  const uint16_t *g;
+  float *sigma;
+  int H;
 };
 
 // One warp per token: logits = fixed-order sum of the router GEMM's K-split partials plus
 // the per-expert offsets, held in registers (EC per lane); the k largest (logit desc, index
-// asc); softmax over the k.  The block's selections are counted
-// per expert in shared memory and written to the count table (every expert, zeros included):
-// the scan turns each expert's row into block prefixes, so the bucketing is stable without a
-// global atomic per selection (a skewed router sends most tokens to the same experts).
+// asc); softmax over the k.  The block's selections are counted per expert in shared memory
+// and written to the count table (every expert, zeros included): the scan and the placement
+// turn the counts into block prefixes, so the bucketing is stable without a global atomic per
+// selection (a skewed router sends most tokens to the same experts).  The warp also writes
+// its token's row in the permuted K order for the gate/up GEMM and the shared gate.
 constexpr int kTopkTokens = 16;  // tokens (warps) per block
 constexpr int kMaxTopK = 16;     // the API's top-k limit
 template <int EC>
@@ -752,6 +757,7 @@ __global__ void __launch_bounds__(32 * kTopkTokens) topk_prefill_kernel(TopkArgs
   __syncthreads();
   const int lane = threadIdx.x & 31;
   const int t = blockIdx.x * kTopkTokens + (threadIdx.x >> 5);
+  if (t < a.T) permute_token_row(a.x, a.xp, t, a.H, a.g, a.sigma);
   if (t < a.T) {
   // every partial logit of the lane is loaded before any is summed (the split count is at most
   // kRouterSplit(H) = 4), then the partials are summed in split order
@@ -1256,7 +1262,7 @@ static bool router8(const lily_q4_moe_layer &L) { return L.router_bits == 8; }
 static bool shared8(const lily_q4_moe_layer &L) { return L.has_shared && L.shared_bits == 8; }
 
 int prefill_launch_count(const lily_q4_moe_layer &L) {
-  return 8 + (router8(L) ? 2 : 0) + (shared8(L) ? 3 : 0);
+  return 7 + (router8(L) ? 2 : 0) + (shared8(L) ? 3 : 0);
 }
 
 // -------------------------------------------------------------------------------------
@@ -1377,12 +1383,6 @@ int launch_moe_prefill(const lily_q4_moe_layer &L, const uint16_t *x, int T, uin
   // Every launch below is a programmatic dependent of the one before it (launch_pdl): set-up
   // overlaps the previous kernel's tail, and each kernel waits for that kernel's completion
   // before it reads or writes anything the chain shares.
-  // token permutation, and the shared expert's gate (one warp per token)
-  const uint16_t *sgate = L.has_shared ? L.shared_gate : nullptr;
-  if (launch_pdl(x_perm_kernel, dim3((T + 7) / 8), dim3(256), 0, st, x, xperm, T, H, sgate, sigma) !=
-      cudaSuccess)
-    return LILY_Q4_ERR_CUDA;
-
   // router GEMM (an 8-bit router in its exact bf16 form, the token rows widened to match)
   const uint16_t *ra_a = L.router, *ra_b = x;
   if (router8(L)) {
@@ -1412,7 +1412,9 @@ int launch_moe_prefill(const lily_q4_moe_layer &L, const uint16_t *x, int T, uin
   int rc = launch_gemm<kRouter>(ra, ra.n_items_static < sms ? ra.n_items_static : sms, st);
   if (rc != LILY_Q4_OK) return rc;
 
-  TopkArgs ta{logits, L.router_bias, ra.ksplit, T, E, k, idx, p, ctab, topk_idx, topk_w};
+  const uint16_t *sgate = L.has_shared ? L.shared_gate : nullptr;
+  TopkArgs ta{logits, L.router_bias, ra.ksplit, T, E, k, idx, p, ctab, topk_idx, topk_w,
+              x, xperm, sgate, sigma, H};
   const dim3 tk_grid(nbk), tk_block(32 * kTopkTokens);
   cudaError_t ce = E <= 256   ? launch_pdl(topk_prefill_kernel<8>, tk_grid, tk_block, 0, st, ta)
                    : E <= 512 ? launch_pdl(topk_prefill_kernel<16>, tk_grid, tk_block, 0, st, ta)

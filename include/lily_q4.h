@@ -240,7 +240,7 @@ LILY_Q4_API size_t lily_q4_gemv_argmax_workspace_bytes(int32_t N, int32_t K);
  * (prefill = 1) call enqueues for this layer and T; 0 when the arguments are invalid.
  * Decode uses one launch when its single-launch kernel covers the shapes and batch (one
  * block per SM, enqueued as a programmatic dependent of the previous kernel on the
- * stream), three launches otherwise (four with an 8-bit shared expert).  Prefill uses 8
+ * stream), three launches otherwise (four with an 8-bit shared expert).  Prefill uses 7
  * launches, plus 2 that prepare an 8-bit router and 3 that prepare an 8-bit shared expert. */
 LILY_Q4_API int lily_q4_moe_launches(const lily_q4_moe_layer *layer, int32_t T, int32_t prefill);
 

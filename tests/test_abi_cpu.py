@@ -118,8 +118,8 @@ def test_8bit_layer_argument_errors(lib):
     L.router_q8 = q4.lily_q4_mat(FAKE, FAKE + 4096, FAKE + 8192)
     L.router = None                                                        # the bf16 router is then unused
     assert _decode(lib, L, T=0) == q4.OK
-    # prefill takes it: 8 launches plus two that prepare the 8-bit router's exact bf16 form
-    assert lib.lily_q4_moe_launches(C.byref(L), 4, 1) == 10
+    # prefill takes it: 7 launches plus two that prepare the 8-bit router's exact bf16 form
+    assert lib.lily_q4_moe_launches(C.byref(L), 4, 1) == 9
     assert lib.lily_q4_moe_prefill(C.byref(L), None, 1, None, None, None, None, 0, None) == q4.ERR_INVALID_ARG
 
 
