@@ -47,6 +47,8 @@ def run_prefill(torch, dev, dl, x_bits, ws=None):
     (2048, 4, 2, 512, True, False, 1),      # a single token
     (256, 64, 6, 1024, True, True, 200),
     (256, 32, 8, 128, True, False, 8192),   # the largest chunk: selections not staged in bucketing
+    (256, 1024, 16, 128, True, True, 100),  # most experts, largest k: one count-table group
+    (256, 512, 4, 128, False, True, 2100),  # two groups of 72 top-k blocks (segments read in chunks)
 ])
 def test_shapes(torch_dev, H, E, k, I, shared, bias, T):
     torch, dev = torch_dev
